@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Throughput of the Qwen3-0.6B-shaped decoder step on one GB300 (or N replicas).
+
+Headline workload (the serving configuration): bf16 weights, f16 paged KV
+cache (16-token blocks), fp32 accumulation; 32 sequences preloaded with
+uniform-random contexts of distinct lengths 1024..2048 by a real prefill, then
+K greedy decode steps at batch 32 (each step feeds the previous step's argmax
+ids).  `value` = decode tokens/s with every input resident in HBM; the same
+run also reports batch-1 decode (context 2048) and a chunked prefill of
+4 x 4096 tokens in 512-token chunks.  Weights are random-init N(0, 0.02).
+
+Every timed step reads 1.19 GB of weights plus the KV cache (5.6+ GB at batch
+32), far larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch with torch.distributed.run: each rank runs an independent
+replica on its own GPU (the step has no exchange), timing is max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s (batch 1/32) & prefill tokens/s at 0.6B shape; % HBM/TC roofline"
+WORKLOAD = ("qwen3-0.6B-shape decoder (596,049,920 params), bf16 weights / f16 paged KV (block 16) / fp32 accum; "
+            "greedy decode at batch 32, contexts 1024..2048 (distinct) preloaded by prefill")
+KV_BYTES_PER_CTX_TOKEN_LAYER = 8 * 128 * 2 * 2  # K and V, 8 KV heads x 128, f16
+WEIGHT_BYTES_BF16 = 1_192_099_840  # 596,049,920 params x 2 bytes (tied head read once per step)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class Clocks:
+    """Sample SM clocks and throttle reasons with nvidia-smi during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.3)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+
+def build_model(shape, weights, max_positions, max_tokens, max_seqs, n_blocks):
+    from decoder_qwen3_step_gb300 import dec
+    from decoder_qwen3_step_gb300.runtime import Decoder
+
+    return Decoder(shape, weights, mode=dec.DEC_BF16_F16KV, max_positions=max_positions, max_tokens=max_tokens,
+                   max_seqs=max_seqs, n_blocks=n_blocks)
+
+
+def profile_classes(m, classes, on):
+    for c in classes:
+        m.L.dec_profile_enable(m.handle, c, 1 if on else 0)
+
+
+def read_profile(m, cls):
+    ms, n = C.c_double(), C.c_int64()
+    m.L.dec_profile_read(m.handle, cls, C.byref(ms), C.byref(n))
+    return ms.value, n.value
+
+
+def launches(m):
+    n = C.c_int64()
+    m.L.dec_launch_count(m.handle, C.byref(n))
+    return n.value
+
+
+def our_arm(args, rank, world):
+    import torch
+
+    from decoder_qwen3_step_gb300 import dec, inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    shape = inputs.SHAPES["qwen3_0p6b"]
+    S = 32
+    lens = inputs.serving_context_lengths(S)
+    e2e_steps = max(8, args.steps // 4)
+    b1_steps = max(32, args.steps)
+    # positions every sequence may reach: warmup, 2 profiled steps, timed, e2e, batch-1 (last sequence only)
+    extra = args.warmup + 2 + args.steps + e2e_steps + 3 + b1_steps + 16
+    max_positions = max(((max(lens) + extra + 15) // 16) * 16, 4096 + 64)
+    weights = inputs.make_weights(shape)
+    blocks_needed = sum((L + extra) // 16 + 1 for L in lens) + 4 * (4096 // 16 + 2) + 200
+    m = build_model(shape, weights, max_positions, 8192, 64, blocks_needed)
+    del weights
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    # ---- preload: every sequence's context by a real prefill (rows: last token) ----
+    ctx_ids = [inputs.make_ids(shape["vocab"], 2048, seed=100 + s)[:lens[s]] for s in range(S)]
+    tables = [m.blocks_for(L + extra) for L in lens]
+    group = 4
+    first = []
+    for g in range(0, S, group):
+        _, am = m.prefill([(ctx_ids[s], 0, tables[s]) for s in range(g, g + group)], rows=dec.DEC_ROWS_LAST)
+        first.append(am)
+    next_ids = torch.cat(first).to(torch.int32)
+    torch.cuda.synchronize()
+    pos = list(lens)
+
+    V = shape["vocab"]
+    logits = torch.empty((S, V), dtype=torch.float32, device=dev)
+    ids_buf = [torch.empty((S,), dtype=torch.int32, device=dev) for _ in range(2)]
+    ids_buf[0].copy_(next_ids)
+
+    def decode_step(i, batch_pos, seqs_idx, buf_in, buf_out):
+        m.decode([([0], batch_pos[j], tables[s]) for j, s in enumerate(seqs_idx)], device_ids=buf_in,
+                 out=(logits[:len(seqs_idx)], buf_out))
+
+    # warmup
+    for i in range(args.warmup):
+        decode_step(i, pos, range(S), ids_buf[i & 1], ids_buf[(i + 1) & 1])
+        pos = [p + 1 for p in pos]
+    torch.cuda.synchronize()
+    launches(m)
+    # which kernel class dominates the step (short events pass, untimed)
+    profile_classes(m, range(len(dec.KERNEL_CLASSES)), True)
+    for i in range(2):
+        decode_step(i, pos, range(S), ids_buf[(args.warmup + i) & 1], ids_buf[(args.warmup + i + 1) & 1])
+        pos = [p + 1 for p in pos]
+    shares = {name: read_profile(m, c)[0] for c, name in enumerate(dec.KERNEL_CLASSES)}
+    profile_classes(m, range(len(dec.KERNEL_CLASSES)), False)
+    dom_name = max(shares, key=shares.get)
+    dom = dec.KERNEL_CLASSES.index(dom_name)
+    launches(m)
+
+    # ---- timed region: K decode steps at batch 32 ----
+    ctx_sum = 0
+    profile_classes(m, [dom], True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    base = args.warmup + 2
+    with Clocks(dev.index) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            ctx_sum += sum(p + 1 for p in pos)
+            decode_step(i, pos, range(S), ids_buf[(base + i) & 1], ids_buf[(base + i + 1) & 1])
+            pos = [p + 1 for p in pos]
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    n_launch = launches(m)
+    dom_ms, dom_n = read_profile(m, dom)
+    profile_classes(m, [dom], False)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = S * args.steps * world
+    value = tokens / (ms / 1e3)
+
+    # roofline of the dominant kernel class: algorithmic bytes per launch / event time per launch
+    L = shape["n_layers"]
+    per_launch_s = (dom_ms / max(dom_n, 1)) / 1e3
+    if dom_name == "attn":
+        alg_bytes = ctx_sum * KV_BYTES_PER_CTX_TOKEN_LAYER / args.steps  # per launch (one layer)
+        unit_note = "4,096 B of K+V per context token per layer; units = sum of the 32 context lengths"
+    else:
+        alg_bytes = _class_weight_bytes(dom_name, shape) + 0.0
+        unit_note = "weight bytes of this projection (bf16), read once per launch"
+    achieved = alg_bytes / per_launch_s / 1e9
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                "peak_source": pk["source"], "bytes_per_launch": int(alg_bytes), "per_unit": unit_note,
+                "launch_us": round(per_launch_s * 1e6, 2), "launches": dom_n,
+                "step_share": {k: round(v / max(sum(shares.values()), 1e-9), 4) for k, v in shares.items()}}
+
+    # ---- e2e: host ids in, host ids out, every step ----
+    host_ids = next_ids.cpu().numpy().astype(np.int32)
+    pinned_out = torch.empty((S,), dtype=torch.int32, pin_memory=True)
+    torch.cuda.synchronize()
+    h2d = 0
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        seqs = [([int(host_ids[s])], pos[s], tables[s]) for s in range(S)]
+        m.decode(seqs, out=(logits, ids_buf[0]))
+        pinned_out.copy_(ids_buf[0], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        host_ids = pinned_out.numpy().copy()
+        pos = [p + 1 for p in pos]
+    e2e_s = time.perf_counter() - t0
+    MB = (max_positions + 15) // 16
+    h2d = 4 * (3 * S + (S + 1) + S + S + S * MB)
+    e2e = {"value": round(S * e2e_steps * world / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": 4 * S, "steps": e2e_steps}
+
+    # ---- batch-1 decode at context 2048 (the longest sequence) ----
+    s1 = S - 1
+    b1_ids = [torch.empty((1,), dtype=torch.int32, device=dev) for _ in range(2)]
+    b1_ids[0].copy_(ids_buf[0][s1:s1 + 1])
+    lg1 = torch.empty((1, V), dtype=torch.float32, device=dev)
+    p1 = pos[s1]
+    for i in range(3):
+        m.decode([([0], p1, tables[s1])], device_ids=b1_ids[i & 1], out=(lg1, b1_ids[(i + 1) & 1]))
+        p1 += 1
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    b1_ctx = 0
+    for i in range(b1_steps):
+        b1_ctx += p1 + 1
+        m.decode([([0], p1, tables[s1])], device_ids=b1_ids[(i + 3) & 1], out=(lg1, b1_ids[(i + 4) & 1]))
+        p1 += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    b1_ms = e0.elapsed_time(e1) / b1_steps
+    b1_bytes = WEIGHT_BYTES_BF16 + (b1_ctx / b1_steps) * KV_BYTES_PER_CTX_TOKEN_LAYER * L
+    decode_b1 = {"tokens_per_s": round(1e3 / b1_ms, 1), "ms_per_token": round(b1_ms, 4),
+                 "hbm_frac": round(b1_bytes / (b1_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                 "bytes_per_token": int(b1_bytes), "context": p1}
+
+    # ---- chunked prefill: 4 x 4096 tokens, 512-token chunks interleaved across sequences ----
+    pf_ids = [inputs.make_ids(V, 4096, seed=200 + s) for s in range(4)]
+    pf_tab = [m.blocks_for(4096) for _ in range(4)]
+
+    def prefill_pass():
+        for k in range(8):
+            m.prefill([(pf_ids[s][512 * k:512 * (k + 1)], 512 * k, pf_tab[s]) for s in range(4)],
+                      rows=dec.DEC_ROWS_LAST, out=(logits[:4], ids_buf[1][:4]))
+
+    prefill_pass()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    prefill_pass()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pf_ms = e0.elapsed_time(e1)
+    # layer projections of 16,384 tokens + the LM head on the 32 chunk-last rows
+    proj_flops = 2 * 16384 * 440_401_920 + 2 * 32 * 155_582_464
+    prefill = {"tokens_per_s": round(16384 / (pf_ms / 1e3), 1), "ms": round(pf_ms, 3),
+               "projection_tflops": round(proj_flops / (pf_ms / 1e3) / 1e12, 2)}
+
+    status = m.device_status()
+    m.close()
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": S, "context_lengths": [min(lens), max(lens)],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (1.19 GB weights + >5.6 GB KV read per step); no flush"},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": n_launch, "clocks": clk.summary(),
+        "decode_b1": decode_b1, "prefill_4x4096": prefill, "device_status": status,
+    }
+
+
+def _class_weight_bytes(name, shape):
+    d, H, Hkv, D, F, V = (shape[k] for k in ("d_model", "n_heads", "n_kv_heads", "head_dim", "ff_hidden", "vocab"))
+    return 2 * {"qkv": (H + 2 * Hkv) * D * d, "oproj": d * H * D, "gateup": 2 * F * d, "down": d * F,
+                "lmhead": V * d}.get(name, 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# the oracle on host cores: the CPU baseline and the reference arm
+# ------------------------------------------------------------------------------------------------
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+def oracle_decode_sample(budget_s=12.0, n_sample=4):
+    """Oracle decode steps on a sample of the headline workload's sequences.
+
+    The sampled sequences keep their context lengths; their float64 caches are
+    filled with seeded random K/V (the cost of a decode step does not depend
+    on the cached values), so no prefill is timed.  Steps run until the
+    budget is spent; returns tokens/s and a description."""
+    from decoder_qwen3_step_gb300 import inputs
+    from oracle.model import DecoderConfig, Oracle
+
+    shape = inputs.SHAPES["qwen3_0p6b"]
+    lens = inputs.serving_context_lengths(32)
+    pick = [lens[i] for i in np.linspace(0, 31, n_sample).astype(int)]
+    cfg = DecoderConfig(**shape, max_positions=max(pick) + 64)
+    orc = Oracle(cfg, inputs.make_weights(shape), mode="bf16")
+    rng = np.random.default_rng(5)
+    caches = []
+    for L in pick:
+        c = orc.new_cache(L + 64)
+        for l in range(cfg.n_layers):
+            c.k[l][:L] = rng.standard_normal((L, cfg.n_kv_heads, cfg.head_dim))
+            c.v[l][:L] = rng.standard_normal((L, cfg.n_kv_heads, cfg.head_dim))
+            c.written[l][:L] = True
+        caches.append(c)
+    tokens, t0 = 0, time.perf_counter()
+    step = 0
+    while True:
+        for c, L in zip(caches, pick):
+            orc.forward(c, [step % cfg.vocab], L + step)
+            tokens += 1
+        step += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return tokens / dt, {"kind": "oracle", "cores": blas_threads(),
+                         "sample": f"{step} float64 decode step(s) of {n_sample} of the 32 sequences "
+                                   f"(contexts {pick}), caches filled with seeded random K/V; {dt:.1f} s"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    budget = min(25.0, max(8.0, 2.0 * args.steps))
+    v, info = oracle_decode_sample(budget_s=budget)
+    info["value"] = round(v, 3)
+    return {"metric": METRIC, "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "batch": 32, "parallelism": "host cores"},
+            "cpu_baseline": info,
+            "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+    else:
+        line = our_arm(args, rank, world)
+        if rank == 0 and not args.no_cpu_baseline:
+            v, info = oracle_decode_sample()
+            info["value"] = round(v, 3)
+            info["unit"] = "tokens/s"
+            line["cpu_baseline"] = info
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,697 @@
+// api.cu - the C ABI of libdec (declared in include/dec.h): config checks,
+// weight packing, the paged KV pool's host allocator, batch validation,
+// per-step metadata staging and the launch sequence of one decoder step.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <array>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/dec.h"
+#include "common.cuh"
+#include "launch.h"
+
+using namespace dec;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define DEC_CUDA(call)                                                                  \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess) return fail(DEC_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int act_bytes(const dec_config& c) { return c.mode == DEC_FP32 ? 4 : 2; }
+int kv_bytes(const dec_config& c) { return c.mode == DEC_FP32 ? 4 : 2; }
+int qkv_rows(const dec_config& c) { return (c.n_heads + 2 * c.n_kv_heads) * c.head_dim; }
+int max_blocks_of(const dec_config& c) { return (c.max_positions + c.block_tokens - 1) / c.block_tokens; }
+int max_chunks_of(const dec_config& c) { return (c.max_positions + kDecodeChunk - 1) / kDecodeChunk; }
+
+int check_config(const dec_config* c) {
+  if (!c) return fail(DEC_EINVAL, "config is NULL");
+  if (c->mode != DEC_FP32 && c->mode != DEC_BF16_F16KV) return fail(DEC_EINVAL, "unknown mode %d", c->mode);
+  if (c->rope_scaling) return fail(DEC_EINVAL, "unsupported: scaled RoPE");
+  if (c->sliding_window) return fail(DEC_EINVAL, "unsupported: sliding-window attention");
+  if (c->attention_bias) return fail(DEC_EINVAL, "unsupported: attention biases");
+  if (c->qk_norm != 1 || c->rope_split != 1 || c->tied != 1)
+    return fail(DEC_EINVAL, "unsupported: qk_norm, rope_split and tied must all be 1");
+  if (c->vocab <= 0 || c->d_model <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 ||
+      c->head_dim <= 0 || c->ff_hidden <= 0 || c->max_positions <= 0)
+    return fail(DEC_EINVAL, "dimensions must be positive");
+  if (c->n_heads % c->n_kv_heads) return fail(DEC_EINVAL, "n_heads must be a multiple of n_kv_heads");
+  const int G = c->n_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return fail(DEC_EINVAL, "query heads per KV head must be 1, 2 or 4");
+  if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
+    return fail(DEC_EINVAL, "head_dim must be 32, 64 or 128");
+  if (c->d_model % 32) return fail(DEC_EINVAL, "d_model must be a multiple of 32");
+  if (c->ff_hidden % 16) return fail(DEC_EINVAL, "ff_hidden must be a multiple of 16");
+  if (c->vocab % 16) return fail(DEC_EINVAL, "vocab must be a multiple of 16");
+  if (c->block_tokens != 16) return fail(DEC_EINVAL, "block_tokens must be 16");
+  if (!(c->rope_base > 1.0) || !(c->rms_eps > 0.0)) return fail(DEC_EINVAL, "rope_base must be > 1, rms_eps > 0");
+  if (c->max_positions > (1 << 20)) return fail(DEC_EINVAL, "max_positions too large");
+  return DEC_OK;
+}
+
+// Packed weight buffer: RoPE table, embedding, final gain, then per layer
+// gains and the fused matrices [Wq;Wk;Wv], Wo, gate/up interleaved by 8 rows, Wd.
+struct PackedLayout {
+  size_t rope, embed, final_norm;
+  size_t attn_norm, mlp_norm, q_norm, k_norm, wqkv, wo, wgu, wd;  // offsets within a layer
+  size_t layer0, layer_stride, total;
+};
+
+PackedLayout packed_layout(const dec_config& c) {
+  PackedLayout L{};
+  const size_t wb = c.mode == DEC_FP32 ? 4 : 2;
+  const size_t d = c.d_model, D = c.head_dim, F = c.ff_hidden, HD = (size_t)c.n_heads * D;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  L.rope = take((size_t)c.max_positions * (D / 2) * 2 * sizeof(float));
+  L.embed = take((size_t)c.vocab * d * wb);
+  L.final_norm = take(d * sizeof(float));
+  L.layer0 = off;
+  size_t lo = 0;
+  auto ltake = [&](size_t bytes) { size_t o = lo; lo = align256(lo + bytes); return o; };
+  L.attn_norm = ltake(d * 4);
+  L.mlp_norm = ltake(d * 4);
+  L.q_norm = ltake(D * 4);
+  L.k_norm = ltake(D * 4);
+  L.wqkv = ltake((size_t)qkv_rows(c) * d * wb);
+  L.wo = ltake(d * HD * wb);
+  L.wgu = ltake(2 * F * d * wb);
+  L.wd = ltake(d * F * wb);
+  L.layer_stride = lo;
+  L.total = L.layer0 + (size_t)c.n_layers * lo;
+  return L;
+}
+
+struct WsLayout {
+  size_t X, XN, SSQ, RAW, Q, ATT, ACT, PART, META, KEYS, ERR, total;
+  size_t meta_ints;
+};
+
+WsLayout ws_layout(const dec_config& c, int T, int S) {
+  WsLayout L{};
+  const size_t a = act_bytes(c), d = c.d_model, HD = (size_t)c.n_heads * c.head_dim;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  L.X = take((size_t)T * d * 4);
+  L.XN = take((size_t)T * d * a);
+  L.SSQ = take((size_t)T * (d / kSsqChunk) * 4);
+  L.RAW = take((size_t)T * qkv_rows(c) * 4);
+  L.Q = take((size_t)T * HD * 4);
+  L.ATT = take((size_t)T * HD * a);
+  L.ACT = take((size_t)T * c.ff_hidden * a);
+  L.PART = take((size_t)S * c.n_heads * max_chunks_of(c) * (c.head_dim + 2) * 4);
+  // ids, tok_pos, tok_seq, row_tok [T]; seq_start [S+1]; seq_ctx [S]; tables [S*MB]; work [3*(T+S)]
+  L.meta_ints = 4 * (size_t)T + 2 * (size_t)S + 1 + (size_t)S * max_blocks_of(c) + 3 * ((size_t)T + S);
+  L.META = take(L.meta_ints * 4);
+  L.KEYS = take((size_t)T * 8);
+  L.ERR = take(64);
+  L.total = off;
+  return L;
+}
+
+constexpr int kStageSlots = 4;
+
+}  // namespace
+
+struct dec_pool {
+  dec_config cfg;
+  int n_blocks;
+  void* slabs;
+  std::vector<int32_t> refs;
+  std::vector<int32_t> free_list;  // stack; top = next id handed out
+};
+
+struct dec_model {
+  dec_config cfg;
+  PackedLayout pl;
+  WsLayout wl;
+  char* packed;
+  char* ws;
+  int Tmax, Smax, MB, NCH;
+  int device;
+  int32_t* stage[kStageSlots];
+  cudaEvent_t stage_ev[kStageSlots];
+  int stage_next;
+  float* dump;
+  size_t dump_floats;
+  cudaStream_t last_stream;
+  // profiling: event pairs around the launches of enabled kernel classes
+  struct ProfRec { cudaEvent_t a, b; int cls; };
+  bool prof_on[DEC_K_COUNT];
+  std::vector<ProfRec> prof_pending;
+  std::vector<cudaEvent_t> ev_free;
+  double prof_ms[DEC_K_COUNT];
+  int64_t prof_n[DEC_K_COUNT];
+  int64_t launches;
+};
+
+namespace {
+
+cudaEvent_t take_event(dec_model* m) {
+  if (!m->ev_free.empty()) {
+    cudaEvent_t e = m->ev_free.back();
+    m->ev_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch one kernel (expr returns cudaError_t) of class cls on stream st,
+// bracketed by CUDA events when that class is being profiled.
+template <typename F>
+int timed_launch(dec_model* m, int cls, cudaStream_t st, F&& fn, const char* what) {
+  cudaEvent_t a = nullptr;
+  if (m->prof_on[cls]) {
+    a = take_event(m);
+    cudaEventRecord(a, st);
+  }
+  cudaError_t e = fn();
+  if (e != cudaSuccess) return fail(DEC_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+  if (a) {
+    cudaEvent_t b = take_event(m);
+    cudaEventRecord(b, st);
+    m->prof_pending.push_back({a, b, cls});
+  }
+  ++m->launches;
+  return DEC_OK;
+}
+
+}  // namespace
+
+#define DEC_LAUNCH(cls, expr)                                                   \
+  do {                                                                          \
+    int rc_ = timed_launch(m, cls, st, [&]() { return (expr); }, #expr);        \
+    if (rc_) return rc_;                                                        \
+  } while (0)
+
+extern "C" {
+
+const char* dec_last_error(void) { return g_err.c_str(); }
+const char* dec_version(void) { return "libdec 0.1 (sm_103a)"; }
+
+int dec_config_check(const dec_config* cfg) { return check_config(cfg); }
+
+int dec_weights_bytes(const dec_config* cfg, size_t* bytes) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!bytes) return fail(DEC_EINVAL, "bytes is NULL");
+  *bytes = packed_layout(*cfg).total;
+  return DEC_OK;
+}
+
+int dec_workspace_bytes(const dec_config* cfg, int32_t max_tokens, int32_t max_seqs, size_t* bytes) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!bytes) return fail(DEC_EINVAL, "bytes is NULL");
+  if (max_tokens < 1 || max_seqs < 1 || max_seqs > max_tokens)
+    return fail(DEC_EINVAL, "need 1 <= max_seqs <= max_tokens");
+  *bytes = ws_layout(*cfg, max_tokens, max_seqs).total;
+  return DEC_OK;
+}
+
+int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, size_t packed_bytes, void* workspace,
+               size_t workspace_bytes, int32_t max_tokens, int32_t max_seqs, void* stream, dec_model** out) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!w || !packed_buf || !workspace || !out) return fail(DEC_EINVAL, "NULL argument");
+  if (max_tokens < 1 || max_seqs < 1 || max_seqs > max_tokens)
+    return fail(DEC_EINVAL, "need 1 <= max_seqs <= max_tokens");
+  const dec_config& c = *cfg;
+  PackedLayout pl = packed_layout(c);
+  WsLayout wl = ws_layout(c, max_tokens, max_seqs);
+  if (packed_bytes < pl.total) return fail(DEC_EINVAL, "packed buffer too small: %zu < %zu", packed_bytes, pl.total);
+  if (workspace_bytes < wl.total) return fail(DEC_EINVAL, "workspace too small: %zu < %zu", workspace_bytes, wl.total);
+  if (((uintptr_t)packed_buf | (uintptr_t)workspace) & 255) return fail(DEC_EINVAL, "buffers must be 256-byte aligned");
+  if (!w->embed || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->q_norm || !w->k_norm ||
+      !w->wo || !w->mlp_norm || !w->w_gate || !w->w_up || !w->w_down)
+    return fail(DEC_EINVAL, "missing weight pointer");
+  for (int l = 0; l < c.n_layers; ++l)
+    if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->q_norm[l] || !w->k_norm[l] || !w->wo[l] ||
+        !w->mlp_norm[l] || !w->w_gate[l] || !w->w_up[l] || !w->w_down[l])
+      return fail(DEC_EINVAL, "missing weight pointer in layer %d", l);
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool bf = c.mode == DEC_BF16_F16KV;
+  char* P = (char*)packed_buf;
+  const int d = c.d_model, D = c.head_dim, F = c.ff_hidden, H = c.n_heads, Hkv = c.n_kv_heads;
+  const size_t wb = bf ? 2 : 4;
+
+  // RoPE table in double precision, rounded once to fp32: phi = pos * base^(-2j/D)
+  // (1bit-MONSTER "Byte-identical", "The rope table that was too accurate").
+  {
+    std::vector<float> tab((size_t)c.max_positions * (D / 2) * 2);
+    std::vector<double> theta(D / 2);
+    for (int j = 0; j < D / 2; ++j) theta[j] = std::pow(c.rope_base, -2.0 * j / D);
+    for (int p = 0; p < c.max_positions; ++p)
+      for (int j = 0; j < D / 2; ++j) {
+        const double phi = (double)p * theta[j];
+        tab[((size_t)p * (D / 2) + j) * 2] = (float)std::cos(phi);
+        tab[((size_t)p * (D / 2) + j) * 2 + 1] = (float)std::sin(phi);
+      }
+    DEC_CUDA(cudaMemcpyAsync(P + pl.rope, tab.data(), tab.size() * sizeof(float), cudaMemcpyHostToDevice, s));
+    DEC_CUDA(cudaStreamSynchronize(s));
+  }
+  DEC_CUDA(launch_pack(P + pl.embed, w->embed, c.vocab, d, PACK_IDENTITY, bf, s));
+  DEC_CUDA(cudaMemcpyAsync(P + pl.final_norm, w->final_norm, d * 4, cudaMemcpyDeviceToDevice, s));
+  for (int l = 0; l < c.n_layers; ++l) {
+    char* Lb = P + pl.layer0 + (size_t)l * pl.layer_stride;
+    DEC_CUDA(cudaMemcpyAsync(Lb + pl.attn_norm, w->attn_norm[l], d * 4, cudaMemcpyDeviceToDevice, s));
+    DEC_CUDA(cudaMemcpyAsync(Lb + pl.mlp_norm, w->mlp_norm[l], d * 4, cudaMemcpyDeviceToDevice, s));
+    DEC_CUDA(cudaMemcpyAsync(Lb + pl.q_norm, w->q_norm[l], D * 4, cudaMemcpyDeviceToDevice, s));
+    DEC_CUDA(cudaMemcpyAsync(Lb + pl.k_norm, w->k_norm[l], D * 4, cudaMemcpyDeviceToDevice, s));
+    char* qkv = Lb + pl.wqkv;
+    DEC_CUDA(launch_pack(qkv, w->wq[l], H * D, d, PACK_IDENTITY, bf, s));
+    DEC_CUDA(launch_pack(qkv + (size_t)H * D * d * wb, w->wk[l], Hkv * D, d, PACK_IDENTITY, bf, s));
+    DEC_CUDA(launch_pack(qkv + (size_t)(H + Hkv) * D * d * wb, w->wv[l], Hkv * D, d, PACK_IDENTITY, bf, s));
+    DEC_CUDA(launch_pack(Lb + pl.wo, w->wo[l], d, H * D, PACK_IDENTITY, bf, s));
+    DEC_CUDA(launch_pack(Lb + pl.wgu, w->w_gate[l], F, d, PACK_GATE, bf, s));
+    DEC_CUDA(launch_pack(Lb + pl.wgu, w->w_up[l], F, d, PACK_UP, bf, s));
+    DEC_CUDA(launch_pack(Lb + pl.wd, w->w_down[l], d, F, PACK_IDENTITY, bf, s));
+  }
+  DEC_CUDA(cudaMemsetAsync((char*)workspace + wl.ERR, 0, 64, s));
+  DEC_CUDA(cudaStreamSynchronize(s));
+
+  dec_model* m = new dec_model();
+  m->cfg = c;
+  m->pl = pl;
+  m->wl = wl;
+  m->packed = P;
+  m->ws = (char*)workspace;
+  m->Tmax = max_tokens;
+  m->Smax = max_seqs;
+  m->MB = max_blocks_of(c);
+  m->NCH = max_chunks_of(c);
+  cudaGetDevice(&m->device);
+  m->stage_next = 0;
+  m->dump = nullptr;
+  m->dump_floats = 0;
+  m->last_stream = s;
+  for (int i = 0; i < DEC_K_COUNT; ++i) {
+    m->prof_on[i] = false;
+    m->prof_ms[i] = 0.0;
+    m->prof_n[i] = 0;
+  }
+  m->launches = 0;
+  for (int i = 0; i < kStageSlots; ++i) {
+    m->stage[i] = nullptr;
+    m->stage_ev[i] = nullptr;
+  }
+  for (int i = 0; i < kStageSlots; ++i) {
+    cudaError_t e1 = cudaHostAlloc((void**)&m->stage[i], wl.meta_ints * 4, cudaHostAllocDefault);
+    cudaError_t e2 = cudaEventCreateWithFlags(&m->stage_ev[i], cudaEventDisableTiming);
+    if (e1 != cudaSuccess || e2 != cudaSuccess) {
+      dec_destroy(m);
+      return fail(DEC_ECUDA, "pinned staging allocation failed");
+    }
+  }
+  *out = m;
+  return DEC_OK;
+}
+
+void dec_destroy(dec_model* m) {
+  if (!m) return;
+  for (int i = 0; i < kStageSlots; ++i) {
+    if (m->stage_ev[i]) {
+      cudaEventSynchronize(m->stage_ev[i]);
+      cudaEventDestroy(m->stage_ev[i]);
+    }
+    if (m->stage[i]) cudaFreeHost(m->stage[i]);
+  }
+  for (auto& r : m->prof_pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : m->ev_free) cudaEventDestroy(e);
+  delete m;
+}
+
+int dec_device_status(dec_model* m, uint32_t* flags) {
+  if (!m || !flags) return fail(DEC_EINVAL, "NULL argument");
+  DEC_CUDA(cudaStreamSynchronize(m->last_stream));
+  uint32_t v = 0;
+  DEC_CUDA(cudaMemcpy(&v, m->ws + m->wl.ERR, 4, cudaMemcpyDeviceToHost));
+  DEC_CUDA(cudaMemset(m->ws + m->wl.ERR, 0, 4));
+  *flags = v;
+  return DEC_OK;
+}
+
+int dec_profile_enable(dec_model* m, int32_t kernel_class, int32_t on) {
+  if (!m || kernel_class < 0 || kernel_class >= DEC_K_COUNT) return fail(DEC_EINVAL, "bad model or kernel class");
+  m->prof_on[kernel_class] = on != 0;
+  return DEC_OK;
+}
+
+int dec_profile_read(dec_model* m, int32_t kernel_class, double* total_ms, int64_t* launches) {
+  if (!m || !total_ms || !launches || kernel_class < 0 || kernel_class >= DEC_K_COUNT)
+    return fail(DEC_EINVAL, "bad arguments");
+  for (auto& r : m->prof_pending) {
+    DEC_CUDA(cudaEventSynchronize(r.b));
+    float ms = 0.f;
+    DEC_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+    m->prof_ms[r.cls] += ms;
+    m->prof_n[r.cls] += 1;
+    m->ev_free.push_back(r.a);
+    m->ev_free.push_back(r.b);
+  }
+  m->prof_pending.clear();
+  *total_ms = m->prof_ms[kernel_class];
+  *launches = m->prof_n[kernel_class];
+  m->prof_ms[kernel_class] = 0.0;
+  m->prof_n[kernel_class] = 0;
+  return DEC_OK;
+}
+
+int dec_launch_count(dec_model* m, int64_t* launches) {
+  if (!m || !launches) return fail(DEC_EINVAL, "bad arguments");
+  *launches = m->launches;
+  m->launches = 0;
+  return DEC_OK;
+}
+
+int dec_set_dump(dec_model* m, float* dump, size_t dump_floats) {
+  if (!m) return fail(DEC_EINVAL, "model is NULL");
+  m->dump = dump;
+  m->dump_floats = dump ? dump_floats : 0;
+  return DEC_OK;
+}
+
+// ---- pool -------------------------------------------------------------------
+
+int dec_pool_bytes(const dec_config* cfg, int32_t n_blocks, size_t* bytes) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!bytes) return fail(DEC_EINVAL, "bytes is NULL");
+  if (n_blocks <= 0) return fail(DEC_EINVAL, "a pool needs at least one block");
+  *bytes = (size_t)n_blocks * cfg->n_layers * 2 * cfg->n_kv_heads * cfg->block_tokens * cfg->head_dim * kv_bytes(*cfg);
+  return DEC_OK;
+}
+
+int dec_pool_create(const dec_config* cfg, int32_t n_blocks, void* slabs, size_t bytes, dec_pool** out) {
+  size_t need = 0;
+  int rc = dec_pool_bytes(cfg, n_blocks, &need);
+  if (rc) return rc;
+  if (!slabs || !out) return fail(DEC_EINVAL, "NULL argument");
+  if (bytes < need) return fail(DEC_EINVAL, "slab buffer too small: %zu < %zu", bytes, need);
+  if ((uintptr_t)slabs & 255) return fail(DEC_EINVAL, "slab buffer must be 256-byte aligned");
+  dec_pool* p = new dec_pool();
+  p->cfg = *cfg;
+  p->n_blocks = n_blocks;
+  p->slabs = slabs;
+  p->refs.assign(n_blocks, 0);
+  p->free_list.resize(n_blocks);
+  for (int i = 0; i < n_blocks; ++i) p->free_list[i] = n_blocks - 1 - i;
+  *out = p;
+  return DEC_OK;
+}
+
+void dec_pool_destroy(dec_pool* p) { delete p; }
+
+int dec_pool_alloc(dec_pool* p, int32_t n, int32_t* ids) {
+  if (!p || (!ids && n > 0)) return fail(DEC_EINVAL, "NULL argument");
+  if (n < 0) return fail(DEC_EINVAL, "negative block count");
+  if ((size_t)n > p->free_list.size())
+    return fail(DEC_ECAPACITY, "pool exhausted: %d blocks asked, %zu free", n, p->free_list.size());
+  for (int i = 0; i < n; ++i) {
+    ids[i] = p->free_list.back();
+    p->free_list.pop_back();
+    p->refs[ids[i]] = 1;
+  }
+  return DEC_OK;
+}
+
+int dec_pool_retain(dec_pool* p, int32_t id) {
+  if (!p) return fail(DEC_EINVAL, "pool is NULL");
+  if (id < 0 || id >= p->n_blocks || p->refs[id] <= 0) return fail(DEC_EBLOCK, "block %d is not allocated", id);
+  ++p->refs[id];
+  return DEC_OK;
+}
+
+int dec_pool_release(dec_pool* p, int32_t id) {
+  if (!p) return fail(DEC_EINVAL, "pool is NULL");
+  if (id < 0 || id >= p->n_blocks || p->refs[id] <= 0) return fail(DEC_EBLOCK, "block %d is not allocated", id);
+  if (--p->refs[id] == 0) p->free_list.push_back(id);
+  return DEC_OK;
+}
+
+int dec_pool_free_blocks(const dec_pool* p, int32_t* n) {
+  if (!p || !n) return fail(DEC_EINVAL, "NULL argument");
+  *n = (int32_t)p->free_list.size();
+  return DEC_OK;
+}
+
+int dec_pool_refcount(const dec_pool* p, int32_t id, int32_t* refs) {
+  if (!p || !refs) return fail(DEC_EINVAL, "NULL argument");
+  if (id < 0 || id >= p->n_blocks) return fail(DEC_EBLOCK, "block %d outside the pool", id);
+  *refs = p->refs[id];
+  return DEC_OK;
+}
+
+int dec_kv_offset(const dec_pool* p, const int32_t* table, int32_t n_table, int32_t pos, int32_t layer,
+                  int32_t kv_head, int32_t is_v, int64_t* offset) {
+  if (!p || !table || !offset) return fail(DEC_EINVAL, "NULL argument");
+  const dec_config& c = p->cfg;
+  if (pos < 0 || layer < 0 || layer >= c.n_layers || kv_head < 0 || kv_head >= c.n_kv_heads || (is_v != 0 && is_v != 1))
+    return fail(DEC_EINVAL, "bad position, layer, head or slab");
+  const int bi = pos / c.block_tokens;
+  if (bi >= n_table) return fail(DEC_ERANGE, "block table too short for position %d", pos);
+  const int blk = table[bi];
+  if (blk < 0 || blk >= p->n_blocks) return fail(DEC_EBLOCK, "block id %d outside the pool", blk);
+  *offset = kv_offset(layer, blk, is_v, kv_head, pos % c.block_tokens, p->n_blocks, c.n_kv_heads, c.block_tokens,
+                      c.head_dim);
+  return DEC_OK;
+}
+
+// ---- the step ------------------------------------------------------------------
+
+static bool same_shape(const dec_config& a, const dec_config& b) {
+  return a.n_layers == b.n_layers && a.n_kv_heads == b.n_kv_heads && a.head_dim == b.head_dim &&
+         a.block_tokens == b.block_tokens && a.mode == b.mode;
+}
+
+static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_mode, float* logits, int32_t* argmax,
+                    cudaStream_t st, bool decode) {
+  if (!m || !pool || !b || !argmax) return fail(DEC_EINVAL, "NULL argument");
+  const dec_config& c = m->cfg;
+  if (!same_shape(c, pool->cfg)) return fail(DEC_EINVAL, "pool was made for another decoder shape or mode");
+  if (rows_mode != DEC_ROWS_ALL && rows_mode != DEC_ROWS_LAST) return fail(DEC_EINVAL, "bad rows mode");
+  const int S = b->n_seqs, N = b->n_tokens;
+  if (S < 1 || N < 1) return fail(DEC_EINVAL, "empty step: %d sequences, %d tokens", S, N);
+  if (S > m->Smax || N > m->Tmax)
+    return fail(DEC_ERANGE, "step of %d tokens / %d sequences exceeds the workspace (%d / %d)", N, S, m->Tmax, m->Smax);
+  if (decode && N != S) return fail(DEC_EINVAL, "decode takes exactly one token per sequence");
+  if (!b->seq_start || !b->positions || !b->block_table || (!b->ids && !b->ids_device))
+    return fail(DEC_EINVAL, "NULL batch array");
+  if (b->seq_start[0] != 0 || b->seq_start[S] != N) return fail(DEC_EINVAL, "seq_start must run from 0 to n_tokens");
+  const int B = c.block_tokens;
+  int max_nch = 0;
+  for (int s = 0; s < S; ++s) {
+    const int a0 = b->seq_start[s], a1 = b->seq_start[s + 1];
+    if (a1 <= a0) return fail(DEC_EINVAL, "sequence %d has no new tokens", s);
+    const int p0 = b->positions[a0];
+    if (p0 < 0) return fail(DEC_ERANGE, "negative position in sequence %d", s);
+    for (int t = a0; t < a1; ++t) {
+      if (b->positions[t] != p0 + (t - a0))
+        return fail(DEC_ERANGE, "positions of sequence %d are not consecutive", s);
+      if (b->ids && !b->ids_device && (b->ids[t] < 0 || b->ids[t] >= c.vocab))
+        return fail(DEC_EVOCAB, "token id %d outside the vocabulary (%d)", b->ids[t], c.vocab);
+    }
+    const int last = p0 + (a1 - a0) - 1;
+    if (last >= c.max_positions) return fail(DEC_ERANGE, "position %d past the context (%d)", last, c.max_positions);
+    const int nb = last / B + 1;
+    if (nb > b->max_blocks) return fail(DEC_ERANGE, "block table of sequence %d too short for position %d", s, last);
+    for (int i = 0; i < nb; ++i) {
+      const int id = b->block_table[(size_t)s * b->max_blocks + i];
+      if (id < 0 || id >= pool->n_blocks || pool->refs[id] <= 0)
+        return fail(DEC_EBLOCK, "sequence %d names block %d which is not allocated", s, id);
+    }
+    max_nch = std::max(max_nch, (last + kDecodeChunk) / kDecodeChunk);
+  }
+  const int R = rows_mode == DEC_ROWS_ALL ? N : S;
+
+  // ---- metadata: assemble, stage in pinned memory, one host->device copy ----
+  const int MB = m->MB, Tm = m->Tmax, Sm = m->Smax;
+  (void)Tm;
+  (void)Sm;
+  const int G = c.n_heads / c.n_kv_heads;
+  const int QT = prefill_tile_queries(G);
+  const int slot = m->stage_next;
+  m->stage_next = (m->stage_next + 1) % kStageSlots;
+  DEC_CUDA(cudaEventSynchronize(m->stage_ev[slot]));  // the copy that last used this slot has run
+  int32_t* H = m->stage[slot];
+  size_t o = 0;
+  const size_t o_ids = o; o += N;
+  const size_t o_pos = o; o += N;
+  const size_t o_seq = o; o += N;
+  const size_t o_start = o; o += S + 1;
+  const size_t o_ctx = o; o += S;
+  const size_t o_row = o; o += R;
+  const size_t o_tab = o; o += (size_t)S * MB;
+  const size_t o_work = o;
+  for (int s = 0; s < S; ++s) {
+    const int a0 = b->seq_start[s], a1 = b->seq_start[s + 1];
+    for (int t = a0; t < a1; ++t) {
+      H[o_ids + t] = b->ids ? b->ids[t] : 0;
+      H[o_pos + t] = b->positions[t];
+      H[o_seq + t] = s;
+    }
+    H[o_start + s] = a0;
+    H[o_ctx + s] = b->positions[a1 - 1] + 1;
+    const int nb = b->positions[a1 - 1] / B + 1;
+    for (int i = 0; i < MB; ++i) H[o_tab + (size_t)s * MB + i] = i < nb ? b->block_table[(size_t)s * b->max_blocks + i] : 0;
+  }
+  H[o_start + S] = N;
+  if (rows_mode == DEC_ROWS_ALL)
+    for (int t = 0; t < N; ++t) H[o_row + t] = t;
+  else
+    for (int s = 0; s < S; ++s) H[o_row + s] = b->seq_start[s + 1] - 1;
+  // prefill attention tiles, the ones reaching furthest first
+  std::vector<std::array<int, 3>> work;
+  if (!decode) {
+    for (int s = 0; s < S; ++s)
+      for (int t = b->seq_start[s]; t < b->seq_start[s + 1]; t += QT)
+        work.push_back({s, t, std::min(QT, b->seq_start[s + 1] - t)});
+    std::stable_sort(work.begin(), work.end(), [&](const std::array<int, 3>& x, const std::array<int, 3>& y) {
+      return b->positions[x[1] + x[2] - 1] > b->positions[y[1] + y[2] - 1];
+    });
+  }
+  for (size_t i = 0; i < work.size(); ++i)
+    for (int k = 0; k < 3; ++k) H[o_work + 3 * i + k] = work[i][k];
+  o += 3 * work.size();
+  if (o > m->wl.meta_ints) return fail(DEC_ERANGE, "step metadata exceeds the workspace");
+
+  char* ws = m->ws;
+  int32_t* dmeta = (int32_t*)(ws + m->wl.META);
+  DEC_CUDA(cudaMemcpyAsync(dmeta, H, o * 4, cudaMemcpyHostToDevice, st));
+  DEC_CUDA(cudaEventRecord(m->stage_ev[slot], st));
+  m->last_stream = st;
+
+  StepMeta meta;
+  meta.ids = b->ids_device ? b->ids_device : dmeta + o_ids;
+  meta.tok_pos = dmeta + o_pos;
+  meta.tok_seq = dmeta + o_seq;
+  meta.seq_start = dmeta + o_start;
+  meta.seq_ctx = dmeta + o_ctx;
+  meta.row_tok = dmeta + o_row;
+  meta.tables = dmeta + o_tab;
+  meta.work = dmeta + o_work;
+
+  Dims dm;
+  dm.vocab = c.vocab; dm.d = c.d_model; dm.n_layers = c.n_layers; dm.H = c.n_heads; dm.Hkv = c.n_kv_heads;
+  dm.D = c.head_dim; dm.F = c.ff_hidden; dm.B = B; dm.n_blocks = pool->n_blocks; dm.max_blocks = MB;
+  dm.eps = (float)c.rms_eps;
+
+  const bool bf = c.mode == DEC_BF16_F16KV;
+  char* P = m->packed;
+  const PackedLayout& pl = m->pl;
+  const WsLayout& wl = m->wl;
+  float* X = (float*)(ws + wl.X);
+  void* XN = ws + wl.XN;
+  float* SSQ = (float*)(ws + wl.SSQ);
+  float* RAW = (float*)(ws + wl.RAW);
+  float* Q = (float*)(ws + wl.Q);
+  void* ATT = ws + wl.ATT;
+  void* ACT = ws + wl.ACT;
+  float* PART = (float*)(ws + wl.PART);
+  unsigned long long* KEYS = (unsigned long long*)(ws + wl.KEYS);
+  uint32_t* ERR = (uint32_t*)(ws + wl.ERR);
+  const int d = c.d_model;
+  auto layer = [&](int l) { return P + pl.layer0 + (size_t)l * pl.layer_stride; };
+  const bool dumping = m->dump && m->dump_floats >= (size_t)(c.n_layers + 1) * N * d;
+
+  EmbedArgs ea{P + pl.embed, meta.ids, N, d, c.vocab, R, (const float*)(layer(0) + pl.attn_norm), X, XN, SSQ, KEYS, ERR};
+  DEC_LAUNCH(DEC_K_EMBED, launch_embed(ea, bf, st));
+  if (dumping) DEC_CUDA(cudaMemcpyAsync(m->dump, X, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, st));
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    char* Lb = layer(l);
+    GemvArgs g{};
+    g.d = d;
+    g.eps = dm.eps;
+    g.F = c.ff_hidden;
+    // RMSNorm + [Wq;Wk;Wv]
+    g.W = Lb + pl.wqkv; g.rows = qkv_rows(c); g.K = d; g.X = XN; g.x_row = nullptr; g.T = N; g.ssq = SSQ;
+    g.out_f32 = RAW;
+    DEC_LAUNCH(DEC_K_QKV, launch_gemv(g, EPI_QKV_RAW, bf, st));
+    QkvPostArgs qa{RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope),
+                   Q, pool->slabs, l, meta, dm};
+    DEC_LAUNCH(DEC_K_QKV_POST, launch_qkv_post(qa, N, bf, st));
+    // attention
+    AttnArgs aa{Q, pool->slabs, l, meta, dm, ATT, PART, m->NCH, S, 1.0f / std::sqrt((float)c.head_dim)};
+    if (decode) {
+      DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, max_nch, bf, st));
+      DEC_LAUNCH(DEC_K_ATTN_MERGE, launch_attn_merge(aa, bf, st));
+    } else {
+      DEC_LAUNCH(DEC_K_ATTN, launch_attn_prefill(aa, (int)work.size(), bf, st));
+    }
+    // O projection + residual; next GEMM input x * w_mlp
+    GemvArgs go{};
+    go.d = d; go.eps = dm.eps; go.F = c.ff_hidden;
+    go.W = Lb + pl.wo; go.rows = d; go.K = c.n_heads * c.head_dim; go.X = ATT; go.T = N; go.ssq = nullptr;
+    go.X_res = X; go.XN = XN; go.SSQ_out = SSQ; go.w_next = (const float*)(Lb + pl.mlp_norm);
+    DEC_LAUNCH(DEC_K_OPROJ, launch_gemv(go, EPI_RESID, bf, st));
+    // RMSNorm + gate/up + SiLU*mul
+    GemvArgs gu{};
+    gu.d = d; gu.eps = dm.eps; gu.F = c.ff_hidden;
+    gu.W = Lb + pl.wgu; gu.rows = 2 * c.ff_hidden; gu.K = d; gu.X = XN; gu.T = N; gu.ssq = SSQ; gu.act_out = ACT;
+    DEC_LAUNCH(DEC_K_GATEUP, launch_gemv(gu, EPI_SWIGLU, bf, st));
+    // down projection + residual; next GEMM input x * (next attention gain | final gain)
+    GemvArgs gd{};
+    gd.d = d; gd.eps = dm.eps; gd.F = c.ff_hidden;
+    gd.W = Lb + pl.wd; gd.rows = d; gd.K = c.ff_hidden; gd.X = ACT; gd.T = N; gd.ssq = nullptr;
+    gd.X_res = X; gd.XN = XN; gd.SSQ_out = SSQ;
+    gd.w_next = l + 1 < c.n_layers ? (const float*)(layer(l + 1) + pl.attn_norm) : (const float*)(P + pl.final_norm);
+    DEC_LAUNCH(DEC_K_DOWN, launch_gemv(gd, EPI_RESID, bf, st));
+    if (dumping)
+      DEC_CUDA(cudaMemcpyAsync(m->dump + (size_t)(l + 1) * N * d, X, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, st));
+  }
+  // final RMSNorm + tied LM head + argmax
+  GemvArgs gl{};
+  gl.d = d; gl.eps = dm.eps; gl.F = c.ff_hidden;
+  gl.W = P + pl.embed; gl.rows = c.vocab; gl.K = d; gl.X = XN; gl.x_row = meta.row_tok; gl.T = R; gl.ssq = SSQ;
+  gl.out_f32 = logits; gl.keys = KEYS;
+  DEC_LAUNCH(DEC_K_LMHEAD, launch_gemv(gl, EPI_LOGITS, bf, st));
+  DEC_LAUNCH(DEC_K_ARGMAX, launch_argmax_finalize(KEYS, argmax, R, st));
+  return DEC_OK;
+}
+
+int dec_prefill(dec_model* m, dec_pool* pool, const dec_batch* b, int32_t rows, float* logits, int32_t* argmax,
+                void* stream) {
+  return run_step(m, pool, b, rows, logits, argmax, (cudaStream_t)stream, false);
+}
+
+int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, int32_t* argmax, void* stream) {
+  return run_step(m, pool, b, DEC_ROWS_LAST, logits, argmax, (cudaStream_t)stream, true);
+}
+
+int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!in || !out))) return fail(DEC_EINVAL, "bad arguments");
+  DEC_CUDA(launch_f32_to_f16(in, out, n, (cudaStream_t)stream));
+  return DEC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,379 @@
+// kernels_attn.cu - causal grouped-query attention over the paged KV cache.
+//
+// o_t = sum_{j <= pos(t)} softmax_j(q_t . k_j / sqrt(D)) v_j, query head h
+// reading KV head floor(h * Hkv / H); each query attends over exactly its
+// visible keys, no mask is stored (tinyllm L10.1 "Candle model runner ...",
+// section 2.4 and its batch-invariance paragraph).  Keys live in pool blocks:
+// position j of a sequence is slot j % B of block table[j / B].
+//
+// Decode (one query per sequence): split-K over fixed 64-key chunks (the split
+// never depends on the batch), one warp per 16-key block, warp-shuffle softmax,
+// then a second kernel merges the chunk partials in chunk order.
+// Prefill: one CTA per (tile of queries, KV head) with the G query heads of
+// the group stacked as rows; key tiles of 32 are staged in shared memory and
+// folded in with an online softmax.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace dec {
+
+template <int N> struct VecN;
+template <typename KT, int N>
+__device__ __forceinline__ void loadN(const KT* p, float* v) {
+  if constexpr (N % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 8) load8(p + i, v + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = to_f32(p[i]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention, split-K.  grid (chunk, kv head, sequence), 4 warps.
+// ---------------------------------------------------------------------------
+template <typename KT, int D, int G>
+__global__ void __launch_bounds__(128) k_attn_decode(AttnArgs a) {
+  const Dims& dm = a.dims;
+  const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int ctx = a.meta.seq_ctx[s];
+  const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
+  if (c >= nch) return;
+  const int t = a.meta.seq_start[s];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float qs[G][D];
+  __shared__ float ms[4][G], ls[4][G];
+  __shared__ float os[4][G][D];
+  for (int i = threadIdx.x; i < G * D; i += 128)
+    qs[i / D][i % D] = a.Q[((size_t)t * dm.H + g * G + i / D) * D + i % D];
+  __syncthreads();
+
+  constexpr int kPerLane = D / 32;  // output dims per lane
+  float m[G], l[G], o[G][kPerLane];
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPerLane; ++e) o[i][e] = 0.f;
+  }
+  const int bi = c * (kDecodeChunk / 16) + warp;  // block index within the table (B = 16)
+  const int key0 = bi * 16;
+  const int nkeys = min(max(ctx - key0, 0), 16);
+  if (nkeys > 0) {
+    const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
+    const KT* kv = reinterpret_cast<const KT*>(a.kv);
+    const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+    const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+    const int key = lane >> 1, hf = lane & 1;
+    constexpr int kHalf = D / 2;
+    float kvals[kHalf];
+    loadN<KT, kHalf>(Kb + key * D + hf * kHalf, kvals);
+    float sc[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], kvals[e], acc);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      sc[i] = key < nkeys ? acc * a.scale : -INFINITY;
+    }
+    float p[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      m[i] = warp_max(sc[i]);
+      p[i] = key < nkeys ? expf(sc[i] - m[i]) : 0.f;
+      l[i] = warp_sum(hf == 0 ? p[i] : 0.f);
+    }
+    for (int k = 0; k < nkeys; ++k) {
+      float vv[kPerLane];
+      loadN<KT, kPerLane>(Vb + k * D + lane * kPerLane, vv);
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const float pk = __shfl_sync(0xffffffffu, p[i], 2 * k);
+#pragma unroll
+        for (int e = 0; e < kPerLane; ++e) o[i][e] = fmaf(pk, vv[e], o[i][e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    if (lane == 0) {
+      ms[warp][i] = m[i];
+      ls[warp][i] = l[i];
+    }
+#pragma unroll
+    for (int e = 0; e < kPerLane; ++e) os[warp][i][lane * kPerLane + e] = o[i][e];
+  }
+  __syncthreads();
+  // merge the 4 warps in warp order; write (m, l, o[D]) of this chunk
+  for (int i = threadIdx.x; i < G * D; i += 128) {
+    const int h = i / D, dd = i % D;
+    float M = ms[0][h];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) M = fmaxf(M, ms[w][h]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = ms[w][h] == -INFINITY ? 0.f : expf(ms[w][h] - M);
+      L = fmaf(ls[w][h], f, L);
+      O = fmaf(os[w][h][dd], f, O);
+    }
+    float* part = a.part + (((size_t)s * dm.H + g * G + h) * a.nchunk_cap + c) * (D + 2);
+    if (dd == 0) {
+      part[0] = M;
+      part[1] = L;
+    }
+    part[2 + dd] = O;
+  }
+}
+
+// Merge the chunk partials of one (sequence, query head) in chunk order.
+template <typename AT, int D>
+__global__ void k_attn_combine(AttnArgs a) {
+  const Dims& dm = a.dims;
+  const int s = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
+  const int ctx = a.meta.seq_ctx[s];
+  const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
+  const int t = a.meta.seq_start[s];
+  const float* part = a.part + ((size_t)s * dm.H + h) * a.nchunk_cap * (D + 2);
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, part[c * (D + 2)]);
+  float L = 0.f, O = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const float* p = part + c * (D + 2);
+    const float f = expf(p[0] - M);
+    L = fmaf(p[1], f, L);
+    O = fmaf(p[2 + dd], f, O);
+  }
+  AT* out = reinterpret_cast<AT*>(a.ATT);
+  out[((size_t)t * dm.H + h) * D + dd] = from_f32<AT>(O / L);
+}
+
+// ---------------------------------------------------------------------------
+// Prefill attention.  grid (work tile, kv head), 128 threads.  A tile is up to
+// QT = 64/G consecutive new tokens of one sequence; its 64 query-head rows are
+// row r = query * G + head-in-group.  Thread (ty, tx) = (tid / 8, tid % 8) owns
+// rows 4ty..4ty+3; for scores it owns keys tx + 8i of the 32-key tile, for the
+// output it owns dims tx*4 + 32i + (0..3).
+// ---------------------------------------------------------------------------
+constexpr int kPfRows = 64;
+constexpr int kPfKeys = 32;
+
+template <typename KT, typename AT, int D, int G>
+__global__ void __launch_bounds__(128) k_attn_prefill(AttnArgs a) {
+  constexpr int LD = D + 4;  // padded row stride (floats)
+  constexpr int kDimGroups = D / 32;
+  extern __shared__ __align__(16) float sm[];
+  float* Qs = sm;                      // [64][LD]
+  float* Ks = Qs + kPfRows * LD;       // [32][LD]
+  float* Vs = Ks + kPfKeys * LD;       // [32][LD]
+  float* Ps = Vs + kPfKeys * LD;       // [64][33]
+  const Dims& dm = a.dims;
+  const int* w = a.meta.work + blockIdx.x * 3;
+  const int s = w[0], tok0 = w[1], ntok = w[2];
+  const int g = blockIdx.y;
+  const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
+  const int p0 = a.meta.tok_pos[tok0];
+  const int p_last = p0 + ntok - 1;
+  const KT* kv = reinterpret_cast<const KT*>(a.kv);
+
+  for (int i = tid; i < kPfRows * (D / 4); i += 128) {
+    const int r = i / (D / 4), c4 = i % (D / 4);
+    const int qi = r / G, hh = r % G;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (qi < ntok) v = *reinterpret_cast<const float4*>(a.Q + ((size_t)(tok0 + qi) * dm.H + g * G + hh) * D + c4 * 4);
+    *reinterpret_cast<float4*>(Qs + r * LD + c4 * 4) = v;
+  }
+  float m[4], l[4], o[4][kDimGroups][4];
+  int rpos[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+    rpos[i] = p0 + (ty * 4 + i) / G;
+#pragma unroll
+    for (int j = 0; j < kDimGroups; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[i][j][e] = 0.f;
+  }
+  const int ntiles = p_last / kPfKeys + 1;
+  for (int kt = 0; kt < ntiles; ++kt) {
+    const int j0 = kt * kPfKeys;
+    __syncthreads();  // previous tile fully consumed
+    for (int i = tid; i < kPfKeys * (D / 8); i += 128) {
+      const int kk = i / (D / 8), c8 = (i % (D / 8)) * 8;
+      const int j = j0 + kk;
+      float kvv[8], vvv[8];
+      if (j <= p_last) {
+        const int blk = a.meta.tables[(size_t)s * dm.max_blocks + j / dm.B];
+        const int slot = j % dm.B;
+        load8(kv + kv_offset(a.layer, blk, 0, g, slot, dm.n_blocks, dm.Hkv, dm.B, D) + c8, kvv);
+        load8(kv + kv_offset(a.layer, blk, 1, g, slot, dm.n_blocks, dm.Hkv, dm.B, D) + c8, vvv);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kvv[e] = vvv[e] = 0.f;
+      }
+      *reinterpret_cast<float4*>(Ks + kk * LD + c8) = make_float4(kvv[0], kvv[1], kvv[2], kvv[3]);
+      *reinterpret_cast<float4*>(Ks + kk * LD + c8 + 4) = make_float4(kvv[4], kvv[5], kvv[6], kvv[7]);
+      *reinterpret_cast<float4*>(Vs + kk * LD + c8) = make_float4(vvv[0], vvv[1], vvv[2], vvv[3]);
+      *reinterpret_cast<float4*>(Vs + kk * LD + c8 + 4) = make_float4(vvv[4], vvv[5], vvv[6], vvv[7]);
+    }
+    __syncthreads();
+    // scores: 4 rows x 4 keys per thread
+    float sc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[i][j] = 0.f;
+#pragma unroll 4
+    for (int d4 = 0; d4 < D; d4 += 4) {
+      float4 q[4], k[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * LD + d4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) k[j] = *reinterpret_cast<const float4*>(Ks + (tx + 8 * j) * LD + d4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float acc = sc[i][j];
+          acc = fmaf(q[i].x, k[j].x, acc);
+          acc = fmaf(q[i].y, k[j].y, acc);
+          acc = fmaf(q[i].z, k[j].z, acc);
+          acc = fmaf(q[i].w, k[j].w, acc);
+          sc[i][j] = acc;
+        }
+    }
+    // online softmax per row over the 8 threads sharing ty
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int key = j0 + tx + 8 * j;
+        sc[i][j] = key <= rpos[i] ? sc[i][j] * a.scale : -INFINITY;
+        mx = fmaxf(mx, sc[i][j]);
+      }
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m[i], mx);
+      float corr = 1.f, rs = 0.f;
+      if (m_new != -INFINITY) {
+        corr = m[i] == -INFINITY ? 0.f : expf(m[i] - m_new);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float p = sc[i][j] == -INFINITY ? 0.f : expf(sc[i][j] - m_new);
+          Ps[(ty * 4 + i) * (kPfKeys + 1) + tx + 8 * j] = p;
+          rs += p;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Ps[(ty * 4 + i) * (kPfKeys + 1) + tx + 8 * j] = 0.f;
+      }
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
+      m[i] = m_new;
+      l[i] = l[i] * corr + rs;
+#pragma unroll
+      for (int j = 0; j < kDimGroups; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[i][j][e] *= corr;
+    }
+    __syncthreads();
+    // o += P V
+#pragma unroll 4
+    for (int kk = 0; kk < kPfKeys; ++kk) {
+      float p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = Ps[(ty * 4 + i) * (kPfKeys + 1) + kk];
+#pragma unroll
+      for (int j = 0; j < kDimGroups; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(Vs + kk * LD + tx * 4 + 32 * j);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          o[i][j][0] = fmaf(p[i], v.x, o[i][j][0]);
+          o[i][j][1] = fmaf(p[i], v.y, o[i][j][1]);
+          o[i][j][2] = fmaf(p[i], v.z, o[i][j][2]);
+          o[i][j][3] = fmaf(p[i], v.w, o[i][j][3]);
+        }
+      }
+    }
+  }
+  AT* out = reinterpret_cast<AT*>(a.ATT);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ty * 4 + i, qi = r / G, hh = r % G;
+    if (qi >= ntok) continue;
+    const float inv = 1.0f / l[i];
+    AT* dst = out + ((size_t)(tok0 + qi) * dm.H + g * G + hh) * D;
+#pragma unroll
+    for (int j = 0; j < kDimGroups; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[tx * 4 + 32 * j + e] = from_f32<AT>(o[i][j][e] * inv);
+  }
+}
+
+int prefill_tile_queries(int G) { return kPfRows / G; }
+
+// ---------------------------------------------------------------------------
+// launchers: head_dim in {32, 64, 128}, group size in {1, 2, 4}
+// ---------------------------------------------------------------------------
+template <typename KT, typename AT, int D, int G>
+static cudaError_t attn_decode_t(const AttnArgs& a, int nchunk, cudaStream_t s) {
+  dim3 grid(nchunk, a.dims.Hkv, a.S);
+  k_attn_decode<KT, D, G><<<grid, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename KT, typename AT, int D, int G>
+static cudaError_t attn_merge_t(const AttnArgs& a, int, cudaStream_t s) {
+  k_attn_combine<AT, D><<<dim3(a.S, a.dims.H), D, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename KT, typename AT, int D, int G>
+static cudaError_t attn_prefill_t(const AttnArgs& a, int n_work, cudaStream_t s) {
+  constexpr int LD = D + 4;
+  const size_t smem = ((size_t)kPfRows * LD + 2 * kPfKeys * LD + kPfRows * (kPfKeys + 1)) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<KT, AT, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  k_attn_prefill<KT, AT, D, G><<<dim3(n_work, a.dims.Hkv), 128, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+#define DEC_DISPATCH_DG(FN, KT, AT, ...)                                         \
+  do {                                                                          \
+    const int D_ = a.dims.D, G_ = a.dims.H / a.dims.Hkv;                        \
+    if (D_ == 128 && G_ == 2) return FN<KT, AT, 128, 2>(a, __VA_ARGS__);        \
+    if (D_ == 128 && G_ == 1) return FN<KT, AT, 128, 1>(a, __VA_ARGS__);        \
+    if (D_ == 128 && G_ == 4) return FN<KT, AT, 128, 4>(a, __VA_ARGS__);        \
+    if (D_ == 64 && G_ == 2) return FN<KT, AT, 64, 2>(a, __VA_ARGS__);          \
+    if (D_ == 64 && G_ == 1) return FN<KT, AT, 64, 1>(a, __VA_ARGS__);          \
+    if (D_ == 64 && G_ == 4) return FN<KT, AT, 64, 4>(a, __VA_ARGS__);          \
+    if (D_ == 32 && G_ == 2) return FN<KT, AT, 32, 2>(a, __VA_ARGS__);          \
+    if (D_ == 32 && G_ == 1) return FN<KT, AT, 32, 1>(a, __VA_ARGS__);          \
+    if (D_ == 32 && G_ == 4) return FN<KT, AT, 32, 4>(a, __VA_ARGS__);          \
+    return cudaErrorInvalidValue;                                               \
+  } while (0)
+
+cudaError_t launch_attn_decode(const AttnArgs& a, int nchunk, bool wbf16, cudaStream_t s) {
+  if (wbf16) DEC_DISPATCH_DG(attn_decode_t, __half, bf16, nchunk, s);
+  DEC_DISPATCH_DG(attn_decode_t, float, float, nchunk, s);
+}
+
+cudaError_t launch_attn_merge(const AttnArgs& a, bool wbf16, cudaStream_t s) {
+  if (wbf16) DEC_DISPATCH_DG(attn_merge_t, __half, bf16, 0, s);
+  DEC_DISPATCH_DG(attn_merge_t, float, float, 0, s);
+}
+
+cudaError_t launch_attn_prefill(const AttnArgs& a, int n_work, bool wbf16, cudaStream_t s) {
+  if (wbf16) DEC_DISPATCH_DG(attn_prefill_t, __half, bf16, n_work, s);
+  DEC_DISPATCH_DG(attn_prefill_t, float, float, n_work, s);
+}
+
+}  // namespace dec

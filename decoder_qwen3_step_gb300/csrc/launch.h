@@ -1,0 +1,88 @@
+// launch.h - host-side launchers of the decoder kernels (internal to libdec).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace dec {
+
+enum Epi { EPI_QKV_RAW = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+
+// One weight-streaming product Y[t, r] = sum_k X[row(t), k] W[r, k] with a
+// fused epilogue.  W is [rows, K] (fp32 or bf16), X is [*, K] (act type).
+struct GemvArgs {
+  const void* W;
+  int rows, K;
+  const void* X;
+  const int32_t* x_row;   // activation row of token-row t (null: t)
+  int T;                  // token rows
+  const float* ssq;       // RMSNorm partials of the activation rows (null: no row scale)
+  int d;
+  float eps;
+  float* out_f32;         // QKV_RAW [T, rows]; LOGITS [T, rows] (may be null)
+  float* X_res;           // RESID residual [T, d]
+  void* XN;               // RESID next GEMM input [T, d]
+  float* SSQ_out;         // RESID partials [T, d/16]
+  const float* w_next;    // RESID next RMSNorm gain [d]
+  void* act_out;          // SWIGLU output [T, F]
+  int F;
+  unsigned long long* keys; // LOGITS argmax keys [T]
+};
+
+struct EmbedArgs {
+  const void* E;  // [vocab, d] weight type
+  const int32_t* ids;
+  int T, d, vocab, R;
+  const float* w0;  // first RMSNorm gain
+  float* X;
+  void* XN;
+  float* SSQ;
+  unsigned long long* keys;
+  uint32_t* err;
+};
+
+struct QkvPostArgs {
+  const float* raw;  // [T, (H+2Hkv)*D]
+  const float* q_norm;
+  const float* k_norm;
+  const float* rope;  // [max_positions, D/2, 2] (cos, sin)
+  float* Q;           // [T, H, D]
+  void* kv;           // pool slabs
+  int layer;
+  StepMeta meta;
+  Dims dims;
+};
+
+struct AttnArgs {
+  const float* Q;   // [T, H, D]
+  const void* kv;   // pool slabs
+  int layer;
+  StepMeta meta;
+  Dims dims;
+  void* ATT;        // [T, H*D] act type
+  float* part;      // decode partials [S, H, nchunk_cap, D+2]
+  int nchunk_cap;
+  int S;
+  float scale;      // 1/sqrt(D)
+};
+
+// Launchers; `wbf16` selects bf16 weights / activations / f16 KV (serving
+// mode) versus fp32 everywhere (parity mode).  Return cudaGetLastError().
+cudaError_t launch_embed(const EmbedArgs& a, bool wbf16, cudaStream_t s);
+cudaError_t launch_gemv(const GemvArgs& a, int epi, bool wbf16, cudaStream_t s);
+cudaError_t launch_qkv_post(const QkvPostArgs& a, int T, bool wbf16, cudaStream_t s);
+cudaError_t launch_argmax_finalize(const unsigned long long* keys, int32_t* ids, int R, cudaStream_t s);
+cudaError_t launch_attn_decode(const AttnArgs& a, int nchunk, bool wbf16, cudaStream_t s);
+cudaError_t launch_attn_merge(const AttnArgs& a, bool wbf16, cudaStream_t s);
+cudaError_t launch_attn_prefill(const AttnArgs& a, int n_work, bool wbf16, cudaStream_t s);
+// Packing: dst row map modes.
+enum PackMode { PACK_IDENTITY = 0, PACK_GATE = 1, PACK_UP = 2 };
+cudaError_t launch_pack(void* dst, const float* src, int rows, int cols, int mode, bool wbf16, cudaStream_t s);
+cudaError_t launch_f32_to_f16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
+
+// Query rows of one prefill attention tile (query-head rows / group size).
+int prefill_tile_queries(int G);
+
+}  // namespace dec

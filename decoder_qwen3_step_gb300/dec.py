@@ -1,0 +1,113 @@
+"""ctypes binding of libdec (include/dec.h): argument marshalling only.
+
+Every function keeps its C name and signature.  Loading fails loudly when the
+library has not been built: there is no fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdec.so")
+
+DEC_OK, DEC_EINVAL, DEC_ECAPACITY, DEC_EBLOCK, DEC_ERANGE, DEC_EVOCAB, DEC_ECUDA, DEC_EDEVICE = range(8)
+DEC_FP32, DEC_BF16_F16KV = 0, 1
+DEC_ROWS_ALL, DEC_ROWS_LAST = 0, 1
+DEC_DEV_BAD_ID, DEC_DEV_TIMEOUT = 1, 2
+
+ERROR_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ECAPACITY", 3: "DEC_EBLOCK", 4: "DEC_ERANGE",
+               5: "DEC_EVOCAB", 6: "DEC_ECUDA", 7: "DEC_EDEVICE"}
+
+# Every symbol include/dec.h declares (the tests check the library exports all of them).
+EXPORTS = (
+    "dec_last_error", "dec_config_check", "dec_weights_bytes", "dec_workspace_bytes", "dec_create", "dec_destroy",
+    "dec_device_status", "dec_set_dump", "dec_pool_bytes", "dec_pool_create", "dec_pool_destroy", "dec_pool_alloc",
+    "dec_pool_retain", "dec_pool_release", "dec_pool_free_blocks", "dec_pool_refcount", "dec_kv_offset",
+    "dec_prefill", "dec_decode", "dec_f32_to_f16", "dec_version", "dec_profile_enable", "dec_profile_read",
+    "dec_launch_count",
+)
+KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax")
+
+
+class dec_config(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("vocab", "d_model", "n_layers", "n_heads", "n_kv_heads", "head_dim",
+                                         "ff_hidden", "max_positions", "block_tokens", "mode")] + [
+        ("rope_base", C.c_double), ("rms_eps", C.c_double)] + [
+        (n, C.c_int32) for n in ("qk_norm", "rope_split", "tied", "rope_scaling", "sliding_window", "attention_bias")]
+
+
+_PP = C.POINTER(C.c_void_p)
+
+
+class dec_weights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("final_norm", C.c_void_p)] + [
+        (n, _PP) for n in ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "mlp_norm", "w_gate", "w_up",
+                           "w_down")]
+
+
+_I32P = C.POINTER(C.c_int32)
+
+
+class dec_batch(C.Structure):
+    _fields_ = [("n_seqs", C.c_int32), ("n_tokens", C.c_int32), ("ids", _I32P), ("ids_device", C.c_void_p),
+                ("positions", _I32P), ("seq_start", _I32P), ("block_table", _I32P), ("max_blocks", C.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdec.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = C.CDLL(LIB_PATH)
+        V, I, SZ, I64 = C.c_void_p, C.c_int, C.c_size_t, C.c_int64
+        cfgp = C.POINTER(dec_config)
+        sig = {
+            "dec_last_error": (C.c_char_p, []),
+            "dec_version": (C.c_char_p, []),
+            "dec_config_check": (I, [cfgp]),
+            "dec_weights_bytes": (I, [cfgp, C.POINTER(SZ)]),
+            "dec_workspace_bytes": (I, [cfgp, C.c_int32, C.c_int32, C.POINTER(SZ)]),
+            "dec_create": (I, [cfgp, C.POINTER(dec_weights), V, SZ, V, SZ, C.c_int32, C.c_int32, V, C.POINTER(V)]),
+            "dec_destroy": (None, [V]),
+            "dec_device_status": (I, [V, C.POINTER(C.c_uint32)]),
+            "dec_set_dump": (I, [V, V, SZ]),
+            "dec_pool_bytes": (I, [cfgp, C.c_int32, C.POINTER(SZ)]),
+            "dec_pool_create": (I, [cfgp, C.c_int32, V, SZ, C.POINTER(V)]),
+            "dec_pool_destroy": (None, [V]),
+            "dec_pool_alloc": (I, [V, C.c_int32, _I32P]),
+            "dec_pool_retain": (I, [V, C.c_int32]),
+            "dec_pool_release": (I, [V, C.c_int32]),
+            "dec_pool_free_blocks": (I, [V, _I32P]),
+            "dec_pool_refcount": (I, [V, C.c_int32, _I32P]),
+            "dec_kv_offset": (I, [V, _I32P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(I64)]),
+            "dec_prefill": (I, [V, V, C.POINTER(dec_batch), C.c_int32, V, V, V]),
+            "dec_decode": (I, [V, V, C.POINTER(dec_batch), V, V, V]),
+            "dec_f32_to_f16": (I, [V, V, I64, V]),
+            "dec_profile_enable": (I, [V, C.c_int32, C.c_int32]),
+            "dec_profile_read": (I, [V, C.c_int32, C.POINTER(C.c_double), C.POINTER(I64)]),
+            "dec_launch_count": (I, [V, C.POINTER(I64)]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+class DecError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = lib().dec_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {ERROR_NAMES.get(code, code)}: {msg}")
+
+
+def check(code: int, where: str) -> None:
+    if code != DEC_OK:
+        raise DecError(code, where)

@@ -1,0 +1,198 @@
+"""A small owner of the device buffers libdec needs, allocated through torch.
+
+torch provides device memory and the stream; every step of the decoder runs
+in libdec's kernels through the C ABI (``decoder_qwen3_step_gb300.dec``).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+import torch
+
+from . import dec
+from .inputs import BLOCK_TOKENS, LAYER_TENSORS, RMS_EPS, ROPE_BASE
+
+
+def make_config(shape: dict, mode: int, max_positions: int) -> dec.dec_config:
+    c = dec.dec_config()
+    for k in ("vocab", "d_model", "n_layers", "n_heads", "n_kv_heads", "head_dim", "ff_hidden"):
+        setattr(c, k, shape[k])
+    c.max_positions = max_positions
+    c.block_tokens = BLOCK_TOKENS
+    c.mode = mode
+    c.rope_base = ROPE_BASE
+    c.rms_eps = RMS_EPS
+    c.qk_norm = c.rope_split = c.tied = 1
+    c.rope_scaling = c.sliding_window = c.attention_bias = 0
+    return c
+
+
+def _stream_ptr(stream) -> C.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+class Batch:
+    """Host arrays of one step, kept alive while the C call reads them."""
+
+    def __init__(self, seqs, device_ids: torch.Tensor | None = None):
+        # seqs: list of (ids, start_position, block_table)
+        self.n_seqs = len(seqs)
+        if not seqs:  # an empty step: marshalled as is, the library refuses it
+            seqs = [([], 0, [])]
+        lens = [len(s[0]) for s in seqs]
+        self.seq_start = _i32(np.concatenate([[0], np.cumsum(lens)]))
+        self.n_tokens = int(self.seq_start[-1])
+        self.ids = _i32(np.concatenate([np.asarray(s[0]) for s in seqs]) if seqs else [])
+        self.positions = _i32(np.concatenate([s[1] + np.arange(n) for s, n in zip(seqs, lens)]))
+        self.max_blocks = max(1, max(len(s[2]) for s in seqs))
+        tab = np.zeros((len(seqs), self.max_blocks), dtype=np.int32)
+        for i, s in enumerate(seqs):
+            tab[i, : len(s[2])] = s[2]
+        self.tables = _i32(tab)
+        self.device_ids = device_ids
+        st = dec.dec_batch()
+        st.n_seqs = self.n_seqs
+        st.n_tokens = self.n_tokens
+        st.ids = _ptr(self.ids) if device_ids is None else None
+        st.ids_device = C.c_void_p(device_ids.data_ptr()) if device_ids is not None else None
+        st.positions = _ptr(self.positions)
+        st.seq_start = _ptr(self.seq_start)
+        st.block_table = _ptr(self.tables)
+        st.max_blocks = self.max_blocks
+        self.struct = st
+
+
+class Decoder:
+    """A model + KV pool + workspace on one GPU, built from float32 weights."""
+
+    def __init__(self, shape: dict, weights: dict, mode: int = dec.DEC_FP32, max_positions: int = 4096,
+                 max_tokens: int = 4096, max_seqs: int = 64, n_blocks: int = 1024, device: str = "cuda:0",
+                 stream=None):
+        L = dec.lib()
+        self.L = L
+        self.shape = dict(shape)
+        self.mode = mode
+        self.device = torch.device(device)
+        self.cfg = make_config(shape, mode, max_positions)
+        self.max_tokens, self.max_seqs = max_tokens, max_seqs
+        torch.cuda.set_device(self.device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        sz = C.c_size_t()
+        dec.check(L.dec_weights_bytes(C.byref(self.cfg), C.byref(sz)), "dec_weights_bytes")
+        self.packed = torch.empty(sz.value, dtype=torch.uint8, device=self.device)
+        dec.check(L.dec_workspace_bytes(C.byref(self.cfg), max_tokens, max_seqs, C.byref(sz)), "dec_workspace_bytes")
+        self.workspace = torch.empty(sz.value, dtype=torch.uint8, device=self.device)
+
+        raw = {k: torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(self.device) for k, v in weights.items()}
+        nl = shape["n_layers"]
+        arrays = {}
+
+        def per_layer(t):
+            arr = (C.c_void_p * nl)(*[raw[f"layers.{l}.{t}"].data_ptr() for l in range(nl)])
+            arrays[t] = arr
+            return C.cast(arr, C.POINTER(C.c_void_p))
+
+        w = dec.dec_weights()
+        w.embed = raw["embed"].data_ptr()
+        w.final_norm = raw["final_norm"].data_ptr()
+        names = {"attn_norm": "attn_norm", "wq": "q", "wk": "k", "wv": "v", "q_norm": "q_norm", "k_norm": "k_norm",
+                 "wo": "o", "mlp_norm": "mlp_norm", "w_gate": "gate", "w_up": "up", "w_down": "down"}
+        assert set(names.values()) == set(LAYER_TENSORS)
+        for field, t in names.items():
+            setattr(w, field, per_layer(t))
+        handle = C.c_void_p()
+        dec.check(L.dec_create(C.byref(self.cfg), C.byref(w), C.c_void_p(self.packed.data_ptr()), self.packed.numel(),
+                               C.c_void_p(self.workspace.data_ptr()), self.workspace.numel(), max_tokens, max_seqs,
+                               _stream_ptr(self.stream), C.byref(handle)), "dec_create")
+        self.handle = handle
+        del raw, arrays
+
+        dec.check(L.dec_pool_bytes(C.byref(self.cfg), n_blocks, C.byref(sz)), "dec_pool_bytes")
+        self.slabs = torch.empty(sz.value, dtype=torch.uint8, device=self.device)
+        pool = C.c_void_p()
+        dec.check(L.dec_pool_create(C.byref(self.cfg), n_blocks, C.c_void_p(self.slabs.data_ptr()), self.slabs.numel(),
+                                    C.byref(pool)), "dec_pool_create")
+        self.pool = pool
+        self.n_blocks = n_blocks
+
+    # -- pool ---------------------------------------------------------------
+    def alloc(self, n: int) -> list:
+        ids = (C.c_int32 * max(n, 1))()
+        dec.check(self.L.dec_pool_alloc(self.pool, n, ids), "dec_pool_alloc")
+        return list(ids[:n])
+
+    def release(self, ids) -> None:
+        for i in ids:
+            dec.check(self.L.dec_pool_release(self.pool, int(i)), "dec_pool_release")
+
+    def free_blocks(self) -> int:
+        n = C.c_int32()
+        dec.check(self.L.dec_pool_free_blocks(self.pool, C.byref(n)), "dec_pool_free_blocks")
+        return n.value
+
+    def blocks_for(self, n_positions: int) -> list:
+        return self.alloc((n_positions + BLOCK_TOKENS - 1) // BLOCK_TOKENS)
+
+    # -- steps ----------------------------------------------------------------
+    def prefill(self, seqs, rows: int = dec.DEC_ROWS_ALL, logits: bool = True, device_ids=None,
+                out=None):
+        """seqs: list of (ids, start, block_table).  Returns (logits [R,V] fp32 | None, argmax [R] int32)."""
+        b = Batch(seqs, device_ids)
+        R = b.n_tokens if rows == dec.DEC_ROWS_ALL else b.n_seqs
+        lg, am = self._outputs(R, logits, out)
+        dec.check(self.L.dec_prefill(self.handle, self.pool, C.byref(b.struct), rows,
+                                     C.c_void_p(lg.data_ptr()) if lg is not None else None,
+                                     C.c_void_p(am.data_ptr()), _stream_ptr(self.stream)), "dec_prefill")
+        return lg, am
+
+    def decode(self, seqs, logits: bool = True, device_ids=None, out=None):
+        b = Batch(seqs, device_ids)
+        lg, am = self._outputs(b.n_seqs, logits, out)
+        dec.check(self.L.dec_decode(self.handle, self.pool, C.byref(b.struct),
+                                    C.c_void_p(lg.data_ptr()) if lg is not None else None,
+                                    C.c_void_p(am.data_ptr()), _stream_ptr(self.stream)), "dec_decode")
+        return lg, am
+
+    def _outputs(self, R, logits, out):
+        if out is not None:
+            return out
+        V = self.shape["vocab"]
+        lg = torch.empty((R, V), dtype=torch.float32, device=self.device) if logits else None
+        am = torch.empty((R,), dtype=torch.int32, device=self.device)
+        return lg, am
+
+    def device_status(self) -> int:
+        f = C.c_uint32()
+        dec.check(self.L.dec_device_status(self.handle, C.byref(f)), "dec_device_status")
+        return f.value
+
+    def set_dump(self, buf: torch.Tensor | None):
+        if buf is None:
+            dec.check(self.L.dec_set_dump(self.handle, None, 0), "dec_set_dump")
+        else:
+            dec.check(self.L.dec_set_dump(self.handle, C.c_void_p(buf.data_ptr()), buf.numel()), "dec_set_dump")
+
+    def close(self):
+        if getattr(self, "pool", None):
+            self.L.dec_pool_destroy(self.pool)
+            self.pool = None
+        if getattr(self, "handle", None):
+            self.L.dec_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,233 @@
+/*
+ * dec.h - C ABI of libdec: one forward step of a Qwen3-style pre-norm decoder
+ * with a paged KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * The step computed (tinyllm L10.1 "Candle model runner (Llama + bigram,
+ * int4), Rust KV cache, sampler and PCG32", section 2.4 "The Llama forward,
+ * one step"; octlm "A real model in our own decoder", the five switches):
+ *
+ *   x = E[id]
+ *   per layer: h = RMSNorm(x) ; q,k,v = h W^T ; q,k <- per-head RMSNorm
+ *              (QK-norm) ; q,k <- split-half RoPE at pos(t), base rope_base ;
+ *              K/V of every new token -> its sequence's KV blocks ;
+ *              o_t = sum_{j <= pos(t)} softmax_j(q_t . k_j / sqrt(D)) v_j
+ *              (grouped-query: query head h reads KV head floor(h*Hkv/H)) ;
+ *              x += o W_o^T ; x += (silu(h2 W_g^T) * (h2 W_u^T)) W_d^T,
+ *              h2 = RMSNorm(x)
+ *   logits = RMSNorm(x) E^T (tied embedding) ; greedy id = argmax, lowest
+ *   id on ties (tinyllm L10.1 section 2.6).
+ *
+ * Conventions for every entry point:
+ *  - Return value: DEC_OK (0) or one of the DEC_E* codes below;
+ *    dec_last_error() then returns a message (thread-local, valid until the
+ *    next call on the same thread).  All argument and batch checks run on the
+ *    host BEFORE any device work is queued, so a refused call leaves the KV
+ *    cache and every output untouched (tinyllm L10.1 section 4,
+ *    forward_refuses_bad_batches).
+ *  - Memory: the caller allocates every device buffer (weights, the packed
+ *    weight buffer, the workspace, the KV slabs, logits, ids).  The library
+ *    never calls cudaMalloc; it owns only host metadata (block refcounts and
+ *    free list, descriptors, a small pinned staging ring for per-step
+ *    metadata, captured CUDA graphs).
+ *  - Streams: device work is queued on the caller's stream (a cudaStream_t
+ *    passed as void*; NULL = the legacy default stream) and is asynchronous;
+ *    outputs are valid once that stream has synchronised.
+ *  - Devices: one GPU per model; all pointers given to a model live on the
+ *    device that was current when dec_create ran.
+ */
+#ifndef DEC_H
+#define DEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define DEC_OK        0
+#define DEC_EINVAL    1 /* bad argument or unsupported config (scaled RoPE, sliding window, biases...) */
+#define DEC_ECAPACITY 2 /* pool has fewer free blocks than asked (allocation is all-or-nothing) */
+#define DEC_EBLOCK    3 /* block id outside the pool or not currently allocated */
+#define DEC_ERANGE    4 /* position past max_positions, short block table, or too many tokens */
+#define DEC_EVOCAB    5 /* token id outside [0, vocab) */
+#define DEC_ECUDA     6 /* a CUDA runtime call failed */
+#define DEC_EDEVICE   7 /* a kernel raised its device error word (see dec_device_status) */
+
+/* ---- numeric modes -------------------------------------------------------- */
+#define DEC_FP32       0 /* fp32 weights, fp32 activations, fp32 KV: parity mode, true fp32 (no TF32) */
+#define DEC_BF16_F16KV 1 /* bf16 weights and GEMM inputs, fp32 accumulation and residual, f16 KV */
+
+/* which rows of a prefill get logits */
+#define DEC_ROWS_ALL  0 /* every new token (octlm "Proving it's the same model": every position) */
+#define DEC_ROWS_LAST 1 /* last new token of each sequence (tinyllm L10.1 section 2.4) */
+
+/* Decoder shape and switches (octlm "A real model in our own decoder",
+ * qwen_config).  Everything the decoder cannot run is refused with
+ * DEC_EINVAL, never served wrong (tinyllm L10.1 section 2.3). */
+typedef struct dec_config {
+    int32_t vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ff_hidden;
+    int32_t max_positions; /* positions 0 .. max_positions-1 are valid */
+    int32_t block_tokens;  /* KV block size B; 16 */
+    int32_t mode;          /* DEC_FP32 or DEC_BF16_F16KV */
+    double rope_base;      /* 1e6 for Qwen3 */
+    double rms_eps;        /* 1e-6; inside the square root */
+    int32_t qk_norm;       /* must be 1 */
+    int32_t rope_split;    /* must be 1: channel j pairs with j + head_dim/2 */
+    int32_t tied;          /* must be 1: the LM head is the embedding */
+    int32_t rope_scaling;  /* must be 0 */
+    int32_t sliding_window;/* must be 0 */
+    int32_t attention_bias;/* must be 0 */
+} dec_config;
+
+/* Raw fp32 weights, DEVICE pointers, row-major [out, in] (y = x W^T).
+ * Per-layer fields are HOST arrays of n_layers device pointers.  Read only
+ * during dec_create; the caller may free them afterwards. */
+typedef struct dec_weights {
+    const float* embed;       /* [vocab, d_model] */
+    const float* final_norm;  /* [d_model] */
+    const float* const* attn_norm; /* [d_model] */
+    const float* const* wq;   /* [n_heads*head_dim, d_model] */
+    const float* const* wk;   /* [n_kv_heads*head_dim, d_model] */
+    const float* const* wv;   /* [n_kv_heads*head_dim, d_model] */
+    const float* const* q_norm; /* [head_dim], shared by all query heads */
+    const float* const* k_norm; /* [head_dim], shared by all key heads */
+    const float* const* wo;   /* [d_model, n_heads*head_dim] */
+    const float* const* mlp_norm; /* [d_model] */
+    const float* const* w_gate; /* [ff_hidden, d_model] */
+    const float* const* w_up;   /* [ff_hidden, d_model] */
+    const float* const* w_down; /* [d_model, ff_hidden] */
+} dec_weights;
+
+typedef struct dec_model dec_model; /* opaque */
+typedef struct dec_pool dec_pool;   /* opaque */
+
+/* One step: S sequences, each a run of new tokens at absolute positions
+ * (tinyllm L10.1 section 2.4, ForwardSeq / ForwardBatch in section 4).
+ * All arrays are HOST memory, read during the call only. */
+typedef struct dec_batch {
+    int32_t n_seqs;             /* S >= 1 */
+    int32_t n_tokens;           /* N = total new tokens >= 1 */
+    const int32_t* ids;         /* [N] token ids, sequences back to back; may be NULL if ids_device is set */
+    const int32_t* ids_device;  /* optional DEVICE [N] ids (e.g. the previous step's argmax); checked on the
+                                   device: an id outside the vocabulary sets DEC_DEV_BAD_ID and reads row 0 */
+    const int32_t* positions;   /* [N] absolute positions; within a sequence they must be p_s, p_s+1, ... */
+    const int32_t* seq_start;   /* [S+1] offsets of each sequence's tokens; seq_start[0]=0, seq_start[S]=N */
+    const int32_t* block_table; /* [S * max_blocks] pool block ids; position j of sequence s lives in block
+                                   block_table[s*max_blocks + j/B], slot j % B */
+    int32_t max_blocks;         /* row stride of block_table */
+} dec_batch;
+
+/* ---- errors --------------------------------------------------------------- */
+const char* dec_last_error(void);
+
+/* Device error word bits (dec_device_status). */
+#define DEC_DEV_BAD_ID   1u /* a device-side token id was outside the vocabulary */
+#define DEC_DEV_TIMEOUT  2u /* a bounded wait in a kernel gave up */
+
+/* ---- model ---------------------------------------------------------------- */
+/* Check a config; DEC_OK if the decoder can run it. */
+int dec_config_check(const dec_config* cfg);
+
+/* Bytes of the packed-weight buffer dec_create needs for cfg (device). */
+int dec_weights_bytes(const dec_config* cfg, size_t* bytes);
+
+/* Bytes of the per-model workspace for steps of up to max_tokens new tokens,
+ * max_seqs sequences and max_rows logits rows (device). */
+int dec_workspace_bytes(const dec_config* cfg, int32_t max_tokens, int32_t max_seqs, size_t* bytes);
+
+/* Build a model: validates cfg, packs the raw fp32 weights into packed_buf
+ * (fused [Wq;Wk;Wv] and gate/up layouts; bf16 round-to-nearest-even in
+ * DEC_BF16_F16KV mode) and fills the RoPE cos/sin table, computed on the host
+ * in double precision and rounded once to fp32.  packed_buf (>= dec_weights_bytes)
+ * and workspace (>= dec_workspace_bytes for max_tokens/max_seqs) are caller-owned
+ * device buffers that must outlive the model, 256-byte aligned.  Synchronises
+ * `stream` before returning. */
+int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, size_t packed_bytes,
+               void* workspace, size_t workspace_bytes, int32_t max_tokens, int32_t max_seqs,
+               void* stream, dec_model** out);
+void dec_destroy(dec_model* m);
+
+/* Read and clear the device error word (synchronises the model's last stream). */
+int dec_device_status(dec_model* m, uint32_t* flags);
+
+/* Debug: when dump is non-NULL, every later dec_prefill/dec_decode copies the
+ * fp32 residual stream x [N, d_model] after the embedding and after every layer
+ * into dump[(i * N + t) * d_model + c], i = 0 .. n_layers (needs
+ * (n_layers+1)*N*d_model floats; the caller sizes it for its largest step).
+ * Layer-by-layer comparison against the oracle (1bit-MONSTER "Byte-identical",
+ * "The validation loop closes"). NULL turns it off. */
+int dec_set_dump(dec_model* m, float* dump, size_t dump_floats);
+
+/* ---- paged KV pool (tinyllm L10.1 section 2.2, KvPool in section 4) -------- */
+/* Layout: pool block b of layer l holds a K slab and a V slab, each
+ * [n_kv_heads][block_tokens][head_dim] elements (f32 in DEC_FP32, f16 in
+ * DEC_BF16_F16KV).  Slab (l, b, is_v) starts at element
+ * ((l * n_blocks + b) * 2 + is_v) * n_kv_heads * block_tokens * head_dim of
+ * the caller's slab buffer; K of KV head h, slot s starts at element
+ * (h * block_tokens + s) * head_dim of its slab (section 3, "Where a key lands"). */
+int dec_pool_bytes(const dec_config* cfg, int32_t n_blocks, size_t* bytes);
+/* n_blocks == 0 is refused (DEC_EINVAL, kv_pool_rejects_zero_capacity).  The
+ * slab memory is caller-owned device memory of >= dec_pool_bytes. */
+int dec_pool_create(const dec_config* cfg, int32_t n_blocks, void* slabs, size_t bytes, dec_pool** out);
+void dec_pool_destroy(dec_pool* p);
+/* All-or-nothing: n blocks with refcount 1 into ids[0..n), or DEC_ECAPACITY and nothing taken. */
+int dec_pool_alloc(dec_pool* p, int32_t n, int32_t* ids);
+int dec_pool_retain(dec_pool* p, int32_t id);  /* refcount + 1; DEC_EBLOCK if not allocated */
+int dec_pool_release(dec_pool* p, int32_t id); /* refcount - 1; at 0 the block is free again */
+int dec_pool_free_blocks(const dec_pool* p, int32_t* n);
+int dec_pool_refcount(const dec_pool* p, int32_t id, int32_t* refs);
+/* Element offset (within the slab buffer) of K (is_v=0) or V of KV head h at
+ * position pos of a sequence with the given block table; the same function the
+ * kernels use.  DEC_ERANGE if the table is too short, DEC_EBLOCK on a bad id. */
+int dec_kv_offset(const dec_pool* p, const int32_t* table, int32_t n_table, int32_t pos, int32_t layer,
+                  int32_t kv_head, int32_t is_v, int64_t* offset);
+
+/* ---- the step ------------------------------------------------------------- */
+/* Prefill (or any mixed step): run the batch's new tokens, write their K/V into
+ * the blocks their tables name, and produce fp32 logits [R, vocab] and greedy ids
+ * [R] (int32, device), R = N for DEC_ROWS_ALL or S for DEC_ROWS_LAST; rows are in
+ * token / sequence order.  logits may be NULL (ids only).  Every block a sequence
+ * reads (positions 0 .. its last new position) must be allocated in `pool`. */
+int dec_prefill(dec_model* m, dec_pool* pool, const dec_batch* b, int32_t rows, float* logits,
+                int32_t* argmax, void* stream);
+
+/* Decode: exactly one new token per sequence (N == S).  Logits [S, vocab] and
+ * ids [S] as for dec_prefill with DEC_ROWS_LAST.  Uses the split-K attention. */
+int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, int32_t* argmax,
+               void* stream);
+
+/* ---- profiling ------------------------------------------------------------
+ * Kernel classes of one step, in launch order. */
+#define DEC_K_EMBED       0 /* embedding gather */
+#define DEC_K_QKV         1 /* RMSNorm + [Wq;Wk;Wv] product */
+#define DEC_K_QKV_POST    2 /* QK-norm + RoPE + KV-cache write */
+#define DEC_K_ATTN        3 /* attention: split-K decode or tiled prefill */
+#define DEC_K_ATTN_MERGE  4 /* decode: merge of the split-K partials */
+#define DEC_K_OPROJ       5 /* O projection + residual */
+#define DEC_K_GATEUP      6 /* RMSNorm + gate/up + SiLU*mul */
+#define DEC_K_DOWN        7 /* down projection + residual */
+#define DEC_K_LMHEAD      8 /* final RMSNorm + LM head + argmax keys */
+#define DEC_K_ARGMAX      9 /* argmax keys -> ids */
+#define DEC_K_COUNT      10
+/* Record CUDA events around every later launch of one kernel class (on the
+ * step's stream) while on != 0. */
+int dec_profile_enable(dec_model* m, int32_t kernel_class, int32_t on);
+/* Synchronise, then return the summed event time and launch count of a class
+ * since the last read, and reset them. */
+int dec_profile_read(dec_model* m, int32_t kernel_class, double* total_ms, int64_t* launches);
+/* Kernels this model launched since the last call (then reset). */
+int dec_launch_count(dec_model* m, int64_t* launches);
+
+/* Test hook: the device conversion the f16 KV store uses (f32 -> f16 round to
+ * nearest even, tinyllm L10.1 section 2.3), applied to n device floats. */
+int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream);
+
+/* Library version string. */
+const char* dec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DEC_H */

@@ -1,0 +1,38 @@
+"""Shared pieces of the GPU parity tests: build a decoder and its oracle from
+the same seeded weights, and run the pages' paths (full, cached, decode)."""
+
+from __future__ import annotations
+
+import numpy as np
+
+from decoder_qwen3_step_gb300 import dec, inputs
+from oracle.compare import TOL_BF16, TOL_FP32, compare
+from oracle.model import DecoderConfig, Oracle
+
+MODES = {"fp32": dec.DEC_FP32, "bf16": dec.DEC_BF16_F16KV}
+TOLS = {"fp32": TOL_FP32, "bf16": TOL_BF16}
+
+
+def make_pair(shape_name, mode, max_positions, max_tokens=4096, max_seqs=64, n_blocks=None, weights=None):
+    import torch  # noqa: F401  (device memory for the decoder)
+    from decoder_qwen3_step_gb300.runtime import Decoder
+
+    shape = inputs.SHAPES[shape_name]
+    w = weights if weights is not None else inputs.make_weights(shape)
+    if n_blocks is None:
+        n_blocks = max_seqs * ((max_positions + 15) // 16) + 8
+    m = Decoder(shape, w, mode=MODES[mode], max_positions=max_positions, max_tokens=max_tokens, max_seqs=max_seqs,
+                n_blocks=n_blocks)
+    orc = Oracle(DecoderConfig(**shape, max_positions=max_positions), w, mode=mode)
+    return m, orc, w
+
+
+def check(dev_logits, dev_ids, ref_logits, mode, what=""):
+    r = compare(dev_logits, ref_logits, TOLS[mode], dev_ids)
+    assert r["passed"], f"{what}: {r}"
+    assert r["argmax_agree"] == r["rows"], f"{what}: {r}"
+    return r
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
