@@ -1,6 +1,7 @@
 // api.cu - the C ABI of libdec (declared in include/dec.h): config checks,
 // weight packing, the paged KV pool's host allocator, batch validation,
 // per-step metadata staging and the launch sequence of one decoder step.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -133,6 +134,17 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
 }
 
 constexpr int kStageSlots = 4;
+constexpr size_t kMaxGraphs = 8;
+
+struct GraphEntry {
+  int S;
+  const void* logits;
+  const void* argmax;
+  const void* slabs;
+  cudaGraphExec_t exec;
+  int64_t n_launch;
+  uint64_t last_use;
+};
 
 }  // namespace
 
@@ -166,6 +178,17 @@ struct dec_model {
   double prof_ms[DEC_K_COUNT];
   int64_t prof_n[DEC_K_COUNT];
   int64_t launches;
+  int num_sms;
+  // tcgen05 products: tensor maps of every bf16 weight matrix and activation buffer
+  bool tc_on;
+  bool tc_ready;
+  std::vector<CUtensorMap> tm_qkv, tm_o, tm_gu, tm_d;
+  CUtensorMap tm_embed, tm_xn, tm_att, tm_act;
+  // captured decode steps
+  bool graphs_on;
+  cudaStream_t cap_stream;
+  std::vector<GraphEntry> graphs;
+  uint64_t graph_clock;
 };
 
 namespace {
@@ -208,6 +231,67 @@ int timed_launch(dec_model* m, int cls, cudaStream_t st, F&& fn, const char* wha
     int rc_ = timed_launch(m, cls, st, [&]() { return (expr); }, #expr);        \
     if (rc_) return rc_;                                                        \
   } while (0)
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map of a row-major [rows, cols] matrix, box 64 x 128, 128-byte swizzle.
+bool bf16_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps for the tcgen05 products (serving mode only); false leaves the
+// CUDA-core products in charge.
+bool build_tensor_maps(dec_model* m) {
+  const dec_config& c = m->cfg;
+  if (c.mode != DEC_BF16_F16KV) return false;
+  const int d = c.d_model, HD = c.n_heads * c.head_dim, F = c.ff_hidden;
+  char* P = m->packed;
+  m->tm_qkv.resize(c.n_layers);
+  m->tm_o.resize(c.n_layers);
+  m->tm_gu.resize(c.n_layers);
+  m->tm_d.resize(c.n_layers);
+  bool ok = true;
+  for (int l = 0; l < c.n_layers; ++l) {
+    char* Lb = P + m->pl.layer0 + (size_t)l * m->pl.layer_stride;
+    ok &= bf16_map(&m->tm_qkv[l], Lb + m->pl.wqkv, qkv_rows(c), d);
+    ok &= bf16_map(&m->tm_o[l], Lb + m->pl.wo, d, HD);
+    ok &= bf16_map(&m->tm_gu[l], Lb + m->pl.wgu, 2 * F, d);
+    ok &= bf16_map(&m->tm_d[l], Lb + m->pl.wd, d, F);
+  }
+  ok &= bf16_map(&m->tm_embed, P + m->pl.embed, c.vocab, d);
+  ok &= bf16_map(&m->tm_xn, m->ws + m->wl.XN, m->Tmax, d);
+  ok &= bf16_map(&m->tm_att, m->ws + m->wl.ATT, m->Tmax, HD);
+  ok &= bf16_map(&m->tm_act, m->ws + m->wl.ACT, m->Tmax, F);
+  return ok;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -317,6 +401,14 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
     m->prof_n[i] = 0;
   }
   m->launches = 0;
+  m->num_sms = 0;
+  cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+  if (m->num_sms <= 0) m->num_sms = 148;
+  m->graphs_on = true;
+  m->tc_on = true;
+  m->tc_ready = build_tensor_maps(m);
+  m->cap_stream = nullptr;
+  m->graph_clock = 0;
   for (int i = 0; i < kStageSlots; ++i) {
     m->stage[i] = nullptr;
     m->stage_ev[i] = nullptr;
@@ -347,6 +439,9 @@ void dec_destroy(dec_model* m) {
     cudaEventDestroy(r.b);
   }
   for (auto e : m->ev_free) cudaEventDestroy(e);
+  for (auto& g : m->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   delete m;
 }
 
@@ -383,6 +478,18 @@ int dec_profile_read(dec_model* m, int32_t kernel_class, double* total_ms, int64
   *launches = m->prof_n[kernel_class];
   m->prof_ms[kernel_class] = 0.0;
   m->prof_n[kernel_class] = 0;
+  return DEC_OK;
+}
+
+int dec_set_tensor_cores(dec_model* m, int32_t on) {
+  if (!m) return fail(DEC_EINVAL, "model is NULL");
+  m->tc_on = on != 0;
+  return DEC_OK;
+}
+
+int dec_set_graphs(dec_model* m, int32_t on) {
+  if (!m) return fail(DEC_EINVAL, "model is NULL");
+  m->graphs_on = on != 0;
   return DEC_OK;
 }
 
@@ -493,6 +600,171 @@ static bool same_shape(const dec_config& a, const dec_config& b) {
          a.block_tokens == b.block_tokens && a.mode == b.mode;
 }
 
+// Everything one step's kernels need, fixed before the first launch.
+struct StepPlan {
+  StepMeta meta;
+  Dims dm;
+  int N, S, R;
+  bool decode;
+  int n_work;
+  int slots;  // decode attention CTAs per (sequence, kv head)
+  bool rows_all;
+  void* slabs;
+  float* logits;
+  int32_t* argmax;
+};
+
+// Queue the kernels of one step on `st` (eager, or into a capture).
+static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
+  const dec_config& c = m->cfg;
+  const bool bf = c.mode == DEC_BF16_F16KV;
+  char* P = m->packed;
+  char* ws = m->ws;
+  const PackedLayout& pl = m->pl;
+  const WsLayout& wl = m->wl;
+  float* X = (float*)(ws + wl.X);
+  void* XN = ws + wl.XN;
+  float* SSQ = (float*)(ws + wl.SSQ);
+  float* RAW = (float*)(ws + wl.RAW);
+  float* Q = (float*)(ws + wl.Q);
+  void* ATT = ws + wl.ATT;
+  void* ACT = ws + wl.ACT;
+  float* PART = (float*)(ws + wl.PART);
+  unsigned long long* KEYS = (unsigned long long*)(ws + wl.KEYS);
+  uint32_t* ERR = (uint32_t*)(ws + wl.ERR);
+  const int d = c.d_model, N = sp.N, R = sp.R;
+  const Dims& dm = sp.dm;
+  auto layer = [&](int l) { return P + pl.layer0 + (size_t)l * pl.layer_stride; };
+  const bool dumping = m->dump && m->dump_floats >= (size_t)(c.n_layers + 1) * N * d;
+  // many-token products go to the tensor cores in the serving mode
+  auto product = [&](const GemvArgs& g, int epi, const CUtensorMap* tw, const CUtensorMap* tx) -> cudaError_t {
+    if (bf && m->tc_on && m->tc_ready && g.T > kGemvMaxTokens && tc_eligible(g))
+      return launch_gemm_tc(g, epi, tw, tx, m->num_sms, ERR, st);
+    return launch_gemv(g, epi, bf, st);
+  };
+
+  EmbedArgs ea{P + pl.embed, sp.meta.ids, N, d, c.vocab, R, (const float*)(layer(0) + pl.attn_norm), X, XN, SSQ, KEYS,
+               ERR};
+  DEC_LAUNCH(DEC_K_EMBED, launch_embed(ea, bf, st));
+  if (dumping) DEC_CUDA(cudaMemcpyAsync(m->dump, X, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, st));
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    char* Lb = layer(l);
+    GemvArgs g{};
+    g.d = d;
+    g.eps = dm.eps;
+    g.F = c.ff_hidden;
+    // RMSNorm + [Wq;Wk;Wv]
+    g.W = Lb + pl.wqkv; g.rows = qkv_rows(c); g.K = d; g.X = XN; g.x_row = nullptr; g.T = N; g.ssq = SSQ;
+    g.out_f32 = RAW;
+    DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV_RAW, bf ? &m->tm_qkv[l] : nullptr, &m->tm_xn));
+    QkvPostArgs qa{RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope),
+                   Q, sp.slabs, l, sp.meta, dm};
+    DEC_LAUNCH(DEC_K_QKV_POST, launch_qkv_post(qa, N, bf, st));
+    // attention
+    AttnArgs aa{Q, sp.slabs, l, sp.meta, dm, ATT, PART, m->NCH, sp.S, 1.0f / std::sqrt((float)c.head_dim)};
+    if (sp.decode) {
+      DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, sp.slots, bf, st));
+      DEC_LAUNCH(DEC_K_ATTN_MERGE, launch_attn_merge(aa, bf, st));
+    } else {
+      DEC_LAUNCH(DEC_K_ATTN, launch_attn_prefill(aa, sp.n_work, bf, st));
+    }
+    // O projection + residual; next GEMM input x * w_mlp
+    GemvArgs go{};
+    go.d = d; go.eps = dm.eps; go.F = c.ff_hidden;
+    go.W = Lb + pl.wo; go.rows = d; go.K = c.n_heads * c.head_dim; go.X = ATT; go.T = N; go.ssq = nullptr;
+    go.X_res = X; go.XN = XN; go.SSQ_out = SSQ; go.w_next = (const float*)(Lb + pl.mlp_norm);
+    DEC_LAUNCH(DEC_K_OPROJ, product(go, EPI_RESID, bf ? &m->tm_o[l] : nullptr, &m->tm_att));
+    // RMSNorm + gate/up + SiLU*mul
+    GemvArgs gu{};
+    gu.d = d; gu.eps = dm.eps; gu.F = c.ff_hidden;
+    gu.W = Lb + pl.wgu; gu.rows = 2 * c.ff_hidden; gu.K = d; gu.X = XN; gu.T = N; gu.ssq = SSQ; gu.act_out = ACT;
+    DEC_LAUNCH(DEC_K_GATEUP, product(gu, EPI_SWIGLU, bf ? &m->tm_gu[l] : nullptr, &m->tm_xn));
+    // down projection + residual; next GEMM input x * (next attention gain | final gain)
+    GemvArgs gd{};
+    gd.d = d; gd.eps = dm.eps; gd.F = c.ff_hidden;
+    gd.W = Lb + pl.wd; gd.rows = d; gd.K = c.ff_hidden; gd.X = ACT; gd.T = N; gd.ssq = nullptr;
+    gd.X_res = X; gd.XN = XN; gd.SSQ_out = SSQ;
+    gd.w_next = l + 1 < c.n_layers ? (const float*)(layer(l + 1) + pl.attn_norm) : (const float*)(P + pl.final_norm);
+    DEC_LAUNCH(DEC_K_DOWN, product(gd, EPI_RESID, bf ? &m->tm_d[l] : nullptr, &m->tm_act));
+    if (dumping)
+      DEC_CUDA(cudaMemcpyAsync(m->dump + (size_t)(l + 1) * N * d, X, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, st));
+  }
+  // final RMSNorm + tied LM head + argmax
+  GemvArgs gl{};
+  gl.d = d; gl.eps = dm.eps; gl.F = c.ff_hidden;
+  // every-row logits read the activations in place (no row indirection)
+  gl.W = P + pl.embed; gl.rows = c.vocab; gl.K = d; gl.X = XN; gl.x_row = sp.rows_all ? nullptr : sp.meta.row_tok;
+  gl.T = R; gl.ssq = SSQ;
+  gl.out_f32 = sp.logits; gl.keys = KEYS;
+  DEC_LAUNCH(DEC_K_LMHEAD, product(gl, EPI_LOGITS, &m->tm_embed, &m->tm_xn));
+  DEC_LAUNCH(DEC_K_ARGMAX, launch_argmax_finalize(KEYS, sp.argmax, R, st));
+  return DEC_OK;
+}
+
+static bool profiling_any(const dec_model* m) {
+  for (int i = 0; i < DEC_K_COUNT; ++i)
+    if (m->prof_on[i]) return true;
+  return false;
+}
+
+// Decode steps of one shape replay a captured CUDA graph: the per-step
+// metadata lives at fixed device addresses (one host->device copy before the
+// replay), so only (S, logits, argmax) key a graph.  A key's first step runs
+// eagerly; its second captures.
+static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st) {
+  GraphEntry* hit = nullptr;
+  for (auto& e : m->graphs)
+    if (e.S == sp.S && e.logits == sp.logits && e.argmax == sp.argmax && e.slabs == sp.slabs) hit = &e;
+  ++m->graph_clock;
+  if (hit && hit->exec) {
+    hit->last_use = m->graph_clock;
+    DEC_CUDA(cudaGraphLaunch(hit->exec, st));
+    m->launches += hit->n_launch;
+    return DEC_OK;
+  }
+  if (!hit) {  // first sighting: run eagerly, remember the key
+    if (m->graphs.size() >= kMaxGraphs) {
+      size_t victim = 0;
+      for (size_t i = 1; i < m->graphs.size(); ++i)
+        if (m->graphs[i].last_use < m->graphs[victim].last_use) victim = i;
+      if (m->graphs[victim].exec) cudaGraphExecDestroy(m->graphs[victim].exec);
+      m->graphs.erase(m->graphs.begin() + victim);
+    }
+    GraphEntry e{};
+    e.S = sp.S;
+    e.logits = sp.logits;
+    e.argmax = sp.argmax;
+    e.slabs = sp.slabs;
+    e.last_use = m->graph_clock;
+    m->graphs.push_back(e);
+    return enqueue_step(m, sp, st);
+  }
+  // second sighting: capture on the model's private stream, then replay on st
+  if (!m->cap_stream) DEC_CUDA(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+  const int64_t before = m->launches;
+  DEC_CUDA(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+  int rc = enqueue_step(m, sp, m->cap_stream);
+  cudaGraph_t graph = nullptr;
+  cudaError_t ec = cudaStreamEndCapture(m->cap_stream, &graph);
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (ec != cudaSuccess) return fail(DEC_ECUDA, "graph capture: %s", cudaGetErrorString(ec));
+  cudaGraphExec_t exec = nullptr;
+  ec = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ec != cudaSuccess) return fail(DEC_ECUDA, "graph instantiate: %s", cudaGetErrorString(ec));
+  hit->exec = exec;
+  hit->n_launch = m->launches - before;
+  m->launches = before;
+  hit->last_use = m->graph_clock;
+  DEC_CUDA(cudaGraphLaunch(exec, st));
+  m->launches += hit->n_launch;
+  return DEC_OK;
+}
+
 static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_mode, float* logits, int32_t* argmax,
                     cudaStream_t st, bool decode) {
   if (!m || !pool || !b || !argmax) return fail(DEC_EINVAL, "NULL argument");
@@ -508,7 +780,6 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
     return fail(DEC_EINVAL, "NULL batch array");
   if (b->seq_start[0] != 0 || b->seq_start[S] != N) return fail(DEC_EINVAL, "seq_start must run from 0 to n_tokens");
   const int B = c.block_tokens;
-  int max_nch = 0;
   for (int s = 0; s < S; ++s) {
     const int a0 = b->seq_start[s], a1 = b->seq_start[s + 1];
     if (a1 <= a0) return fail(DEC_EINVAL, "sequence %d has no new tokens", s);
@@ -529,14 +800,11 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
       if (id < 0 || id >= pool->n_blocks || pool->refs[id] <= 0)
         return fail(DEC_EBLOCK, "sequence %d names block %d which is not allocated", s, id);
     }
-    max_nch = std::max(max_nch, (last + kDecodeChunk) / kDecodeChunk);
   }
   const int R = rows_mode == DEC_ROWS_ALL ? N : S;
 
   // ---- metadata: assemble, stage in pinned memory, one host->device copy ----
-  const int MB = m->MB, Tm = m->Tmax, Sm = m->Smax;
-  (void)Tm;
-  (void)Sm;
+  const int MB = m->MB;
   const int G = c.n_heads / c.n_kv_heads;
   const int QT = prefill_tile_queries(G);
   const int slot = m->stage_next;
@@ -584,99 +852,39 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   o += 3 * work.size();
   if (o > m->wl.meta_ints) return fail(DEC_ERANGE, "step metadata exceeds the workspace");
 
-  char* ws = m->ws;
-  int32_t* dmeta = (int32_t*)(ws + m->wl.META);
+  int32_t* dmeta = (int32_t*)(m->ws + m->wl.META);
   DEC_CUDA(cudaMemcpyAsync(dmeta, H, o * 4, cudaMemcpyHostToDevice, st));
   DEC_CUDA(cudaEventRecord(m->stage_ev[slot], st));
   m->last_stream = st;
 
-  StepMeta meta;
-  meta.ids = b->ids_device ? b->ids_device : dmeta + o_ids;
-  meta.tok_pos = dmeta + o_pos;
-  meta.tok_seq = dmeta + o_seq;
-  meta.seq_start = dmeta + o_start;
-  meta.seq_ctx = dmeta + o_ctx;
-  meta.row_tok = dmeta + o_row;
-  meta.tables = dmeta + o_tab;
-  meta.work = dmeta + o_work;
+  const bool graph = decode && m->graphs_on && !m->dump && !profiling_any(m);
+  if (graph && b->ids_device)  // graphs read ids from the metadata block
+    DEC_CUDA(cudaMemcpyAsync(dmeta + o_ids, b->ids_device, (size_t)N * 4, cudaMemcpyDeviceToDevice, st));
 
-  Dims dm;
-  dm.vocab = c.vocab; dm.d = c.d_model; dm.n_layers = c.n_layers; dm.H = c.n_heads; dm.Hkv = c.n_kv_heads;
-  dm.D = c.head_dim; dm.F = c.ff_hidden; dm.B = B; dm.n_blocks = pool->n_blocks; dm.max_blocks = MB;
-  dm.eps = (float)c.rms_eps;
-
-  const bool bf = c.mode == DEC_BF16_F16KV;
-  char* P = m->packed;
-  const PackedLayout& pl = m->pl;
-  const WsLayout& wl = m->wl;
-  float* X = (float*)(ws + wl.X);
-  void* XN = ws + wl.XN;
-  float* SSQ = (float*)(ws + wl.SSQ);
-  float* RAW = (float*)(ws + wl.RAW);
-  float* Q = (float*)(ws + wl.Q);
-  void* ATT = ws + wl.ATT;
-  void* ACT = ws + wl.ACT;
-  float* PART = (float*)(ws + wl.PART);
-  unsigned long long* KEYS = (unsigned long long*)(ws + wl.KEYS);
-  uint32_t* ERR = (uint32_t*)(ws + wl.ERR);
-  const int d = c.d_model;
-  auto layer = [&](int l) { return P + pl.layer0 + (size_t)l * pl.layer_stride; };
-  const bool dumping = m->dump && m->dump_floats >= (size_t)(c.n_layers + 1) * N * d;
-
-  EmbedArgs ea{P + pl.embed, meta.ids, N, d, c.vocab, R, (const float*)(layer(0) + pl.attn_norm), X, XN, SSQ, KEYS, ERR};
-  DEC_LAUNCH(DEC_K_EMBED, launch_embed(ea, bf, st));
-  if (dumping) DEC_CUDA(cudaMemcpyAsync(m->dump, X, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, st));
-
-  for (int l = 0; l < c.n_layers; ++l) {
-    char* Lb = layer(l);
-    GemvArgs g{};
-    g.d = d;
-    g.eps = dm.eps;
-    g.F = c.ff_hidden;
-    // RMSNorm + [Wq;Wk;Wv]
-    g.W = Lb + pl.wqkv; g.rows = qkv_rows(c); g.K = d; g.X = XN; g.x_row = nullptr; g.T = N; g.ssq = SSQ;
-    g.out_f32 = RAW;
-    DEC_LAUNCH(DEC_K_QKV, launch_gemv(g, EPI_QKV_RAW, bf, st));
-    QkvPostArgs qa{RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope),
-                   Q, pool->slabs, l, meta, dm};
-    DEC_LAUNCH(DEC_K_QKV_POST, launch_qkv_post(qa, N, bf, st));
-    // attention
-    AttnArgs aa{Q, pool->slabs, l, meta, dm, ATT, PART, m->NCH, S, 1.0f / std::sqrt((float)c.head_dim)};
-    if (decode) {
-      DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, max_nch, bf, st));
-      DEC_LAUNCH(DEC_K_ATTN_MERGE, launch_attn_merge(aa, bf, st));
-    } else {
-      DEC_LAUNCH(DEC_K_ATTN, launch_attn_prefill(aa, (int)work.size(), bf, st));
-    }
-    // O projection + residual; next GEMM input x * w_mlp
-    GemvArgs go{};
-    go.d = d; go.eps = dm.eps; go.F = c.ff_hidden;
-    go.W = Lb + pl.wo; go.rows = d; go.K = c.n_heads * c.head_dim; go.X = ATT; go.T = N; go.ssq = nullptr;
-    go.X_res = X; go.XN = XN; go.SSQ_out = SSQ; go.w_next = (const float*)(Lb + pl.mlp_norm);
-    DEC_LAUNCH(DEC_K_OPROJ, launch_gemv(go, EPI_RESID, bf, st));
-    // RMSNorm + gate/up + SiLU*mul
-    GemvArgs gu{};
-    gu.d = d; gu.eps = dm.eps; gu.F = c.ff_hidden;
-    gu.W = Lb + pl.wgu; gu.rows = 2 * c.ff_hidden; gu.K = d; gu.X = XN; gu.T = N; gu.ssq = SSQ; gu.act_out = ACT;
-    DEC_LAUNCH(DEC_K_GATEUP, launch_gemv(gu, EPI_SWIGLU, bf, st));
-    // down projection + residual; next GEMM input x * (next attention gain | final gain)
-    GemvArgs gd{};
-    gd.d = d; gd.eps = dm.eps; gd.F = c.ff_hidden;
-    gd.W = Lb + pl.wd; gd.rows = d; gd.K = c.ff_hidden; gd.X = ACT; gd.T = N; gd.ssq = nullptr;
-    gd.X_res = X; gd.XN = XN; gd.SSQ_out = SSQ;
-    gd.w_next = l + 1 < c.n_layers ? (const float*)(layer(l + 1) + pl.attn_norm) : (const float*)(P + pl.final_norm);
-    DEC_LAUNCH(DEC_K_DOWN, launch_gemv(gd, EPI_RESID, bf, st));
-    if (dumping)
-      DEC_CUDA(cudaMemcpyAsync(m->dump + (size_t)(l + 1) * N * d, X, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, st));
-  }
-  // final RMSNorm + tied LM head + argmax
-  GemvArgs gl{};
-  gl.d = d; gl.eps = dm.eps; gl.F = c.ff_hidden;
-  gl.W = P + pl.embed; gl.rows = c.vocab; gl.K = d; gl.X = XN; gl.x_row = meta.row_tok; gl.T = R; gl.ssq = SSQ;
-  gl.out_f32 = logits; gl.keys = KEYS;
-  DEC_LAUNCH(DEC_K_LMHEAD, launch_gemv(gl, EPI_LOGITS, bf, st));
-  DEC_LAUNCH(DEC_K_ARGMAX, launch_argmax_finalize(KEYS, argmax, R, st));
-  return DEC_OK;
+  StepPlan sp;
+  sp.meta.ids = (b->ids_device && !graph) ? b->ids_device : dmeta + o_ids;
+  sp.meta.tok_pos = dmeta + o_pos;
+  sp.meta.tok_seq = dmeta + o_seq;
+  sp.meta.seq_start = dmeta + o_start;
+  sp.meta.seq_ctx = dmeta + o_ctx;
+  sp.meta.row_tok = dmeta + o_row;
+  sp.meta.tables = dmeta + o_tab;
+  sp.meta.work = dmeta + o_work;
+  sp.dm.vocab = c.vocab; sp.dm.d = c.d_model; sp.dm.n_layers = c.n_layers; sp.dm.H = c.n_heads;
+  sp.dm.Hkv = c.n_kv_heads; sp.dm.D = c.head_dim; sp.dm.F = c.ff_hidden; sp.dm.B = B;
+  sp.dm.n_blocks = pool->n_blocks; sp.dm.max_blocks = MB; sp.dm.eps = (float)c.rms_eps;
+  sp.N = N;
+  sp.S = S;
+  sp.R = R;
+  sp.decode = decode;
+  sp.rows_all = rows_mode == DEC_ROWS_ALL;
+  sp.n_work = (int)work.size();
+  sp.slots = std::min(m->NCH, std::max(1, (4 * m->num_sms + c.n_kv_heads * S - 1) / (c.n_kv_heads * S)));
+  sp.slabs = pool->slabs;
+  sp.logits = logits;
+  sp.argmax = argmax;
+  if (graph) return launch_decode_graph(m, sp, st);
+  return enqueue_step(m, sp, st);
 }
 
 int dec_prefill(dec_model* m, dec_pool* pool, const dec_batch* b, int32_t rows, float* logits, int32_t* argmax,

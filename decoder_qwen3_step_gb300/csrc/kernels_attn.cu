@@ -20,7 +20,6 @@
 
 namespace dec {
 
-template <int N> struct VecN;
 template <typename KT, int N>
 __device__ __forceinline__ void loadN(const KT* p, float* v) {
   if constexpr (N % 8 == 0) {
@@ -32,16 +31,56 @@ __device__ __forceinline__ void loadN(const KT* p, float* v) {
   }
 }
 
+// Raw storage of N cache elements in 32-bit registers, filled by the widest
+// aligned vector loads (16, 8 or 4 bytes); converted to fp32 at use.
+template <typename KT, int N>
+struct Raw {
+  static constexpr int kWords = N * (int)sizeof(KT) / 4;
+  uint32_t w[kWords];
+  __device__ __forceinline__ void load(const KT* p) {
+    constexpr int B = N * (int)sizeof(KT);
+    if constexpr (B % 16 == 0) {
+#pragma unroll
+      for (int i = 0; i < B / 16; ++i) reinterpret_cast<uint4*>(w)[i] = reinterpret_cast<const uint4*>(p)[i];
+    } else if constexpr (B % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < B / 8; ++i) reinterpret_cast<uint2*>(w)[i] = reinterpret_cast<const uint2*>(p)[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < kWords; ++i) w[i] = reinterpret_cast<const uint32_t*>(p)[i];
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) w[i] = 0u;
+  }
+  __device__ __forceinline__ float get(int i) const {
+    if constexpr (sizeof(KT) == 4) {
+      return __uint_as_float(w[i]);
+    } else {
+      return __half2float(reinterpret_cast<const __half*>(w)[i]);
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------
-// Decode attention, split-K.  grid (chunk, kv head, sequence), 4 warps.
+// Decode attention, split-K.  grid (slot, kv head, sequence), 4 warps.  Keys
+// are cut into fixed 64-key chunks (4 blocks of 16; the cut depends only on
+// the position, never on the batch); CTA `slot` handles chunks slot,
+// slot + gridDim.x, ...  Per chunk each warp takes one block: lane (key =
+// lane/2, half = lane%2) loads half a key row for the scores, lane (parity =
+// lane/16, segment = lane%16) loads D/16 dims of 8 value rows; all of a
+// block's loads are issued before any is used.  The G query heads of the
+// group share every K/V load.  The 4 warps' partial softmax states merge in
+// warp order into one (max, sum, o[D]) record per chunk and query head.
 // ---------------------------------------------------------------------------
 template <typename KT, int D, int G>
 __global__ void __launch_bounds__(128) k_attn_decode(AttnArgs a) {
   const Dims& dm = a.dims;
-  const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int g = blockIdx.y, s = blockIdx.z;
   const int ctx = a.meta.seq_ctx[s];
   const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
-  if (c >= nch) return;
+  if ((int)blockIdx.x >= nch) return;
   const int t = a.meta.seq_start[s];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ float qs[G][D];
@@ -51,83 +90,95 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnArgs a) {
     qs[i / D][i % D] = a.Q[((size_t)t * dm.H + g * G + i / D) * D + i % D];
   __syncthreads();
 
-  constexpr int kPerLane = D / 32;  // output dims per lane
-  float m[G], l[G], o[G][kPerLane];
-#pragma unroll
-  for (int i = 0; i < G; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.f;
-#pragma unroll
-    for (int e = 0; e < kPerLane; ++e) o[i][e] = 0.f;
-  }
-  const int bi = c * (kDecodeChunk / 16) + warp;  // block index within the table (B = 16)
-  const int key0 = bi * 16;
-  const int nkeys = min(max(ctx - key0, 0), 16);
-  if (nkeys > 0) {
-    const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
-    const KT* kv = reinterpret_cast<const KT*>(a.kv);
-    const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
-    const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
-    const int key = lane >> 1, hf = lane & 1;
-    constexpr int kHalf = D / 2;
-    float kvals[kHalf];
-    loadN<KT, kHalf>(Kb + key * D + hf * kHalf, kvals);
-    float sc[G];
+  constexpr int kHalf = D / 2;   // score dims per lane
+  constexpr int kSeg = D / 16;   // value dims per lane
+  const KT* kv = reinterpret_cast<const KT*>(a.kv);
+  const int key = lane >> 1, hf = lane & 1;
+  const int par = lane >> 4, seg = lane & 15;
+
+  for (int c = blockIdx.x; c < nch; c += gridDim.x) {
+    const int bi = c * (kDecodeChunk / 16) + warp;  // block index within the table (B = 16)
+    const int nkeys = min(max(ctx - bi * 16, 0), 16);
+    float m[G], l[G], o[G][kSeg];
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-      float acc = 0.f;
+      m[i] = -INFINITY;
+      l[i] = 0.f;
 #pragma unroll
-      for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], kvals[e], acc);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      sc[i] = key < nkeys ? acc * a.scale : -INFINITY;
+      for (int e = 0; e < kSeg; ++e) o[i][e] = 0.f;
     }
-    float p[G];
+    if (nkeys > 0) {
+      const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
+      const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+      const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+      Raw<KT, kHalf> kr;
+      kr.load(Kb + key * D + hf * kHalf);
+      Raw<KT, kSeg> vr[8];
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      m[i] = warp_max(sc[i]);
-      p[i] = key < nkeys ? expf(sc[i] - m[i]) : 0.f;
-      l[i] = warp_sum(hf == 0 ? p[i] : 0.f);
-    }
-    for (int k = 0; k < nkeys; ++k) {
-      float vv[kPerLane];
-      loadN<KT, kPerLane>(Vb + k * D + lane * kPerLane, vv);
+      for (int j = 0; j < 8; ++j) {
+        if (2 * j + par < nkeys)
+          vr[j].load(Vb + (2 * j + par) * D + seg * kSeg);
+        else
+          vr[j].zero();
+      }
+      float p[G];
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        const float pk = __shfl_sync(0xffffffffu, p[i], 2 * k);
+        float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < kPerLane; ++e) o[i][e] = fmaf(pk, vv[e], o[i][e]);
+        for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], kr.get(e), acc);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        const float sc = key < nkeys ? acc * a.scale : -INFINITY;
+        m[i] = warp_max(sc);
+        p[i] = key < nkeys ? expf(sc - m[i]) : 0.f;
+        l[i] = warp_sum(hf == 0 ? p[i] : 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const float pk = __shfl_sync(0xffffffffu, p[i], 2 * (2 * j + par));
+#pragma unroll
+          for (int e = 0; e < kSeg; ++e) o[i][e] = fmaf(pk, vr[j].get(e), o[i][e]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < G; ++i)
+#pragma unroll
+        for (int e = 0; e < kSeg; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], 16);
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      if (lane == 0) {
+        ms[warp][i] = m[i];
+        ls[warp][i] = l[i];
+      }
+      if (lane < 16) {
+#pragma unroll
+        for (int e = 0; e < kSeg; ++e) os[warp][i][seg * kSeg + e] = o[i][e];
       }
     }
-  }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * D; i += 128) {
+      const int h = i / D, dd = i % D;
+      float M = ms[0][h];
 #pragma unroll
-  for (int i = 0; i < G; ++i) {
-    if (lane == 0) {
-      ms[warp][i] = m[i];
-      ls[warp][i] = l[i];
+      for (int w = 1; w < 4; ++w) M = fmaxf(M, ms[w][h]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = ms[w][h] == -INFINITY ? 0.f : expf(ms[w][h] - M);
+        L = fmaf(ls[w][h], f, L);
+        O = fmaf(os[w][h][dd], f, O);
+      }
+      float* part = a.part + (((size_t)s * dm.H + g * G + h) * a.nchunk_cap + c) * (D + 2);
+      if (dd == 0) {
+        part[0] = M;
+        part[1] = L;
+      }
+      part[2 + dd] = O;
     }
-#pragma unroll
-    for (int e = 0; e < kPerLane; ++e) os[warp][i][lane * kPerLane + e] = o[i][e];
-  }
-  __syncthreads();
-  // merge the 4 warps in warp order; write (m, l, o[D]) of this chunk
-  for (int i = threadIdx.x; i < G * D; i += 128) {
-    const int h = i / D, dd = i % D;
-    float M = ms[0][h];
-#pragma unroll
-    for (int w = 1; w < 4; ++w) M = fmaxf(M, ms[w][h]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float f = ms[w][h] == -INFINITY ? 0.f : expf(ms[w][h] - M);
-      L = fmaf(ls[w][h], f, L);
-      O = fmaf(os[w][h][dd], f, O);
-    }
-    float* part = a.part + (((size_t)s * dm.H + g * G + h) * a.nchunk_cap + c) * (D + 2);
-    if (dd == 0) {
-      part[0] = M;
-      part[1] = L;
-    }
-    part[2 + dd] = O;
+    __syncthreads();
   }
 }
 

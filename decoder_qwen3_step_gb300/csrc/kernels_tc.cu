@@ -1,0 +1,359 @@
+// kernels_tc.cu - the weight products of many-token steps on the 5th-generation
+// tensor cores (tcgen05 + TMEM, operands staged by TMA), bf16 x bf16 -> fp32.
+//
+// D[r, t] = sum_k W[r, k] X[t, k]: the weight tile is the M = 128 operand,
+// a tile of 128 token rows the N operand, both K-major with the 128-byte
+// swizzle; K advances 64 elements (one 128-byte swizzle row) per stage.
+// Persistent: one CTA per SM walks the (weight tile, token tile) grid.
+//   warp 0      TMA producer: 4-stage shared-memory ring (full/empty mbarriers)
+//   warp 1      TMEM owner and MMA issuer (one elected lane); two 128-column
+//               fp32 accumulators so the epilogue of one tile overlaps the
+//               MMAs of the next
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, staged through
+//               shared memory into the same fused epilogues as the CUDA-core
+//               products (QKV, residual + next-norm input, SwiGLU, logits)
+// Every mbarrier wait is bounded (about a second); on expiry the kernel sets
+// the device error word, lets copies and MMAs in flight land, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "launch.h"
+
+namespace dec {
+
+constexpr int kTcM = 128, kTcN = 128, kTcK = 64, kTcStages = 4;
+constexpr int kTcThreads = 192;
+constexpr int kTcTileLd = kTcN + 1;
+constexpr uint32_t kTcStageA = kTcM * kTcK * 2;  // 16 KB
+constexpr uint32_t kTcStageB = kTcN * kTcK * 2;  // 16 KB
+constexpr uint32_t kTcAccCols = 128;             // fp32 columns per accumulator
+constexpr uint64_t kWaitLimitNs = 1000000000ull; // 1 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Returns false (and
+// raises the abort flag and the device error word) when it gives up or when
+// another role already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// OR of a flag over the 128 epilogue threads (named barrier 1): every
+// epilogue thread takes the same branch after it, so none can be left
+// waiting at a later barrier.
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+struct TcShared {
+  uint64_t full[kTcStages], empty[kTcStages], tfull[2], tempty[2], mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int consumed;  // stage loads the MMA warp has taken (for the teardown drain)
+};
+
+constexpr size_t kTcSmemBytes =
+    1024 + (size_t)kTcStages * (kTcStageA + kTcStageB) + (size_t)kTcM * kTcTileLd * 4 + kTcN * 4 + sizeof(TcShared);
+
+template <typename AT, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, GemvArgs a,
+              uint32_t* err) {
+  extern __shared__ uint8_t tc_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + kTcStages * kTcStageA;
+  float* tile = reinterpret_cast<float*>(sB + kTcStages * kTcStageB);
+  float* rstd_s = tile + kTcM * kTcTileLd;
+  TcShared* sh = reinterpret_cast<TcShared*>(rstd_s + kTcN);
+  volatile int* abort_flag = &sh->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = a.rows / kTcM;
+  const int n_tiles = (a.T + kTcN - 1) / kTcN;
+  const int n_total = m_tiles * n_tiles;
+  const int nk = a.K / kTcK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&sh->full[i], 1);
+      mbar_init(&sh->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->tfull[i], 1);
+      mbar_init(&sh->tempty[i], 128);
+    }
+    mbar_init(&sh->mma_done, 1);
+    sh->abort_flag = 0;
+    sh->consumed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh->tmem_base)),
+                 "r"(2 * kTcAccCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  int issued = 0;  // producer: stage loads issued
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile_i = blockIdx.x; tile_i < n_total; tile_i += gridDim.x) {
+        const int mt = tile_i % m_tiles, nt = tile_i / m_tiles;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&sh->empty[stage], phase ^ 1, abort_flag, err)) goto producer_done;
+          mbar_expect_tx(&sh->full[stage], kTcStageA + kTcStageB);
+          tma_load_2d(sA + stage * kTcStageA, &tmW, kb * kTcK, mt * kTcM, &sh->full[stage]);
+          tma_load_2d(sB + stage * kTcStageB, &tmX, kb * kTcK, nt * kTcN, &sh->full[stage]);
+          ++issued;
+          if (++stage == kTcStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // tail: every stage released by the MMA commits before the CTA may exit
+      for (int i = 0; i < kTcStages && !*abort_flag; ++i) {
+        if (!mbar_wait(&sh->empty[stage], phase ^ 1, abort_flag, err)) break;
+        if (++stage == kTcStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      constexpr uint32_t idesc = idesc_bf16(kTcM, kTcN);
+      for (int tile_i = blockIdx.x; tile_i < n_total; tile_i += gridDim.x) {
+        if (!mbar_wait(&sh->tempty[acc], acc_phase ^ 1, abort_flag, err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * kTcAccCols;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&sh->full[stage], phase, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kTcStageA), b0 = smem_u32(sB + stage * kTcStageB);
+#pragma unroll
+          for (int k = 0; k < kTcK / 16; ++k)
+            tc_mma(d, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
+          tc_commit(&sh->empty[stage]);  // the stage is free once these MMAs have read it
+          sh->consumed = sh->consumed + 1;
+          if (++stage == kTcStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&sh->tfull[acc]);  // the accumulator is complete once every MMA above is
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      tc_commit(&sh->mma_done);
+    }
+  } else {
+    // epilogue warps: TMEM lane quarter (warp % 4), rows 32*(warp%4) .. +31
+    const int et = threadIdx.x - 64;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile_i = blockIdx.x; tile_i < n_total; tile_i += gridDim.x) {
+      const int mt = tile_i % m_tiles, nt = tile_i / m_tiles;
+      const int t0 = nt * kTcN, ntok = min(kTcN, a.T - t0);
+      epi_bar();  // the previous tile's epilogue is done with tile/rstd_s
+      for (int t = et >> 5; t < kTcN; t += 4) {
+        float r = 1.0f;
+        if (a.ssq && t < ntok) r = row_rstd(a.ssq, t0 + t, a.d, a.eps);
+        if (lane == 0) rstd_s[t] = r;
+      }
+      const bool got = mbar_wait(&sh->tfull[acc], acc_phase, abort_flag, err);
+      if (epi_any(!got)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int slab = 0; slab < kTcN / 32; ++slab) {
+        uint32_t v[32];
+        tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * kTcAccCols + slab * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) tile[row * kTcTileLd + slab * 32 + j] = __uint_as_float(v[j]);
+      }
+      tc_fence_before();
+      mbar_arrive(&sh->tempty[acc]);
+      epi_bar();
+      epilogue<AT, EPI, 128>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, et);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // let what is in flight land before the memory goes away
+    if (threadIdx.x == 0) {
+      for (int j = sh->consumed; j < issued; ++j) {
+        const uint64_t t0 = global_ns();
+        while (!mbar_try(&sh->full[j % kTcStages], (j / kTcStages) & 1) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    if (warp == 1) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try(&sh->mma_done, 0) && global_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kTcAccCols) : "memory");
+  }
+}
+
+template <typename AT, int EPI>
+static cudaError_t tc_one(const GemvArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX, int num_sms, uint32_t* err,
+                          cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<AT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kTcSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int tiles = (a.rows / kTcM) * ((a.T + kTcN - 1) / kTcN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  k_gemm_tc<AT, EPI><<<grid, kTcThreads, kTcSmemBytes, s>>>(*tmW, *tmX, a, err);
+  return cudaGetLastError();
+}
+
+bool tc_eligible(const GemvArgs& a) { return a.rows % kTcM == 0 && a.K % kTcK == 0 && a.T > 0 && a.x_row == nullptr; }
+
+cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, const void* tmW, const void* tmX, int num_sms, uint32_t* err,
+                           cudaStream_t s) {
+  const CUtensorMap* w = reinterpret_cast<const CUtensorMap*>(tmW);
+  const CUtensorMap* x = reinterpret_cast<const CUtensorMap*>(tmX);
+  switch (epi) {
+    case EPI_QKV_RAW: return tc_one<bf16, EPI_QKV_RAW>(a, w, x, num_sms, err, s);
+    case EPI_RESID: return tc_one<bf16, EPI_RESID>(a, w, x, num_sms, err, s);
+    case EPI_SWIGLU: return tc_one<bf16, EPI_SWIGLU>(a, w, x, num_sms, err, s);
+    default: return tc_one<bf16, EPI_LOGITS>(a, w, x, num_sms, err, s);
+  }
+}
+
+}  // namespace dec

@@ -10,6 +10,9 @@ namespace dec {
 
 enum Epi { EPI_QKV_RAW = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
+// Token rows up to which the weight-streaming kernel runs a product.
+constexpr int kGemvMaxTokens = 32;
+
 // One weight-streaming product Y[t, r] = sum_k X[row(t), k] W[r, k] with a
 // fused epilogue.  W is [rows, K] (fp32 or bf16), X is [*, K] (act type).
 struct GemvArgs {
@@ -81,6 +84,13 @@ cudaError_t launch_attn_prefill(const AttnArgs& a, int n_work, bool wbf16, cudaS
 enum PackMode { PACK_IDENTITY = 0, PACK_GATE = 1, PACK_UP = 2 };
 cudaError_t launch_pack(void* dst, const float* src, int rows, int cols, int mode, bool wbf16, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
+
+// tcgen05 products (bf16 weights and activations): eligible shapes and launch.
+// tmW / tmX point at host copies of CUtensorMap (weights [rows, K] and
+// activations [T, K], bf16, box 64 x 128, 128-byte swizzle).
+bool tc_eligible(const GemvArgs& a);
+cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, const void* tmW, const void* tmX, int num_sms, uint32_t* err,
+                           cudaStream_t s);
 
 // Query rows of one prefill attention tile (query-head rows / group size).
 int prefill_tile_queries(int G);

@@ -177,6 +177,12 @@ class Decoder:
         dec.check(self.L.dec_device_status(self.handle, C.byref(f)), "dec_device_status")
         return f.value
 
+    def set_tensor_cores(self, on: bool) -> None:
+        dec.check(self.L.dec_set_tensor_cores(self.handle, 1 if on else 0), "dec_set_tensor_cores")
+
+    def set_graphs(self, on: bool) -> None:
+        dec.check(self.L.dec_set_graphs(self.handle, 1 if on else 0), "dec_set_graphs")
+
     def set_dump(self, buf: torch.Tensor | None):
         if buf is None:
             dec.check(self.L.dec_set_dump(self.handle, None, 0), "dec_set_dump")

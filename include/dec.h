@@ -217,7 +217,17 @@ int dec_profile_enable(dec_model* m, int32_t kernel_class, int32_t on);
 /* Synchronise, then return the summed event time and launch count of a class
  * since the last read, and reset them. */
 int dec_profile_read(dec_model* m, int32_t kernel_class, double* total_ms, int64_t* launches);
-/* Kernels this model launched since the last call (then reset). */
+/* Serving mode: products of more than 32 token rows run on the tcgen05
+ * tensor cores (on by default); off routes them to the CUDA-core kernels. */
+int dec_set_tensor_cores(dec_model* m, int32_t on);
+/* Decode steps replay CUDA graphs (on by default): the first step of a given
+ * (batch size, logits, argmax, pool) runs eagerly, the second is captured on
+ * a private stream, later ones replay it on the caller's stream.  Off: every
+ * step launches its kernels one by one.  Graphs are bypassed while a dump or
+ * a profiled kernel class is active. */
+int dec_set_graphs(dec_model* m, int32_t on);
+/* Kernels this model launched since the last call (then reset); a replayed
+ * graph counts every kernel it contains. */
 int dec_launch_count(dec_model* m, int64_t* launches);
 
 /* Test hook: the device conversion the f16 KV store uses (f32 -> f16 round to

@@ -107,6 +107,24 @@ def test_small_batched_full_cached_and_decode():
         m.close()
 
 
+def test_tensor_core_products_match_cuda_core_products():
+    """Serving mode, 300-token prefill of the small shape: the tcgen05 products
+    and the CUDA-core products add the same bf16 products in another order."""
+    m, orc, w = make_pair("small", "bf16", max_positions=512, max_tokens=512, max_seqs=4)
+    ids = inputs.make_ids(8192, 300, seed=77)
+    out = {}
+    for tc in (True, False):
+        m.set_tensor_cores(tc)
+        t = m.blocks_for(300)
+        lg, am = m.prefill([(ids, 0, t)])
+        out[tc] = (np_(lg), np_(am))
+        m.release(t)
+    assert m.device_status() == 0
+    assert np.abs(out[True][0] - out[False][0]).max() < 2e-3
+    check(out[True][0], out[True][1], orc.full(ids), "bf16", "tensor cores vs oracle")
+    m.close()
+
+
 def test_batched_forward_equals_single(tiny):
     mode, m, orc, w = tiny
     a = inputs.make_ids(512, 13, seed=3)
@@ -175,6 +193,30 @@ def test_run_once_returns_its_blocks(tiny):
         m.prefill([(inputs.make_ids(512, 10, seed=i), 0, t)], rows=dec.DEC_ROWS_LAST)
         m.release(t)
     assert m.free_blocks() == free
+
+
+def test_graph_replay_matches_eager_decode_bitwise(tiny):
+    mode, m, orc, w = tiny
+    prompts = [inputs.make_ids(512, n, seed=20 + n) for n in (5, 9, 16)]
+    outs = {}
+    for graphs in (False, True):
+        m.set_graphs(graphs)
+        tabs = [m.blocks_for(40) for _ in prompts]
+        m.prefill([(p, 0, t) for p, t in zip(prompts, tabs)], rows=dec.DEC_ROWS_LAST)
+        lg = torch.empty((3, 512), dtype=torch.float32, device=m.device)
+        ids = [torch.empty((3,), dtype=torch.int32, device=m.device) for _ in range(2)]
+        ids[0].fill_(7)
+        rows = []
+        for i in range(6):  # eager, capture, then replays; ids fed back on the device
+            m.decode([([0], len(p) + i, t) for p, t in zip(prompts, tabs)], device_ids=ids[i & 1],
+                     out=(lg, ids[(i + 1) & 1]))
+            rows.append(np_(lg).copy())
+        outs[graphs] = np.stack(rows)
+        for t in tabs:
+            m.release(t)
+    m.set_graphs(True)
+    assert np.array_equal(outs[False], outs[True])
+    assert m.device_status() == 0
 
 
 def test_f16_kv_store_rounds_to_nearest_even_bit_exact():
