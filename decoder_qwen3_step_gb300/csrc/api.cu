@@ -896,6 +896,46 @@ int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, 
   return run_step(m, pool, b, DEC_ROWS_LAST, logits, argmax, (cudaStream_t)stream, true);
 }
 
+int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X, int32_t T, float* Y, int32_t path,
+                      void* stream) {
+  if (!m || !X || !Y || T < 1 || which < 0 || which > 4 || (path != 0 && path != 1))
+    return fail(DEC_EINVAL, "bad arguments");
+  const dec_config& c = m->cfg;
+  if (which < 4 && (layer < 0 || layer >= c.n_layers)) return fail(DEC_EINVAL, "bad layer");
+  const bool bf = c.mode == DEC_BF16_F16KV;
+  const int d = c.d_model, HD = c.n_heads * c.head_dim, F = c.ff_hidden;
+  char* Lb = m->packed + m->pl.layer0 + (size_t)(which < 4 ? layer : 0) * m->pl.layer_stride;
+  GemvArgs g{};
+  g.d = d;
+  g.eps = (float)c.rms_eps;
+  g.F = F;
+  g.X = X;
+  g.T = T;
+  g.out_f32 = Y;
+  const CUtensorMap* tw = nullptr;
+  switch (which) {
+    case 0: g.W = Lb + m->pl.wqkv; g.rows = qkv_rows(c); g.K = d; if (bf) tw = &m->tm_qkv[layer]; break;
+    case 1: g.W = Lb + m->pl.wo; g.rows = d; g.K = HD; if (bf) tw = &m->tm_o[layer]; break;
+    case 2: g.W = Lb + m->pl.wgu; g.rows = 2 * F; g.K = d; if (bf) tw = &m->tm_gu[layer]; break;
+    case 3: g.W = Lb + m->pl.wd; g.rows = d; g.K = F; if (bf) tw = &m->tm_d[layer]; break;
+    default: g.W = m->packed + m->pl.embed; g.rows = c.vocab; g.K = d; if (bf) tw = &m->tm_embed; break;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t* ERR = (uint32_t*)(m->ws + m->wl.ERR);
+  if (path == 1) {
+    if (!bf || !m->tc_ready || T <= kGemvMaxTokens || !tc_eligible(g))
+      return fail(DEC_EINVAL, "the tensor-core path needs the serving mode, T > %d and a 128-row multiple",
+                  kGemvMaxTokens);
+    CUtensorMap tx;
+    if (!bf16_map(&tx, X, T, g.K)) return fail(DEC_ECUDA, "tensor map for X failed");
+    DEC_CUDA(launch_gemm_tc(g, EPI_QKV_RAW, tw, &tx, m->num_sms, ERR, st));
+  } else {
+    DEC_CUDA(launch_gemv(g, EPI_QKV_RAW, bf, st));
+  }
+  m->last_stream = st;
+  return DEC_OK;
+}
+
 int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream) {
   if (n < 0 || (n > 0 && (!in || !out))) return fail(DEC_EINVAL, "bad arguments");
   DEC_CUDA(launch_f32_to_f16(in, out, n, (cudaStream_t)stream));

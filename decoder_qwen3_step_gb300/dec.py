@@ -26,7 +26,7 @@ EXPORTS = (
     "dec_device_status", "dec_set_dump", "dec_pool_bytes", "dec_pool_create", "dec_pool_destroy", "dec_pool_alloc",
     "dec_pool_retain", "dec_pool_release", "dec_pool_free_blocks", "dec_pool_refcount", "dec_kv_offset",
     "dec_prefill", "dec_decode", "dec_f32_to_f16", "dec_version", "dec_profile_enable", "dec_profile_read",
-    "dec_launch_count", "dec_set_graphs", "dec_set_tensor_cores",
+    "dec_launch_count", "dec_set_graphs", "dec_set_tensor_cores", "dec_debug_product",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax")
 
@@ -94,6 +94,7 @@ def lib() -> C.CDLL:
             "dec_launch_count": (I, [V, C.POINTER(I64)]),
             "dec_set_graphs": (I, [V, C.c_int32]),
             "dec_set_tensor_cores": (I, [V, C.c_int32]),
+            "dec_debug_product": (I, [V, C.c_int32, C.c_int32, V, C.c_int32, V, C.c_int32, V]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -234,6 +234,15 @@ int dec_launch_count(dec_model* m, int64_t* launches);
  * nearest even, tinyllm L10.1 section 2.3), applied to n device floats. */
 int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream);
 
+/* Test hook: one raw weight product Y[t, r] = sum_k X[t, k] W[r, k] with a
+ * packed matrix of the model: which = 0 [Wq;Wk;Wv], 1 Wo, 2 gate/up (rows
+ * interleaved in groups of 8), 3 Wd, 4 the embedding; layer ignored for 4.
+ * X: device [T, K], fp32 in DEC_FP32, bf16 in DEC_BF16_F16KV; Y: device fp32
+ * [T, rows].  path 0 runs the CUDA-core kernels, path 1 the tcgen05 kernel
+ * (serving mode and T > 32 only, else DEC_EINVAL). */
+int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X, int32_t T, float* Y, int32_t path,
+                      void* stream);
+
 /* Library version string. */
 const char* dec_version(void);
 

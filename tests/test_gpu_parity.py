@@ -109,19 +109,35 @@ def test_small_batched_full_cached_and_decode():
 
 def test_tensor_core_products_match_cuda_core_products():
     """Serving mode, 300-token prefill of the small shape: the tcgen05 products
-    and the CUDA-core products add the same bf16 products in another order."""
+    and the CUDA-core products add the same bf16 products in another order.
+    After the first layer the residual streams agree to within the bf16
+    rounding of the attention output (a summation-order difference in k can
+    flip an f16 key, which moves many bf16 roundings downstream); both end
+    results are held to the oracle.  The products alone are pinned exactly in
+    test_gpu_products.py."""
     m, orc, w = make_pair("small", "bf16", max_positions=512, max_tokens=512, max_seqs=4)
     ids = inputs.make_ids(8192, 300, seed=77)
-    out = {}
+    out, dumps = {}, {}
     for tc in (True, False):
         m.set_tensor_cores(tc)
+        dump = torch.zeros((9, 300, 512), dtype=torch.float32, device=m.device)
+        m.set_dump(dump)
         t = m.blocks_for(300)
         lg, am = m.prefill([(ids, 0, t)])
+        torch.cuda.synchronize()
+        m.set_dump(None)
         out[tc] = (np_(lg), np_(am))
+        dumps[tc] = np_(dump)
         m.release(t)
     assert m.device_status() == 0
-    assert np.abs(out[True][0] - out[False][0]).max() < 2e-3
-    check(out[True][0], out[True][1], orc.full(ids), "bf16", "tensor cores vs oracle")
+    x1_tc, x1_cc = dumps[True][1], dumps[False][1]
+    scale = np.abs(x1_cc).max()
+    assert np.abs(x1_tc - x1_cc).max() <= 5e-3 * scale, (np.abs(x1_tc - x1_cc).max(), scale)
+    ref = orc.full(ids)
+    check(out[True][0], out[True][1], ref, "bf16", "tensor cores vs oracle")
+    check(out[False][0], out[False][1], ref, "bf16", "CUDA cores vs oracle")
+    print("tc vs cuda-core: layer-1 residual max diff", float(np.abs(x1_tc - x1_cc).max()), "scale", float(scale),
+          "logits max diff", float(np.abs(out[True][0] - out[False][0]).max()))
     m.close()
 
 
