@@ -107,7 +107,7 @@ PackedLayout packed_layout(const dec_config& c) {
 }
 
 struct WsLayout {
-  size_t X, XN, SSQ, RAW, Q, ATT, ACT, PART, META, KEYS, ERR, total;
+  size_t X, XN, SSQ, RAW, Q, ATT, ACT, PART, ACNT, META, KEYS, ERR, total;
   size_t meta_ints;
 };
 
@@ -124,6 +124,7 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
   L.ATT = take((size_t)T * HD * a);
   L.ACT = take((size_t)T * c.ff_hidden * a);
   L.PART = take((size_t)S * c.n_heads * max_chunks_of(c) * (c.head_dim + 2) * 4);
+  L.ACNT = take((size_t)S * c.n_kv_heads * 4);
   // ids, tok_pos, tok_seq, row_tok [T]; seq_start [S+1]; seq_ctx [S]; tables [S*MB]; work [3*(T+S)]
   L.meta_ints = 4 * (size_t)T + 2 * (size_t)S + 1 + (size_t)S * max_blocks_of(c) + 3 * ((size_t)T + S);
   L.META = take(L.meta_ints * 4);
@@ -184,6 +185,7 @@ struct dec_model {
   bool tc_ready;
   std::vector<CUtensorMap> tm_qkv, tm_o, tm_gu, tm_d;
   CUtensorMap tm_embed, tm_xn, tm_att, tm_act;
+  CUtensorMap tm_xn32, tm_att32, tm_act32;  // 32-row boxes for decode products
   // captured decode steps
   bool graphs_on;
   cudaStream_t cap_stream;
@@ -253,12 +255,12 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 tensor map of a row-major [rows, cols] matrix, box 64 x 128, 128-byte swizzle.
-bool bf16_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols) {
+bool bf16_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -288,6 +290,9 @@ bool build_tensor_maps(dec_model* m) {
   ok &= bf16_map(&m->tm_xn, m->ws + m->wl.XN, m->Tmax, d);
   ok &= bf16_map(&m->tm_att, m->ws + m->wl.ATT, m->Tmax, HD);
   ok &= bf16_map(&m->tm_act, m->ws + m->wl.ACT, m->Tmax, F);
+  ok &= bf16_map(&m->tm_xn32, m->ws + m->wl.XN, m->Tmax, d, 32);
+  ok &= bf16_map(&m->tm_att32, m->ws + m->wl.ATT, m->Tmax, HD, 32);
+  ok &= bf16_map(&m->tm_act32, m->ws + m->wl.ACT, m->Tmax, F, 32);
   return ok;
 }
 
@@ -378,6 +383,7 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
     DEC_CUDA(launch_pack(Lb + pl.wd, w->w_down[l], d, F, PACK_IDENTITY, bf, s));
   }
   DEC_CUDA(cudaMemsetAsync((char*)workspace + wl.ERR, 0, 64, s));
+  DEC_CUDA(cudaMemsetAsync((char*)workspace + wl.ACNT, 0, (size_t)max_seqs * c.n_kv_heads * 4, s));
   DEC_CUDA(cudaStreamSynchronize(s));
 
   dec_model* m = new dec_model();
@@ -637,9 +643,12 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   auto layer = [&](int l) { return P + pl.layer0 + (size_t)l * pl.layer_stride; };
   const bool dumping = m->dump && m->dump_floats >= (size_t)(c.n_layers + 1) * N * d;
   // many-token products go to the tensor cores in the serving mode
-  auto product = [&](const GemvArgs& g, int epi, const CUtensorMap* tw, const CUtensorMap* tx) -> cudaError_t {
+  auto product = [&](const GemvArgs& g, int epi, const CUtensorMap* tw, const CUtensorMap* tx,
+                     const CUtensorMap* tx32) -> cudaError_t {
     if (bf && m->tc_on && m->tc_ready && g.T > kGemvMaxTokens && tc_eligible(g))
       return launch_gemm_tc(g, epi, tw, tx, m->num_sms, ERR, st);
+    if (bf && m->tc_on && m->tc_ready && tc_skinny_eligible(g))
+      return launch_gemm_tc_skinny(g, epi, tw, tx32, ERR, true, st);
     return launch_gemv(g, epi, bf, st);
   };
 
@@ -657,15 +666,15 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     // RMSNorm + [Wq;Wk;Wv]
     g.W = Lb + pl.wqkv; g.rows = qkv_rows(c); g.K = d; g.X = XN; g.x_row = nullptr; g.T = N; g.ssq = SSQ;
     g.out_f32 = RAW;
-    DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV_RAW, bf ? &m->tm_qkv[l] : nullptr, &m->tm_xn));
+    DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV_RAW, bf ? &m->tm_qkv[l] : nullptr, &m->tm_xn, &m->tm_xn32));
     QkvPostArgs qa{RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope),
                    Q, sp.slabs, l, sp.meta, dm};
     DEC_LAUNCH(DEC_K_QKV_POST, launch_qkv_post(qa, N, bf, st));
     // attention
-    AttnArgs aa{Q, sp.slabs, l, sp.meta, dm, ATT, PART, m->NCH, sp.S, 1.0f / std::sqrt((float)c.head_dim)};
+    AttnArgs aa{Q, sp.slabs, l, sp.meta, dm, ATT, PART, m->NCH, sp.S, 1.0f / std::sqrt((float)c.head_dim),
+                (int*)(ws + wl.ACNT)};
     if (sp.decode) {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, sp.slots, bf, st));
-      DEC_LAUNCH(DEC_K_ATTN_MERGE, launch_attn_merge(aa, bf, st));
     } else {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_prefill(aa, sp.n_work, bf, st));
     }
@@ -674,19 +683,19 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     go.d = d; go.eps = dm.eps; go.F = c.ff_hidden;
     go.W = Lb + pl.wo; go.rows = d; go.K = c.n_heads * c.head_dim; go.X = ATT; go.T = N; go.ssq = nullptr;
     go.X_res = X; go.XN = XN; go.SSQ_out = SSQ; go.w_next = (const float*)(Lb + pl.mlp_norm);
-    DEC_LAUNCH(DEC_K_OPROJ, product(go, EPI_RESID, bf ? &m->tm_o[l] : nullptr, &m->tm_att));
+    DEC_LAUNCH(DEC_K_OPROJ, product(go, EPI_RESID, bf ? &m->tm_o[l] : nullptr, &m->tm_att, &m->tm_att32));
     // RMSNorm + gate/up + SiLU*mul
     GemvArgs gu{};
     gu.d = d; gu.eps = dm.eps; gu.F = c.ff_hidden;
     gu.W = Lb + pl.wgu; gu.rows = 2 * c.ff_hidden; gu.K = d; gu.X = XN; gu.T = N; gu.ssq = SSQ; gu.act_out = ACT;
-    DEC_LAUNCH(DEC_K_GATEUP, product(gu, EPI_SWIGLU, bf ? &m->tm_gu[l] : nullptr, &m->tm_xn));
+    DEC_LAUNCH(DEC_K_GATEUP, product(gu, EPI_SWIGLU, bf ? &m->tm_gu[l] : nullptr, &m->tm_xn, &m->tm_xn32));
     // down projection + residual; next GEMM input x * (next attention gain | final gain)
     GemvArgs gd{};
     gd.d = d; gd.eps = dm.eps; gd.F = c.ff_hidden;
     gd.W = Lb + pl.wd; gd.rows = d; gd.K = c.ff_hidden; gd.X = ACT; gd.T = N; gd.ssq = nullptr;
     gd.X_res = X; gd.XN = XN; gd.SSQ_out = SSQ;
     gd.w_next = l + 1 < c.n_layers ? (const float*)(layer(l + 1) + pl.attn_norm) : (const float*)(P + pl.final_norm);
-    DEC_LAUNCH(DEC_K_DOWN, product(gd, EPI_RESID, bf ? &m->tm_d[l] : nullptr, &m->tm_act));
+    DEC_LAUNCH(DEC_K_DOWN, product(gd, EPI_RESID, bf ? &m->tm_d[l] : nullptr, &m->tm_act, &m->tm_act32));
     if (dumping)
       DEC_CUDA(cudaMemcpyAsync(m->dump + (size_t)(l + 1) * N * d, X, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, st));
   }
@@ -694,10 +703,10 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   GemvArgs gl{};
   gl.d = d; gl.eps = dm.eps; gl.F = c.ff_hidden;
   // every-row logits read the activations in place (no row indirection)
-  gl.W = P + pl.embed; gl.rows = c.vocab; gl.K = d; gl.X = XN; gl.x_row = sp.rows_all ? nullptr : sp.meta.row_tok;
+  gl.W = P + pl.embed; gl.rows = c.vocab; gl.K = d; gl.X = XN; gl.x_row = (sp.rows_all || sp.decode) ? nullptr : sp.meta.row_tok;
   gl.T = R; gl.ssq = SSQ;
   gl.out_f32 = sp.logits; gl.keys = KEYS;
-  DEC_LAUNCH(DEC_K_LMHEAD, product(gl, EPI_LOGITS, &m->tm_embed, &m->tm_xn));
+  DEC_LAUNCH(DEC_K_LMHEAD, product(gl, EPI_LOGITS, &m->tm_embed, &m->tm_xn, &m->tm_xn32));
   DEC_LAUNCH(DEC_K_ARGMAX, launch_argmax_finalize(KEYS, sp.argmax, R, st));
   return DEC_OK;
 }
@@ -898,7 +907,7 @@ int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, 
 
 int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X, int32_t T, float* Y, int32_t path,
                       void* stream) {
-  if (!m || !X || !Y || T < 1 || which < 0 || which > 4 || (path != 0 && path != 1))
+  if (!m || !X || !Y || T < 1 || which < 0 || which > 4 || path < 0 || path > 2)
     return fail(DEC_EINVAL, "bad arguments");
   const dec_config& c = m->cfg;
   if (which < 4 && (layer < 0 || layer >= c.n_layers)) return fail(DEC_EINVAL, "bad layer");
@@ -922,7 +931,13 @@ int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X,
   }
   cudaStream_t st = (cudaStream_t)stream;
   uint32_t* ERR = (uint32_t*)(m->ws + m->wl.ERR);
-  if (path == 1) {
+  if (path == 2) {
+    if (!bf || !m->tc_ready || !tc_skinny_eligible(g))
+      return fail(DEC_EINVAL, "the decode tensor-core path needs the serving mode, T <= 32 and a 128-row multiple");
+    CUtensorMap tx;
+    if (!bf16_map(&tx, X, T, g.K, 32)) return fail(DEC_ECUDA, "tensor map for X failed");
+    DEC_CUDA(launch_gemm_tc_skinny(g, EPI_QKV_RAW, tw, &tx, ERR, false, st));
+  } else if (path == 1) {
     if (!bf || !m->tc_ready || T <= kGemvMaxTokens || !tc_eligible(g))
       return fail(DEC_EINVAL, "the tensor-core path needs the serving mode, T > %d and a 128-row multiple",
                   kGemvMaxTokens);

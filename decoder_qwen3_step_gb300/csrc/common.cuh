@@ -50,6 +50,14 @@ struct StepMeta {
   const int32_t* work;      // prefill attention tiles: [n_work, 3] = (seq, first token, n tokens)
 };
 
+// ---- programmatic dependent launch ------------------------------------------
+// Let the next kernel of the stream begin launching (it still waits for this
+// kernel's completion before it reads anything this kernel wrote).
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the previous kernel of the stream has completed and its writes
+// are visible; a no-op for a kernel launched without programmatic serialisation.
+__device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- element loads as fp32 ------------------------------------------------
 __device__ __forceinline__ void load8(const float* p, float* v) {
   float4 a = *reinterpret_cast<const float4*>(p);

@@ -67,15 +67,126 @@ struct Raw {
 // Decode attention, split-K.  grid (slot, kv head, sequence), 4 warps.  Keys
 // are cut into fixed 64-key chunks (4 blocks of 16; the cut depends only on
 // the position, never on the batch); CTA `slot` handles chunks slot,
-// slot + gridDim.x, ...  Per chunk each warp takes one block: lane (key =
-// lane/2, half = lane%2) loads half a key row for the scores, lane (parity =
-// lane/16, segment = lane%16) loads D/16 dims of 8 value rows; all of a
-// block's loads are issued before any is used.  The G query heads of the
-// group share every K/V load.  The 4 warps' partial softmax states merge in
-// warp order into one (max, sum, o[D]) record per chunk and query head.
+// slot + gridDim.x, ... and loads chunk i+1 into registers while it computes
+// chunk i.  Per chunk each warp takes one block: lane (key = lane/2, half =
+// lane%2) holds half a key row for the scores, lane (parity = lane/16,
+// segment = lane%16) D/16 dims of 8 value rows; every load is 128-bit where
+// the row allows.  The G query heads of the group share every K/V load.  The
+// 4 warps' softmax states merge in warp order into one (max, sum, o[D])
+// record per chunk and query head; the last CTA of a (sequence, KV head) to
+// finish merges all records in chunk order and writes the attention output,
+// then re-arms the counter.
 // ---------------------------------------------------------------------------
+template <typename KT, int D>
+struct DecodeRegs {
+  Raw<KT, D / 2> k;
+  Raw<KT, D / 16> v[8];
+};
+
+template <typename KT, int D>
+__device__ __forceinline__ void decode_load(const AttnArgs& a, int s, int g, int c, int ctx, int warp, int lane,
+                                            DecodeRegs<KT, D>& r) {
+  const Dims& dm = a.dims;
+  const int bi = c * (kDecodeChunk / 16) + warp;
+  const int nkeys = min(max(ctx - bi * 16, 0), 16);
+  if (nkeys <= 0) return;
+  const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
+  const KT* kv = reinterpret_cast<const KT*>(a.kv);
+  const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+  const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+  const int key = lane >> 1, hf = lane & 1, par = lane >> 4, seg = lane & 15;
+  r.k.load(Kb + key * D + hf * (D / 2));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (2 * j + par < nkeys)
+      r.v[j].load(Vb + (2 * j + par) * D + seg * (D / 16));
+    else
+      r.v[j].zero();
+  }
+}
+
 template <typename KT, int D, int G>
+__device__ __forceinline__ void decode_chunk(const AttnArgs& a, int s, int g, int c, int ctx, int warp, int lane,
+                                             const DecodeRegs<KT, D>& r, const float (*qs)[D], float (*ms)[G],
+                                             float (*ls)[G], float (*os)[G][D]) {
+  constexpr int kHalf = D / 2, kSeg = D / 16;
+  const Dims& dm = a.dims;
+  const int bi = c * (kDecodeChunk / 16) + warp;
+  const int nkeys = min(max(ctx - bi * 16, 0), 16);
+  const int key = lane >> 1, hf = lane & 1, par = lane >> 4, seg = lane & 15;
+  float m[G], l[G], o[G][kSeg];
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kSeg; ++e) o[i][e] = 0.f;
+  }
+  if (nkeys > 0) {
+    float p[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], r.k.get(e), acc);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      const float sc = key < nkeys ? acc * a.scale : -INFINITY;
+      m[i] = warp_max(sc);
+      p[i] = key < nkeys ? expf(sc - m[i]) : 0.f;
+      l[i] = warp_sum(hf == 0 ? p[i] : 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const float pk = __shfl_sync(0xffffffffu, p[i], 2 * (2 * j + par));
+#pragma unroll
+        for (int e = 0; e < kSeg; ++e) o[i][e] = fmaf(pk, r.v[j].get(e), o[i][e]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+#pragma unroll
+      for (int e = 0; e < kSeg; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], 16);
+  }
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    if (lane == 0) {
+      ms[warp][i] = m[i];
+      ls[warp][i] = l[i];
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int e = 0; e < kSeg; ++e) os[warp][i][seg * kSeg + e] = o[i][e];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += 128) {
+    const int h = i / D, dd = i % D;
+    float M = ms[0][h];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) M = fmaxf(M, ms[w][h]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = ms[w][h] == -INFINITY ? 0.f : expf(ms[w][h] - M);
+      L = fmaf(ls[w][h], f, L);
+      O = fmaf(os[w][h][dd], f, O);
+    }
+    float* part = a.part + (((size_t)s * dm.H + g * G + h) * a.nchunk_cap + c) * (D + 2);
+    if (dd == 0) {
+      part[0] = M;
+      part[1] = L;
+    }
+    part[2 + dd] = O;
+  }
+  __syncthreads();
+}
+
+template <typename KT, typename AT, int D, int G>
 __global__ void __launch_bounds__(128) k_attn_decode(AttnArgs a) {
+  pdl_launch_next();
+  pdl_wait_prev();
   const Dims& dm = a.dims;
   const int g = blockIdx.y, s = blockIdx.z;
   const int ctx = a.meta.seq_ctx[s];
@@ -86,122 +197,53 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnArgs a) {
   __shared__ float qs[G][D];
   __shared__ float ms[4][G], ls[4][G];
   __shared__ float os[4][G][D];
+  __shared__ int last_flag;
   for (int i = threadIdx.x; i < G * D; i += 128)
     qs[i / D][i % D] = a.Q[((size_t)t * dm.H + g * G + i / D) * D + i % D];
+
+  DecodeRegs<KT, D> ra, rb;
+  int c = blockIdx.x;
+  decode_load<KT, D>(a, s, g, c, ctx, warp, lane, ra);
   __syncthreads();
-
-  constexpr int kHalf = D / 2;   // score dims per lane
-  constexpr int kSeg = D / 16;   // value dims per lane
-  const KT* kv = reinterpret_cast<const KT*>(a.kv);
-  const int key = lane >> 1, hf = lane & 1;
-  const int par = lane >> 4, seg = lane & 15;
-
-  for (int c = blockIdx.x; c < nch; c += gridDim.x) {
-    const int bi = c * (kDecodeChunk / 16) + warp;  // block index within the table (B = 16)
-    const int nkeys = min(max(ctx - bi * 16, 0), 16);
-    float m[G], l[G], o[G][kSeg];
-#pragma unroll
-    for (int i = 0; i < G; ++i) {
-      m[i] = -INFINITY;
-      l[i] = 0.f;
-#pragma unroll
-      for (int e = 0; e < kSeg; ++e) o[i][e] = 0.f;
-    }
-    if (nkeys > 0) {
-      const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
-      const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
-      const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
-      Raw<KT, kHalf> kr;
-      kr.load(Kb + key * D + hf * kHalf);
-      Raw<KT, kSeg> vr[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (2 * j + par < nkeys)
-          vr[j].load(Vb + (2 * j + par) * D + seg * kSeg);
-        else
-          vr[j].zero();
-      }
-      float p[G];
-#pragma unroll
-      for (int i = 0; i < G; ++i) {
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], kr.get(e), acc);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        const float sc = key < nkeys ? acc * a.scale : -INFINITY;
-        m[i] = warp_max(sc);
-        p[i] = key < nkeys ? expf(sc - m[i]) : 0.f;
-        l[i] = warp_sum(hf == 0 ? p[i] : 0.f);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int i = 0; i < G; ++i) {
-          const float pk = __shfl_sync(0xffffffffu, p[i], 2 * (2 * j + par));
-#pragma unroll
-          for (int e = 0; e < kSeg; ++e) o[i][e] = fmaf(pk, vr[j].get(e), o[i][e]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < G; ++i)
-#pragma unroll
-        for (int e = 0; e < kSeg; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], 16);
-    }
-#pragma unroll
-    for (int i = 0; i < G; ++i) {
-      if (lane == 0) {
-        ms[warp][i] = m[i];
-        ls[warp][i] = l[i];
-      }
-      if (lane < 16) {
-#pragma unroll
-        for (int e = 0; e < kSeg; ++e) os[warp][i][seg * kSeg + e] = o[i][e];
-      }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += 128) {
-      const int h = i / D, dd = i % D;
-      float M = ms[0][h];
-#pragma unroll
-      for (int w = 1; w < 4; ++w) M = fmaxf(M, ms[w][h]);
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float f = ms[w][h] == -INFINITY ? 0.f : expf(ms[w][h] - M);
-        L = fmaf(ls[w][h], f, L);
-        O = fmaf(os[w][h][dd], f, O);
-      }
-      float* part = a.part + (((size_t)s * dm.H + g * G + h) * a.nchunk_cap + c) * (D + 2);
-      if (dd == 0) {
-        part[0] = M;
-        part[1] = L;
-      }
-      part[2 + dd] = O;
-    }
-    __syncthreads();
+  while (true) {
+    int cn = c + gridDim.x;
+    if (cn < nch) decode_load<KT, D>(a, s, g, cn, ctx, warp, lane, rb);
+    decode_chunk<KT, D, G>(a, s, g, c, ctx, warp, lane, ra, qs, ms, ls, os);
+    if (cn >= nch) break;
+    c = cn;
+    cn = c + gridDim.x;
+    if (cn < nch) decode_load<KT, D>(a, s, g, cn, ctx, warp, lane, ra);
+    decode_chunk<KT, D, G>(a, s, g, c, ctx, warp, lane, rb, qs, ms, ls, os);
+    if (cn >= nch) break;
+    c = cn;
   }
-}
 
-// Merge the chunk partials of one (sequence, query head) in chunk order.
-template <typename AT, int D>
-__global__ void k_attn_combine(AttnArgs a) {
-  const Dims& dm = a.dims;
-  const int s = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
-  const int ctx = a.meta.seq_ctx[s];
-  const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
-  const int t = a.meta.seq_start[s];
-  const float* part = a.part + ((size_t)s * dm.H + h) * a.nchunk_cap * (D + 2);
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, part[c * (D + 2)]);
-  float L = 0.f, O = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const float* p = part + c * (D + 2);
-    const float f = expf(p[0] - M);
-    L = fmaf(p[1], f, L);
-    O = fmaf(p[2 + dd], f, O);
+  // the last CTA of this (sequence, KV head) merges the chunk records in chunk order
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int active = min((int)gridDim.x, nch);
+    last_flag = atomicAdd(a.counters + s * dm.Hkv + g, 1) == active - 1;
   }
+  __syncthreads();
+  if (!last_flag) return;
+  __threadfence();
   AT* out = reinterpret_cast<AT*>(a.ATT);
-  out[((size_t)t * dm.H + h) * D + dd] = from_f32<AT>(O / L);
+  for (int i = threadIdx.x; i < G * D; i += 128) {
+    const int h = i / D, dd = i % D;
+    const float* part = a.part + ((size_t)s * dm.H + g * G + h) * a.nchunk_cap * (D + 2);
+    float M = -INFINITY;
+    for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(part + cc * (D + 2)));
+    float L = 0.f, O = 0.f;
+    for (int cc = 0; cc < nch; ++cc) {
+      const float* p = part + cc * (D + 2);
+      const float f = expf(__ldcg(p) - M);
+      L = fmaf(__ldcg(p + 1), f, L);
+      O = fmaf(__ldcg(p + 2 + dd), f, O);
+    }
+    out[((size_t)t * dm.H + g * G + h) * D + dd] = from_f32<AT>(O / L);
+  }
+  if (threadIdx.x == 0) a.counters[s * dm.Hkv + g] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -216,6 +258,8 @@ constexpr int kPfKeys = 32;
 
 template <typename KT, typename AT, int D, int G>
 __global__ void __launch_bounds__(128) k_attn_prefill(AttnArgs a) {
+  pdl_launch_next();
+  pdl_wait_prev();
   constexpr int LD = D + 4;  // padded row stride (floats)
   constexpr int kDimGroups = D / 32;
   extern __shared__ __align__(16) float sm[];
@@ -376,13 +420,7 @@ int prefill_tile_queries(int G) { return kPfRows / G; }
 template <typename KT, typename AT, int D, int G>
 static cudaError_t attn_decode_t(const AttnArgs& a, int nchunk, cudaStream_t s) {
   dim3 grid(nchunk, a.dims.Hkv, a.S);
-  k_attn_decode<KT, D, G><<<grid, 128, 0, s>>>(a);
-  return cudaGetLastError();
-}
-
-template <typename KT, typename AT, int D, int G>
-static cudaError_t attn_merge_t(const AttnArgs& a, int, cudaStream_t s) {
-  k_attn_combine<AT, D><<<dim3(a.S, a.dims.H), D, 0, s>>>(a);
+  k_attn_decode<KT, AT, D, G><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -415,11 +453,6 @@ static cudaError_t attn_prefill_t(const AttnArgs& a, int n_work, cudaStream_t s)
 cudaError_t launch_attn_decode(const AttnArgs& a, int nchunk, bool wbf16, cudaStream_t s) {
   if (wbf16) DEC_DISPATCH_DG(attn_decode_t, __half, bf16, nchunk, s);
   DEC_DISPATCH_DG(attn_decode_t, float, float, nchunk, s);
-}
-
-cudaError_t launch_attn_merge(const AttnArgs& a, bool wbf16, cudaStream_t s) {
-  if (wbf16) DEC_DISPATCH_DG(attn_merge_t, __half, bf16, 0, s);
-  DEC_DISPATCH_DG(attn_merge_t, float, float, 0, s);
 }
 
 cudaError_t launch_attn_prefill(const AttnArgs& a, int n_work, bool wbf16, cudaStream_t s) {

@@ -22,6 +22,8 @@ namespace dec {
 // ---------------------------------------------------------------------------
 template <typename WT, typename AT>
 __global__ void __launch_bounds__(256) k_embed(EmbedArgs a) {
+  pdl_launch_next();
+  pdl_wait_prev();
   const int t = blockIdx.x;
   int id = a.ids[t];
   if (id < 0 || id >= a.vocab) {
@@ -55,6 +57,8 @@ constexpr int kGemvMaxT = kGemvMaxTokens;  // above this the tiled kernel runs
 
 template <typename WT, typename AT, int EPI>
 __global__ void __launch_bounds__(kGemvThreads) k_gemv(GemvArgs a) {
+  pdl_launch_next();
+  pdl_wait_prev();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   AT* xs = reinterpret_cast<AT*>(smem_raw);  // [kGemvTok][K]
   __shared__ float outs[kGemvRows * kGemvTok];
@@ -133,6 +137,8 @@ constexpr int kTLd = kTM + 4;
 
 template <typename WT, typename AT, int EPI>
 __global__ void __launch_bounds__(kTThreads) k_gemm_tiled(GemvArgs a) {
+  pdl_launch_next();
+  pdl_wait_prev();
   extern __shared__ __align__(16) float tsm[];
   float* As = tsm;                      // [2][kTK][kTLd]   tokens
   float* Bs = tsm + 2 * kTK * kTLd;     // [2][kTK][kTLd]   weight rows
@@ -224,6 +230,8 @@ __global__ void __launch_bounds__(kTThreads) k_gemm_tiled(GemvArgs a) {
 // ---------------------------------------------------------------------------
 template <typename KT>
 __global__ void k_qkv_post(QkvPostArgs a) {
+  pdl_launch_next();
+  pdl_wait_prev();
   extern __shared__ float buf[];  // [warps][D]
   const Dims& dm = a.dims;
   const int t = blockIdx.x;
@@ -266,6 +274,8 @@ __global__ void k_qkv_post(QkvPostArgs a) {
 }
 
 __global__ void k_argmax_finalize(const unsigned long long* keys, int32_t* ids, int R) {
+  pdl_launch_next();
+  pdl_wait_prev();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < R) ids[r] = (int32_t)(0xFFFFFFFFu - (uint32_t)(keys[r] & 0xFFFFFFFFull));
 }

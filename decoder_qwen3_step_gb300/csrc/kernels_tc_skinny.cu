@@ -1,0 +1,273 @@
+// kernels_tc_skinny.cu - weight products of decode steps (at most 32 token
+// rows) on the tcgen05 tensor cores.
+//
+// D[r, t] = sum_k W[r, k] X[t, k] with the 128-row weight tile as the M
+// operand and the (up to) 32 token rows as N = 32.  A step of 1..32 tokens
+// only streams weights, so the grid is made wide by splitting K: the KS CTAs
+// of one weight tile form a thread-block cluster, each multiplies its K range
+// into its own TMEM, copies the 128 x 32 partial tile to shared memory, and
+// after a cluster barrier CTA z sums rows [16z, 16z + 16) over the cluster's
+// tiles in rank order through distributed shared memory (deterministic) and
+// runs the fused epilogue on them.
+//
+// Launched with programmatic dependent launch: the TMA producer issues its
+// first weight tiles before griddepcontrol.wait, so the weight stream of this
+// product overlaps the tail of the previous kernel; activations, norms and
+// the residual are touched only after the wait.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace dec {
+
+constexpr int kSkM = 128, kSkN = 32, kSkK = 64, kSkStages = 4;
+constexpr int kSkThreads = 192;
+constexpr int kSkLd = kSkN + 1;
+constexpr uint32_t kSkStageA = kSkM * kSkK * 2;  // 16 KB
+constexpr uint32_t kSkStageB = kSkN * kSkK * 2;  // 4 KB
+constexpr uint32_t kSkCols = 32;
+
+struct SkShared {
+  uint64_t full[kSkStages], empty[kSkStages], tfull, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int consumed;
+};
+
+constexpr int kSkRedRows = 64;  // reduced rows per CTA when the K split is >= 2
+constexpr size_t kSkSmemBytes = 1024 + (size_t)kSkStages * (kSkStageA + kSkStageB) + (size_t)kSkM * kSkLd * 4 +
+                                (size_t)kSkRedRows * kSkLd * 4 + kSkN * 4 + sizeof(SkShared);
+
+template <typename AT, int EPI>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    k_gemm_tc_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, GemvArgs a,
+                     int ks, uint32_t* err) {
+  extern __shared__ uint8_t sk_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sk_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + kSkStages * kSkStageA;
+  float* tile = reinterpret_cast<float*>(sB + kSkStages * kSkStageB);  // [128][33] this CTA's partial
+  float* red = tile + kSkM * kSkLd;                                     // [<=64][33] reduced rows
+  float* rstd_s = red + kSkRedRows * kSkLd;
+  SkShared* sh = reinterpret_cast<SkShared*>(rstd_s + kSkN);
+  volatile int* abort_flag = &sh->abort_flag;
+
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int z = (int)cluster_rank();
+  const int mt = blockIdx.x / ks;
+  const int nkb = a.K / kSkK / ks;  // K blocks of this CTA
+  const int kb0 = z * nkb;
+  const int ntok = a.T;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSkStages; ++i) {
+      mbar_init(&sh->full[i], 1);
+      mbar_init(&sh->empty[i], 1);
+    }
+    mbar_init(&sh->tfull, 1);
+    mbar_init(&sh->mma_done, 1);
+    sh->abort_flag = 0;
+    sh->consumed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh->tmem_base)),
+                 "r"(kSkCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  int issued = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // weight tiles first: they do not depend on the previous kernel
+      const int pre = nkb < kSkStages ? nkb : kSkStages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(&sh->full[i], kSkStageA + kSkStageB);
+        tma_load_2d(sA + i * kSkStageA, &tmW, (kb0 + i) * kSkK, mt * kSkM, &sh->full[i]);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * kSkStageB, &tmX, (kb0 + i) * kSkK, 0, &sh->full[i]);
+      issued = pre;
+      int stage = pre % kSkStages;
+      uint32_t phase = pre == kSkStages ? 1 : 0;
+      for (int i = pre; i < nkb; ++i) {
+        if (!mbar_wait(&sh->empty[stage], phase ^ 1, abort_flag, err)) break;
+        mbar_expect_tx(&sh->full[stage], kSkStageA + kSkStageB);
+        tma_load_2d(sA + stage * kSkStageA, &tmW, (kb0 + i) * kSkK, mt * kSkM, &sh->full[stage]);
+        tma_load_2d(sB + stage * kSkStageB, &tmX, (kb0 + i) * kSkK, 0, &sh->full[stage]);
+        ++issued;
+        if (++stage == kSkStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      for (int i = 0; i < kSkStages && !*abort_flag; ++i) {  // tail: all stages released
+        if (!mbar_wait(&sh->empty[stage], phase ^ 1, abort_flag, err)) break;
+        if (++stage == kSkStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      constexpr uint32_t idesc = idesc_bf16(kSkM, kSkN);
+      bool ok = true;
+      for (int i = 0; i < nkb; ++i) {
+        if (!mbar_wait(&sh->full[stage], phase, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + stage * kSkStageA), b0 = smem_u32(sB + stage * kSkStageB);
+#pragma unroll
+        for (int k = 0; k < kSkK / 16; ++k) tc_mma(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc, (i | k) != 0);
+        tc_commit(&sh->empty[stage]);
+        sh->consumed = sh->consumed + 1;
+        if (++stage == kSkStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok) tc_commit(&sh->tfull);
+      tc_commit(&sh->mma_done);
+    }
+  } else {
+    const int et = threadIdx.x - 64;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    pdl_wait();
+    for (int t = et >> 5; t < kSkN; t += 4) {
+      float r = 1.0f;
+      if (a.ssq && t < ntok) r = row_rstd(a.ssq, t, a.d, a.eps);
+      if (lane == 0) rstd_s[t] = r;
+    }
+    const bool got = mbar_wait(&sh->tfull, 0, abort_flag, err);
+    if (!epi_any(!got)) {
+      tc_fence_after();
+      uint32_t v[32];
+      tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16), v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) tile[row * kSkLd + j] = __uint_as_float(v[j]);
+    }
+  }
+
+  cluster_sync();  // every partial tile of the cluster is in shared memory
+  if (warp >= 2) {
+    const int et = threadIdx.x - 64;
+    const int rows_per = ks <= 8 ? kSkM / ks : 16;
+    const int r_lo = z * rows_per;
+    if (!*abort_flag && r_lo < kSkM) {
+      const float* src = tile;
+      if (ks > 1) {
+        for (int i = et; i < rows_per * kSkN; i += 128) {
+          const int rr = i / kSkN, t = i % kSkN;
+          const float* p = tile + (r_lo + rr) * kSkLd + t;
+          float sum = 0.f;
+          for (int q = 0; q < ks; ++q) sum += dsmem_ld(dsmem_addr(p, (uint32_t)q));
+          red[rr * kSkLd + t] = sum;
+        }
+        src = red;
+      } else {
+        src = tile + r_lo * kSkLd;
+      }
+      epi_bar();
+      epilogue<AT, EPI, 128>(a, src, kSkLd, mt * kSkM + r_lo, rows_per, 0, ntok, rstd_s, et);
+    }
+  }
+  cluster_sync();  // no CTA leaves while another still reads its tile
+
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      for (int j = sh->consumed; j < issued; ++j) {
+        const uint64_t t0 = global_ns();
+        while (!mbar_try(&sh->full[j % kSkStages], (j / kSkStages) & 1) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    if (warp == 1) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try(&sh->mma_done, 0) && global_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kSkCols) : "memory");
+  }
+}
+
+// Split factor: the smallest power of two giving at least 128 CTAs, at most 16
+// and at most the number of 64-wide K blocks (which it must divide).
+int skinny_splits(int rows, int K) {
+  const int m_tiles = rows / kSkM, nkb = K / kSkK;
+  int ks = 1;
+  while (ks < 16 && m_tiles * ks < 128 && nkb % (2 * ks) == 0) ks *= 2;
+  return ks;
+}
+
+bool tc_skinny_eligible(const GemvArgs& a) {
+  return a.rows % kSkM == 0 && a.K % kSkK == 0 && a.T >= 1 && a.T <= kSkN && a.x_row == nullptr;
+}
+
+template <typename AT, int EPI>
+static cudaError_t skinny_one(const GemvArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX, uint32_t* err,
+                              bool pdl, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc_skinny<AT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSkSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_gemm_tc_skinny<AT, EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int ks = skinny_splits(a.rows, a.K);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.rows / kSkM) * ks, 1, 1);
+  cfg.blockDim = dim3(kSkThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSkSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeClusterDimension;
+  attr[n].val.clusterDim.x = ks;
+  attr[n].val.clusterDim.y = 1;
+  attr[n].val.clusterDim.z = 1;
+  ++n;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc_skinny<AT, EPI>, *tmW, *tmX, a, ks, err);
+}
+
+cudaError_t launch_gemm_tc_skinny(const GemvArgs& a, int epi, const void* tmW, const void* tmX, uint32_t* err,
+                                  bool pdl, cudaStream_t s) {
+  const CUtensorMap* w = reinterpret_cast<const CUtensorMap*>(tmW);
+  const CUtensorMap* x = reinterpret_cast<const CUtensorMap*>(tmX);
+  switch (epi) {
+    case EPI_QKV_RAW: return skinny_one<bf16, EPI_QKV_RAW>(a, w, x, err, pdl, s);
+    case EPI_RESID: return skinny_one<bf16, EPI_RESID>(a, w, x, err, pdl, s);
+    case EPI_SWIGLU: return skinny_one<bf16, EPI_SWIGLU>(a, w, x, err, pdl, s);
+    default: return skinny_one<bf16, EPI_LOGITS>(a, w, x, err, pdl, s);
+  }
+}
+
+}  // namespace dec

@@ -69,6 +69,7 @@ struct AttnArgs {
   int nchunk_cap;
   int S;
   float scale;      // 1/sqrt(D)
+  int* counters;    // decode: finished CTAs per (sequence, kv head), zero between launches
 };
 
 // Launchers; `wbf16` selects bf16 weights / activations / f16 KV (serving
@@ -78,7 +79,6 @@ cudaError_t launch_gemv(const GemvArgs& a, int epi, bool wbf16, cudaStream_t s);
 cudaError_t launch_qkv_post(const QkvPostArgs& a, int T, bool wbf16, cudaStream_t s);
 cudaError_t launch_argmax_finalize(const unsigned long long* keys, int32_t* ids, int R, cudaStream_t s);
 cudaError_t launch_attn_decode(const AttnArgs& a, int nchunk, bool wbf16, cudaStream_t s);
-cudaError_t launch_attn_merge(const AttnArgs& a, bool wbf16, cudaStream_t s);
 cudaError_t launch_attn_prefill(const AttnArgs& a, int n_work, bool wbf16, cudaStream_t s);
 // Packing: dst row map modes.
 enum PackMode { PACK_IDENTITY = 0, PACK_GATE = 1, PACK_UP = 2 };
@@ -91,6 +91,13 @@ cudaError_t launch_f32_to_f16(const float* in, uint16_t* out, int64_t n, cudaStr
 bool tc_eligible(const GemvArgs& a);
 cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, const void* tmW, const void* tmX, int num_sms, uint32_t* err,
                            cudaStream_t s);
+
+// tcgen05 products of decode steps (1..32 token rows; activation maps with a
+// 32-row box), cluster split-K; pdl launches with programmatic serialisation.
+bool tc_skinny_eligible(const GemvArgs& a);
+int skinny_splits(int rows, int K);
+cudaError_t launch_gemm_tc_skinny(const GemvArgs& a, int epi, const void* tmW, const void* tmX, uint32_t* err,
+                                  bool pdl, cudaStream_t s);
 
 // Query rows of one prefill attention tile (query-head rows / group size).
 int prefill_tile_queries(int G);

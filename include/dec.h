@@ -204,7 +204,7 @@ int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, 
 #define DEC_K_QKV         1 /* RMSNorm + [Wq;Wk;Wv] product */
 #define DEC_K_QKV_POST    2 /* QK-norm + RoPE + KV-cache write */
 #define DEC_K_ATTN        3 /* attention: split-K decode or tiled prefill */
-#define DEC_K_ATTN_MERGE  4 /* decode: merge of the split-K partials */
+#define DEC_K_ATTN_MERGE  4 /* reserved (the split-K merge is fused into DEC_K_ATTN) */
 #define DEC_K_OPROJ       5 /* O projection + residual */
 #define DEC_K_GATEUP      6 /* RMSNorm + gate/up + SiLU*mul */
 #define DEC_K_DOWN        7 /* down projection + residual */
@@ -217,8 +217,8 @@ int dec_profile_enable(dec_model* m, int32_t kernel_class, int32_t on);
 /* Synchronise, then return the summed event time and launch count of a class
  * since the last read, and reset them. */
 int dec_profile_read(dec_model* m, int32_t kernel_class, double* total_ms, int64_t* launches);
-/* Serving mode: products of more than 32 token rows run on the tcgen05
- * tensor cores (on by default); off routes them to the CUDA-core kernels. */
+/* Serving mode: the weight products run on the tcgen05 tensor cores (on by
+ * default); off routes them to the CUDA-core kernels. */
 int dec_set_tensor_cores(dec_model* m, int32_t on);
 /* Decode steps replay CUDA graphs (on by default): the first step of a given
  * (batch size, logits, argmax, pool) runs eagerly, the second is captured on
@@ -239,7 +239,8 @@ int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream);
  * interleaved in groups of 8), 3 Wd, 4 the embedding; layer ignored for 4.
  * X: device [T, K], fp32 in DEC_FP32, bf16 in DEC_BF16_F16KV; Y: device fp32
  * [T, rows].  path 0 runs the CUDA-core kernels, path 1 the tcgen05 kernel
- * (serving mode and T > 32 only, else DEC_EINVAL). */
+ * for many tokens (serving mode, T > 32), path 2 the tcgen05 kernel for
+ * decode steps (serving mode, T <= 32); otherwise DEC_EINVAL. */
 int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X, int32_t T, float* Y, int32_t path,
                       void* stream);
 

@@ -66,7 +66,7 @@ def test_every_product_against_float64(mode):
             W = bf16_round(W)
         W = W.astype(np.float64)
         K = W.shape[1]
-        for T in (7, 300):
+        for T in (1, 7, 32, 300):
             Xf = rng.standard_normal((T, K)).astype(np.float32)
             if mode == "bf16":
                 Xf = bf16_round(Xf)
@@ -75,7 +75,9 @@ def test_every_product_against_float64(mode):
                 X = torch.from_numpy(Xf).cuda()
             ref = Xf.astype(np.float64) @ W.T
             scale = np.abs(Xf).astype(np.float64) @ np.abs(W).T  # bound on the rounding of each sum
-            paths = [0] + ([1] if mode == "bf16" and T > 32 and W.shape[0] % 128 == 0 else [])
+            paths = [0]
+            if mode == "bf16" and W.shape[0] % 128 == 0:
+                paths.append(1 if T > 32 else 2)
             for path in paths:
                 Y = run_product(m, which, layer, X, path)
                 err = np.abs(Y - ref) / np.maximum(scale, 1e-30)
