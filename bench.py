@@ -138,7 +138,7 @@ def our_arm(args, rank, world):
     e2e_steps = max(8, args.steps // 4)
     b1_steps = max(32, args.steps)
     # positions every sequence may reach: warmup, 2 profiled steps, timed, e2e, batch-1 (last sequence only)
-    extra = args.warmup + 2 + args.steps + e2e_steps + 3 + b1_steps + 16
+    extra = args.warmup + 2 + args.steps + e2e_steps + 3 + b1_steps + 2 + 16
     max_positions = max(((max(lens) + extra + 15) // 16) * 16, 4096 + 64)
     weights = inputs.make_weights(shape)
     blocks_needed = sum((L + extra) // 16 + 1 for L in lens) + 4 * (4096 // 16 + 2) + 200
@@ -271,10 +271,20 @@ def our_arm(args, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     b1_ms = e0.elapsed_time(e1) / b1_steps
+    # kernel-class shares of a batch-1 step (two extra steps with events, untimed)
+    profile_classes(m, range(len(dec.KERNEL_CLASSES)), True)
+    for i in range(2):
+        m.decode([([0], p1, tables[s1])], device_ids=b1_ids[i & 1], out=(lg1, b1_ids[(i + 1) & 1]))
+        p1 += 1
+    b1_cls = {name: read_profile(m, c) for c, name in enumerate(dec.KERNEL_CLASSES)}
+    profile_classes(m, range(len(dec.KERNEL_CLASSES)), False)
+    b1_tot = sum(v[0] for v in b1_cls.values()) or 1e-9
     b1_bytes = WEIGHT_BYTES_BF16 + (b1_ctx / b1_steps) * KV_BYTES_PER_CTX_TOKEN_LAYER * L
     decode_b1 = {"tokens_per_s": round(1e3 / b1_ms, 1), "ms_per_token": round(b1_ms, 4),
                  "hbm_frac": round(b1_bytes / (b1_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
-                 "bytes_per_token": int(b1_bytes), "context": p1}
+                 "bytes_per_token": int(b1_bytes), "context": p1,
+                 "kernel_us_per_step": {k: round(v[0] * 1e3 / 2, 1) for k, v in b1_cls.items() if v[1]},
+                 "kernel_share": {k: round(v[0] / b1_tot, 4) for k, v in b1_cls.items() if v[1]}}
 
     # ---- chunked prefill: 4 x 4096 tokens, 512-token chunks interleaved across sequences ----
     pf_ids = [inputs.make_ids(V, 4096, seed=200 + s) for s in range(4)]

@@ -139,6 +139,7 @@ constexpr size_t kMaxGraphs = 8;
 
 struct GraphEntry {
   int S;
+  int slots;
   const void* logits;
   const void* argmax;
   const void* slabs;
@@ -719,12 +720,13 @@ static bool profiling_any(const dec_model* m) {
 
 // Decode steps of one shape replay a captured CUDA graph: the per-step
 // metadata lives at fixed device addresses (one host->device copy before the
-// replay), so only (S, logits, argmax) key a graph.  A key's first step runs
+// replay), so (S, attention grid, logits, argmax, pool) key a graph.  A key's first step runs
 // eagerly; its second captures.
 static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   GraphEntry* hit = nullptr;
   for (auto& e : m->graphs)
-    if (e.S == sp.S && e.logits == sp.logits && e.argmax == sp.argmax && e.slabs == sp.slabs) hit = &e;
+    if (e.S == sp.S && e.slots == sp.slots && e.logits == sp.logits && e.argmax == sp.argmax && e.slabs == sp.slabs)
+      hit = &e;
   ++m->graph_clock;
   if (hit && hit->exec) {
     hit->last_use = m->graph_clock;
@@ -742,6 +744,7 @@ static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st
     }
     GraphEntry e{};
     e.S = sp.S;
+    e.slots = sp.slots;
     e.logits = sp.logits;
     e.argmax = sp.argmax;
     e.slabs = sp.slabs;
@@ -811,6 +814,8 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
     }
   }
   const int R = rows_mode == DEC_ROWS_ALL ? N : S;
+  int max_ctx = 0;
+  for (int s = 0; s < S; ++s) max_ctx = std::max(max_ctx, b->positions[b->seq_start[s + 1] - 1] + 1);
 
   // ---- metadata: assemble, stage in pinned memory, one host->device copy ----
   const int MB = m->MB;
@@ -888,7 +893,9 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   sp.decode = decode;
   sp.rows_all = rows_mode == DEC_ROWS_ALL;
   sp.n_work = (int)work.size();
-  sp.slots = std::min(m->NCH, std::max(1, (4 * m->num_sms + c.n_kv_heads * S - 1) / (c.n_kv_heads * S)));
+  // decode attention grid: one CTA per 128-key chunk of the longest sequence, rounded
+  // up to a multiple of 4 chunks so a captured graph serves 512 positions of growth
+  sp.slots = std::min(m->NCH, ((max_ctx + kDecodeChunk - 1) / kDecodeChunk + 3) / 4 * 4);
   sp.slabs = pool->slabs;
   sp.logits = logits;
   sp.argmax = argmax;

@@ -64,56 +64,62 @@ struct Raw {
 };
 
 // ---------------------------------------------------------------------------
-// Decode attention, split-K.  grid (slot, kv head, sequence), 4 warps.  Keys
-// are cut into fixed 64-key chunks (4 blocks of 16; the cut depends only on
-// the position, never on the batch); CTA `slot` handles chunks slot,
-// slot + gridDim.x, ... and loads chunk i+1 into registers while it computes
-// chunk i.  Per chunk each warp takes one block: lane (key = lane/2, half =
-// lane%2) holds half a key row for the scores, lane (parity = lane/16,
-// segment = lane%16) D/16 dims of 8 value rows; every load is 128-bit where
-// the row allows.  The G query heads of the group share every K/V load.  The
-// 4 warps' softmax states merge in warp order into one (max, sum, o[D])
-// record per chunk and query head; the last CTA of a (sequence, KV head) to
-// finish merges all records in chunk order and writes the attention output,
-// then re-arms the counter.
+// Decode attention, split-K.  grid (chunk, kv head, sequence), 8 warps.  Keys
+// are cut into fixed 128-key chunks (8 blocks of 16; the cut depends only on
+// the position, never on the batch), one chunk per CTA and one block per
+// warp, so every K/V load of the chunk is in flight at once.  Lane (key =
+// lane/2, half = lane%2) holds half a key row for the scores, lane (parity =
+// lane/16, segment = lane%16) D/16 dims of 8 value rows; loads are 128-bit
+// where the row allows.  The G query heads of the group share every K/V load.
+// The 8 warps' softmax states merge in warp order into one (max, sum, o[D])
+// record per chunk and query head.  The last CTA of a (sequence, KV head) to
+// finish merges all records in chunk order, writes the attention output and
+// re-arms the counter.
 // ---------------------------------------------------------------------------
-template <typename KT, int D>
-struct DecodeRegs {
-  Raw<KT, D / 2> k;
-  Raw<KT, D / 16> v[8];
-};
+constexpr int kDecWarps = kDecodeChunk / 16;
 
-template <typename KT, int D>
-__device__ __forceinline__ void decode_load(const AttnArgs& a, int s, int g, int c, int ctx, int warp, int lane,
-                                            DecodeRegs<KT, D>& r) {
+template <typename KT, typename AT, int D, int G>
+__global__ void __launch_bounds__(kDecWarps * 32, 2) k_attn_decode(AttnArgs a) {
+  pdl_launch_next();
+  pdl_wait_prev();
+  constexpr int kHalf = D / 2, kSeg = D / 16, kThreads = kDecWarps * 32;
   const Dims& dm = a.dims;
-  const int bi = c * (kDecodeChunk / 16) + warp;
+  const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int ctx = a.meta.seq_ctx[s];
+  const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
+  if (c >= nch) return;
+  const int t = a.meta.seq_start[s];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float qs[G][D];
+  __shared__ float ms[kDecWarps][G], ls[kDecWarps][G];
+  __shared__ float os[kDecWarps][G][D];
+  __shared__ float fac[G][64];
+  __shared__ int last_flag;
+
+  // issue this warp's block loads first, then stage q
+  const int bi = c * kDecWarps + warp;
   const int nkeys = min(max(ctx - bi * 16, 0), 16);
-  if (nkeys <= 0) return;
-  const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
-  const KT* kv = reinterpret_cast<const KT*>(a.kv);
-  const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
-  const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
   const int key = lane >> 1, hf = lane & 1, par = lane >> 4, seg = lane & 15;
-  r.k.load(Kb + key * D + hf * (D / 2));
+  Raw<KT, kHalf> kr;
+  Raw<KT, kSeg> vr[8];
+  if (nkeys > 0) {
+    const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
+    const KT* kv = reinterpret_cast<const KT*>(a.kv);
+    const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+    const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
+    kr.load(Kb + key * D + hf * kHalf);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (2 * j + par < nkeys)
-      r.v[j].load(Vb + (2 * j + par) * D + seg * (D / 16));
-    else
-      r.v[j].zero();
+    for (int j = 0; j < 8; ++j) {
+      if (2 * j + par < nkeys)
+        vr[j].load(Vb + (2 * j + par) * D + seg * kSeg);
+      else
+        vr[j].zero();
+    }
   }
-}
+  for (int i = threadIdx.x; i < G * D; i += kThreads)
+    qs[i / D][i % D] = a.Q[((size_t)t * dm.H + g * G + i / D) * D + i % D];
+  __syncthreads();
 
-template <typename KT, int D, int G>
-__device__ __forceinline__ void decode_chunk(const AttnArgs& a, int s, int g, int c, int ctx, int warp, int lane,
-                                             const DecodeRegs<KT, D>& r, const float (*qs)[D], float (*ms)[G],
-                                             float (*ls)[G], float (*os)[G][D]) {
-  constexpr int kHalf = D / 2, kSeg = D / 16;
-  const Dims& dm = a.dims;
-  const int bi = c * (kDecodeChunk / 16) + warp;
-  const int nkeys = min(max(ctx - bi * 16, 0), 16);
-  const int key = lane >> 1, hf = lane & 1, par = lane >> 4, seg = lane & 15;
   float m[G], l[G], o[G][kSeg];
 #pragma unroll
   for (int i = 0; i < G; ++i) {
@@ -128,7 +134,7 @@ __device__ __forceinline__ void decode_chunk(const AttnArgs& a, int s, int g, in
     for (int i = 0; i < G; ++i) {
       float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], r.k.get(e), acc);
+      for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], kr.get(e), acc);
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       const float sc = key < nkeys ? acc * a.scale : -INFINITY;
       m[i] = warp_max(sc);
@@ -141,7 +147,7 @@ __device__ __forceinline__ void decode_chunk(const AttnArgs& a, int s, int g, in
       for (int i = 0; i < G; ++i) {
         const float pk = __shfl_sync(0xffffffffu, p[i], 2 * (2 * j + par));
 #pragma unroll
-        for (int e = 0; e < kSeg; ++e) o[i][e] = fmaf(pk, r.v[j].get(e), o[i][e]);
+        for (int e = 0; e < kSeg; ++e) o[i][e] = fmaf(pk, vr[j].get(e), o[i][e]);
       }
     }
 #pragma unroll
@@ -161,14 +167,14 @@ __device__ __forceinline__ void decode_chunk(const AttnArgs& a, int s, int g, in
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < G * D; i += 128) {
+  for (int i = threadIdx.x; i < G * D; i += kThreads) {
     const int h = i / D, dd = i % D;
     float M = ms[0][h];
 #pragma unroll
-    for (int w = 1; w < 4; ++w) M = fmaxf(M, ms[w][h]);
+    for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, ms[w][h]);
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < kDecWarps; ++w) {
       const float f = ms[w][h] == -INFINITY ? 0.f : expf(ms[w][h] - M);
       L = fmaf(ls[w][h], f, L);
       O = fmaf(os[w][h][dd], f, O);
@@ -180,68 +186,39 @@ __device__ __forceinline__ void decode_chunk(const AttnArgs& a, int s, int g, in
     }
     part[2 + dd] = O;
   }
-  __syncthreads();
-}
-
-template <typename KT, typename AT, int D, int G>
-__global__ void __launch_bounds__(128) k_attn_decode(AttnArgs a) {
-  pdl_launch_next();
-  pdl_wait_prev();
-  const Dims& dm = a.dims;
-  const int g = blockIdx.y, s = blockIdx.z;
-  const int ctx = a.meta.seq_ctx[s];
-  const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
-  if ((int)blockIdx.x >= nch) return;
-  const int t = a.meta.seq_start[s];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ float qs[G][D];
-  __shared__ float ms[4][G], ls[4][G];
-  __shared__ float os[4][G][D];
-  __shared__ int last_flag;
-  for (int i = threadIdx.x; i < G * D; i += 128)
-    qs[i / D][i % D] = a.Q[((size_t)t * dm.H + g * G + i / D) * D + i % D];
-
-  DecodeRegs<KT, D> ra, rb;
-  int c = blockIdx.x;
-  decode_load<KT, D>(a, s, g, c, ctx, warp, lane, ra);
-  __syncthreads();
-  while (true) {
-    int cn = c + gridDim.x;
-    if (cn < nch) decode_load<KT, D>(a, s, g, cn, ctx, warp, lane, rb);
-    decode_chunk<KT, D, G>(a, s, g, c, ctx, warp, lane, ra, qs, ms, ls, os);
-    if (cn >= nch) break;
-    c = cn;
-    cn = c + gridDim.x;
-    if (cn < nch) decode_load<KT, D>(a, s, g, cn, ctx, warp, lane, ra);
-    decode_chunk<KT, D, G>(a, s, g, c, ctx, warp, lane, rb, qs, ms, ls, os);
-    if (cn >= nch) break;
-    c = cn;
-  }
 
   // the last CTA of this (sequence, KV head) merges the chunk records in chunk order
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const int active = min((int)gridDim.x, nch);
-    last_flag = atomicAdd(a.counters + s * dm.Hkv + g, 1) == active - 1;
-  }
+  if (threadIdx.x == 0) last_flag = atomicAdd(a.counters + s * dm.Hkv + g, 1) == nch - 1;
   __syncthreads();
   if (!last_flag) return;
   __threadfence();
-  AT* out = reinterpret_cast<AT*>(a.ATT);
-  for (int i = threadIdx.x; i < G * D; i += 128) {
-    const int h = i / D, dd = i % D;
-    const float* part = a.part + ((size_t)s * dm.H + g * G + h) * a.nchunk_cap * (D + 2);
-    float M = -INFINITY;
-    for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(part + cc * (D + 2)));
-    float L = 0.f, O = 0.f;
-    for (int cc = 0; cc < nch; ++cc) {
-      const float* p = part + cc * (D + 2);
-      const float f = expf(__ldcg(p) - M);
-      L = fmaf(__ldcg(p + 1), f, L);
-      O = fmaf(__ldcg(p + 2 + dd), f, O);
+  const float* base = a.part + ((size_t)s * dm.H + g * G) * a.nchunk_cap * (D + 2);
+  // per-chunk scale factors exp(m_c - M) and the total L, per head, via shared memory
+  if (warp < G) {
+    const float* ph = base + (size_t)warp * a.nchunk_cap * (D + 2);
+    float mx = -INFINITY;
+    for (int cc = lane; cc < nch; cc += 32) mx = fmaxf(mx, __ldcg(ph + cc * (D + 2)));
+    mx = warp_max(mx);
+    float sum = 0.f;
+    for (int cc = lane; cc < nch; cc += 32) {
+      const float f = expf(__ldcg(ph + cc * (D + 2)) - mx);
+      fac[warp][cc] = f;
+      sum = fmaf(__ldcg(ph + cc * (D + 2) + 1), f, sum);
     }
-    out[((size_t)t * dm.H + g * G + h) * D + dd] = from_f32<AT>(O / L);
+    sum = warp_sum(sum);
+    if (lane == 0) ms[0][warp] = sum;
+  }
+  __syncthreads();
+  AT* out = reinterpret_cast<AT*>(a.ATT);
+  for (int i = threadIdx.x; i < G * D; i += kThreads) {
+    const int h = i / D, dd = i % D;
+    const float* ph = base + (size_t)h * a.nchunk_cap * (D + 2) + 2 + dd;
+    float O = 0.f;
+#pragma unroll 4
+    for (int cc = 0; cc < nch; ++cc) O = fmaf(__ldcg(ph + cc * (D + 2)), fac[h][cc], O);
+    out[((size_t)t * dm.H + g * G + h) * D + dd] = from_f32<AT>(O / ms[0][h]);
   }
   if (threadIdx.x == 0) a.counters[s * dm.Hkv + g] = 0;
 }
@@ -420,7 +397,7 @@ int prefill_tile_queries(int G) { return kPfRows / G; }
 template <typename KT, typename AT, int D, int G>
 static cudaError_t attn_decode_t(const AttnArgs& a, int nchunk, cudaStream_t s) {
   dim3 grid(nchunk, a.dims.Hkv, a.S);
-  k_attn_decode<KT, AT, D, G><<<grid, 128, 0, s>>>(a);
+  k_attn_decode<KT, AT, D, G><<<grid, kDecWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
