@@ -667,13 +667,22 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     // RMSNorm + [Wq;Wk;Wv]
     g.W = Lb + pl.wqkv; g.rows = qkv_rows(c); g.K = d; g.X = XN; g.x_row = nullptr; g.T = N; g.ssq = SSQ;
     g.out_f32 = RAW;
-    DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV_RAW, bf ? &m->tm_qkv[l] : nullptr, &m->tm_xn, &m->tm_xn32));
-    QkvPostArgs qa{RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope),
-                   Q, sp.slabs, l, sp.meta, dm};
-    DEC_LAUNCH(DEC_K_QKV_POST, launch_qkv_post(qa, N, bf, st));
+    const bool tc_qkv = bf && m->tc_on && m->tc_ready &&
+                        ((N > kGemvMaxTokens && tc_eligible(g)) || tc_skinny_eligible(g));
+    if (tc_qkv) {
+      // tensor-core product with QK-norm, RoPE and the cache write in its epilogue
+      g.qf = QkvFuse{(const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope), Q,
+                     sp.slabs, l, sp.meta, c.n_heads, c.n_kv_heads, c.head_dim, dm.B, dm.n_blocks, dm.max_blocks};
+      DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV, &m->tm_qkv[l], &m->tm_xn, &m->tm_xn32));
+    } else {
+      DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV_RAW, bf ? &m->tm_qkv[l] : nullptr, &m->tm_xn, &m->tm_xn32));
+      QkvPostArgs qa{RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm),
+                     (const float*)(P + pl.rope), Q, sp.slabs, l, sp.meta, dm};
+      DEC_LAUNCH(DEC_K_QKV_POST, launch_qkv_post(qa, N, bf, st));
+    }
     // attention
     AttnArgs aa{Q, sp.slabs, l, sp.meta, dm, ATT, PART, m->NCH, sp.S, 1.0f / std::sqrt((float)c.head_dim),
-                (int*)(ws + wl.ACNT)};
+                (int*)(ws + wl.ACNT), ERR};
     if (sp.decode) {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, sp.slots, bf, st));
     } else {

@@ -77,4 +77,77 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
   }
 }
 
+// One output row (0 <= j < D) of a query or key head after QK-norm and
+// split-half RoPE: y and yp are the head's values at channel j and at its
+// partner j +- D/2, rn the head's 1/rms.
+__device__ __forceinline__ float qk_rope(const QkvFuse& f, int gh, int j, float y, float yp, float rn, int pos) {
+  const int half = f.D / 2;
+  const float* g = gh < f.H ? f.q_norm : f.k_norm;
+  const int jj = j < half ? j : j - half;
+  const int jp = j < half ? j + half : j - half;
+  const float a_ = y * rn * g[j], b_ = yp * rn * g[jp];
+  const float c = f.rope[((size_t)pos * half + jj) * 2], sn = f.rope[((size_t)pos * half + jj) * 2 + 1];
+  return j < half ? a_ * c - b_ * sn : a_ * c + b_ * sn;
+}
+
+// Cache block holding position `pos` of the sequence of token row tt.
+__device__ __forceinline__ int qkv_block(const QkvFuse& f, int tt, int pos) {
+  return f.meta.tables[(size_t)f.meta.tok_seq[tt] * f.max_blocks + pos / f.B];
+}
+
+// Write output row j of head gh for absolute token row tt at position pos
+// (cache block blk): queries to Q (fp32), keys and values to their slot (KT).
+template <typename KT>
+__device__ __forceinline__ void qkv_store(const QkvFuse& f, int tt, int gh, int j, float v, int pos, int blk) {
+  if (gh < f.H) {
+    f.Q[((size_t)tt * f.H + gh) * f.D + j] = v;
+    return;
+  }
+  const int is_v = gh >= f.H + f.Hkv;
+  const int h = gh - f.H - (is_v ? f.Hkv : 0);
+  reinterpret_cast<KT*>(f.kv)[kv_offset(f.layer, blk, is_v, h, pos % f.B, f.n_blocks, f.Hkv, f.B, f.D) + j] =
+      from_f32<KT>(v);
+}
+
+// Fused QKV epilogue over a tile of whole heads: y = acc * rstd; per query or
+// key head RMSNorm over its D rows with the shared gain, then split-half RoPE
+// at the token's position; queries to Q, keys and values into the cache.
+// `rn` is scratch for [nrows / D][ntok] head norms; `sync` orders the phases.
+template <typename KT, int NT, typename Sync>
+__device__ __forceinline__ void epilogue_qkv_tile(const GemvArgs& a, const float* tile, int ld, int r0, int nrows,
+                                                  int t0, int ntok, const float* rstd_s, float* rn, int* tpos,
+                                                  int* tblk, int tid, Sync sync) {
+  const QkvFuse& f = a.qf;
+  const int D = f.D, heads = nrows / D;
+  for (int i = tid; i < ntok * heads; i += NT) {
+    const int t = i % ntok, hh = i / ntok;
+    const float rs = rstd_s[t];
+    float ss = 0.f;
+    for (int j = 0; j < D; ++j) {
+      const float y = tile[(hh * D + j) * ld + t] * rs;
+      ss = fmaf(y, y, ss);
+    }
+    rn[hh * ntok + t] = 1.0f / sqrtf(ss / (float)D + a.eps);
+  }
+  for (int t = tid; t < ntok; t += NT) {
+    const int pos = f.meta.tok_pos[t0 + t];
+    tpos[t] = pos;
+    tblk[t] = qkv_block(f, t0 + t, pos);
+  }
+  sync();
+  const int half = D / 2;
+  for (int i = tid; i < ntok * nrows; i += NT) {
+    const int t = i / nrows, r = i - t * nrows;
+    const int hh = r / D, j = r - hh * D;
+    const int gh = (r0 + hh * D) / D;
+    const float y = tile[r * ld + t] * rstd_s[t];
+    float out = y;
+    if (gh < f.H + f.Hkv) {
+      const int rp = j < half ? r + half : r - half;
+      out = qk_rope(f, gh, j, y, tile[rp * ld + t] * rstd_s[t], rn[hh * ntok + t], tpos[t]);
+    }
+    qkv_store<KT>(f, t0 + t, gh, j, out, tpos[t], tblk[t]);
+  }
+}
+
 }  // namespace dec

@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tc_common.cuh"
 
 namespace dec {
 
@@ -64,96 +65,181 @@ struct Raw {
 };
 
 // ---------------------------------------------------------------------------
-// Decode attention, split-K.  grid (chunk, kv head, sequence), 8 warps.  Keys
+// Decode attention, split-K.  grid (chunk, kv head, sequence), 4 warps.  Keys
 // are cut into fixed 128-key chunks (8 blocks of 16; the cut depends only on
-// the position, never on the batch), one chunk per CTA and one block per
-// warp, so every K/V load of the chunk is in flight at once.  Lane (key =
-// lane/2, half = lane%2) holds half a key row for the scores, lane (parity =
-// lane/16, segment = lane%16) D/16 dims of 8 value rows; loads are 128-bit
-// where the row allows.  The G query heads of the group share every K/V load.
-// The 8 warps' softmax states merge in warp order into one (max, sum, o[D])
-// record per chunk and query head.  The last CTA of a (sequence, KV head) to
-// finish merges all records in chunk order, writes the attention output and
-// re-arms the counter.
+// the position, never on the batch), one chunk per CTA.  One thread issues
+// bulk asynchronous copies of the chunk's K and V slabs (4 KB each per block
+// and KV head at the serving shape) into shared memory on one mbarrier, so a
+// whole chunk is in flight at once without holding registers.  Warp w then
+// folds blocks w and w + 4 into an online softmax: lane l holds D/32 dims of
+// the G queries, forms partial dots with 16 keys, and a 31-shuffle
+// reduce-scatter leaves lane l with the full score of (head l/16, key l%16);
+// the value rows are read one 256-byte row per instruction.  The 4 warps'
+// states merge in warp order into one (max, sum, o[D]) record per chunk and
+// query head; the last CTA of a (sequence, KV head) to finish merges all
+// records in chunk order, writes the attention output and re-arms the counter.
 // ---------------------------------------------------------------------------
-constexpr int kDecWarps = kDecodeChunk / 16;
+constexpr int kDecWarps = 4;
+constexpr int kDecBlocks = kDecodeChunk / 16;  // 8
+
+template <typename KT, int D>
+__host__ __device__ constexpr size_t decode_smem_bytes() {
+  return (size_t)2 * kDecBlocks * 16 * D * sizeof(KT);
+}
+
+// The score of lane (head lane/16, key lane%16) from 32 per-lane partials
+// v[i*16 + k] (G = 2): reduce-scatter over the warp, 31 shuffles.
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float send = up ? v[j] : v[j + w];
+      const float keep = up ? v[j + w] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
 
 template <typename KT, typename AT, int D, int G>
-__global__ void __launch_bounds__(kDecWarps * 32, 2) k_attn_decode(AttnArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32) k_attn_decode(AttnArgs a) {
   pdl_launch_next();
   pdl_wait_prev();
-  constexpr int kHalf = D / 2, kSeg = D / 16, kThreads = kDecWarps * 32;
+  constexpr int kThreads = kDecWarps * 32, kDim = D / 32;
   const Dims& dm = a.dims;
   const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int ctx = a.meta.seq_ctx[s];
   const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
   if (c >= nch) return;
-  const int t = a.meta.seq_start[s];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  KT* Ks = reinterpret_cast<KT*>(dsm);        // [8 blocks][16 keys][D]
+  KT* Vs = Ks + kDecBlocks * 16 * D;          // [8 blocks][16 keys][D]
   __shared__ float qs[G][D];
   __shared__ float ms[kDecWarps][G], ls[kDecWarps][G];
   __shared__ float os[kDecWarps][G][D];
   __shared__ float fac[G][64];
-  __shared__ int last_flag;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int last_flag, abort_flag;
+  const int t = a.meta.seq_start[s];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int keys_here = min(kDecodeChunk, ctx - c * kDecodeChunk);
+  const int nblk = (keys_here + 15) / 16;
+  constexpr uint32_t kSlab = 16 * D * sizeof(KT);
 
-  // issue this warp's block loads first, then stage q
-  const int bi = c * kDecWarps + warp;
-  const int nkeys = min(max(ctx - bi * 16, 0), 16);
-  const int key = lane >> 1, hf = lane & 1, par = lane >> 4, seg = lane & 15;
-  Raw<KT, kHalf> kr;
-  Raw<KT, kSeg> vr[8];
-  if (nkeys > 0) {
-    const int blk = a.meta.tables[(size_t)s * dm.max_blocks + bi];
-    const KT* kv = reinterpret_cast<const KT*>(a.kv);
-    const KT* Kb = kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D);
-    const KT* Vb = kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D);
-    kr.load(Kb + key * D + hf * kHalf);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (2 * j + par < nkeys)
-        vr[j].load(Vb + (2 * j + par) * D + seg * kSeg);
-      else
-        vr[j].zero();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // lane b looks up block b's pool id and issues its two copies: the table
+    // reads are independent, so their latencies overlap
+    if (lane == 0) mbar_expect_tx(&bar, 2 * kSlab * nblk);
+    __syncwarp();
+    if (lane < nblk) {
+      const KT* kv = reinterpret_cast<const KT*>(a.kv);
+      const int blk = a.meta.tables[(size_t)s * dm.max_blocks + c * kDecBlocks + lane];
+      bulk_g2s(Ks + lane * 16 * D, kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D), kSlab, &bar);
+      bulk_g2s(Vs + lane * 16 * D, kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D), kSlab, &bar);
     }
   }
   for (int i = threadIdx.x; i < G * D; i += kThreads)
     qs[i / D][i % D] = a.Q[((size_t)t * dm.H + g * G + i / D) * D + i % D];
   __syncthreads();
+  float q[G][kDim];
+#pragma unroll
+  for (int i = 0; i < G; ++i)
+#pragma unroll
+    for (int e = 0; e < kDim; ++e) q[i][e] = qs[i][lane * kDim + e];
+  const bool ok = mbar_wait(&bar, 0, &abort_flag, a.err);
 
-  float m[G], l[G], o[G][kSeg];
+  float m[G], l[G], o[G][kDim];
 #pragma unroll
   for (int i = 0; i < G; ++i) {
     m[i] = -INFINITY;
     l[i] = 0.f;
 #pragma unroll
-    for (int e = 0; e < kSeg; ++e) o[i][e] = 0.f;
+    for (int e = 0; e < kDim; ++e) o[i][e] = 0.f;
   }
-  if (nkeys > 0) {
-    float p[G];
+  if (ok) {
+    for (int b = warp; b < nblk; b += kDecWarps) {
+      const KT* Kb = Ks + b * 16 * D;
+      const KT* Vb = Vs + b * 16 * D;
+      const int nkeys = min(16, keys_here - b * 16);
+      float sc[G];
+      if constexpr (G == 2) {
+        float v[32];
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      float acc = 0.f;
+        for (int k = 0; k < 16; ++k) {
+          float kk[kDim];
 #pragma unroll
-      for (int e = 0; e < kHalf; ++e) acc = fmaf(qs[i][hf * kHalf + e], kr.get(e), acc);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      const float sc = key < nkeys ? acc * a.scale : -INFINITY;
-      m[i] = warp_max(sc);
-      p[i] = key < nkeys ? expf(sc - m[i]) : 0.f;
-      l[i] = warp_sum(hf == 0 ? p[i] : 0.f);
-    }
+          for (int e = 0; e < kDim; ++e) kk[e] = to_f32(Kb[k * D + lane * kDim + e]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+          for (int i = 0; i < 2; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < kDim; ++e) acc = fmaf(q[i][e], kk[e], acc);
+            v[i * 16 + k] = acc;
+          }
+        }
+        const float full = reduce_scatter32(v, lane) * a.scale;  // lane = head*16 + key
+        sc[0] = sc[1] = ((lane & 15) < nkeys) ? full : -INFINITY;
+      } else {
+        // general group size: one butterfly per (key, head); lane (i*16 + k) keeps its own
+#pragma unroll
+        for (int i = 0; i < G; ++i) sc[i] = -INFINITY;
+        for (int k = 0; k < 16; ++k) {
+          float kk[kDim];
+#pragma unroll
+          for (int e = 0; e < kDim; ++e) kk[e] = to_f32(Kb[k * D + lane * kDim + e]);
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < kDim; ++e) acc = fmaf(q[i][e], kk[e], acc);
+            acc = warp_sum(acc) * a.scale;
+            if ((lane & 15) == k && k < nkeys) sc[i] = acc;
+          }
+        }
+      }
+      // per head: the block's max over its 16 keys, rescale the running state
+      float p[G];
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        const float pk = __shfl_sync(0xffffffffu, p[i], 2 * (2 * j + par));
+        const int owner = G == 2 ? i : 0;  // G == 2: lanes 16*i .. 16*i+15 hold head i
+        float mx = sc[i];
 #pragma unroll
-        for (int e = 0; e < kSeg; ++e) o[i][e] = fmaf(pk, vr[j].get(e), o[i][e]);
+        for (int o2 = 8; o2 >= 1; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+        const float mb = __shfl_sync(0xffffffffu, mx, owner * 16);
+        const float m_new = fmaxf(m[i], mb);
+        const float corr = m[i] == -INFINITY ? 0.f : expf(m[i] - m_new);
+        p[i] = sc[i] == -INFINITY ? 0.f : expf(sc[i] - m_new);
+        float ps = p[i];
+#pragma unroll
+        for (int o2 = 8; o2 >= 1; o2 >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o2);
+        ps = __shfl_sync(0xffffffffu, ps, owner * 16);
+        l[i] = l[i] * corr + ps;
+        m[i] = m_new;
+#pragma unroll
+        for (int e = 0; e < kDim; ++e) o[i][e] *= corr;
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (k >= nkeys) break;  // slots past the context may hold anything, even NaN
+        float vv[kDim];
+#pragma unroll
+        for (int e = 0; e < kDim; ++e) vv[e] = to_f32(Vb[k * D + lane * kDim + e]);
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const float pk = __shfl_sync(0xffffffffu, p[i], (G == 2 ? i * 16 : 0) + k);
+#pragma unroll
+          for (int e = 0; e < kDim; ++e) o[i][e] = fmaf(pk, vv[e], o[i][e]);
+        }
       }
     }
-#pragma unroll
-    for (int i = 0; i < G; ++i)
-#pragma unroll
-      for (int e = 0; e < kSeg; ++e) o[i][e] += __shfl_xor_sync(0xffffffffu, o[i][e], 16);
   }
 #pragma unroll
   for (int i = 0; i < G; ++i) {
@@ -161,10 +247,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) k_attn_decode(AttnArgs a) {
       ms[warp][i] = m[i];
       ls[warp][i] = l[i];
     }
-    if (lane < 16) {
 #pragma unroll
-      for (int e = 0; e < kSeg; ++e) os[warp][i][seg * kSeg + e] = o[i][e];
-    }
+    for (int e = 0; e < kDim; ++e) os[warp][i][lane * kDim + e] = o[i][e];
   }
   __syncthreads();
   for (int i = threadIdx.x; i < G * D; i += kThreads) {
@@ -186,6 +270,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) k_attn_decode(AttnArgs a) {
     }
     part[2 + dd] = O;
   }
+  if (!ok && threadIdx.x == 0) {  // let the copies land before shared memory goes away
+    const uint64_t t0 = global_ns();
+    while (!mbar_try(&bar, 0) && global_ns() - t0 < kWaitLimitNs) {
+    }
+  }
 
   // the last CTA of this (sequence, KV head) merges the chunk records in chunk order
   __threadfence();
@@ -195,7 +284,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) k_attn_decode(AttnArgs a) {
   if (!last_flag) return;
   __threadfence();
   const float* base = a.part + ((size_t)s * dm.H + g * G) * a.nchunk_cap * (D + 2);
-  // per-chunk scale factors exp(m_c - M) and the total L, per head, via shared memory
   if (warp < G) {
     const float* ph = base + (size_t)warp * a.nchunk_cap * (D + 2);
     float mx = -INFINITY;
@@ -396,8 +484,16 @@ int prefill_tile_queries(int G) { return kPfRows / G; }
 // ---------------------------------------------------------------------------
 template <typename KT, typename AT, int D, int G>
 static cudaError_t attn_decode_t(const AttnArgs& a, int nchunk, cudaStream_t s) {
+  static bool configured = false;
+  constexpr size_t smem = decode_smem_bytes<KT, D>();
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_decode<KT, AT, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   dim3 grid(nchunk, a.dims.Hkv, a.S);
-  k_attn_decode<KT, AT, D, G><<<grid, kDecWarps * 32, 0, s>>>(a);
+  k_attn_decode<KT, AT, D, G><<<grid, kDecWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -32,6 +32,8 @@ constexpr uint32_t kTcStageA = kTcM * kTcK * 2;  // 16 KB
 constexpr uint32_t kTcStageB = kTcN * kTcK * 2;  // 16 KB
 constexpr uint32_t kTcAccCols = 128;             // fp32 columns per accumulator
 struct TcShared {
+  float rn[4 * kTcN];  // fused QKV epilogue: head norms [heads per tile][tokens]
+  int tpos[kTcN], tblk[kTcN];  // fused QKV epilogue: position and cache block per token
   uint64_t full[kTcStages], empty[kTcStages], tfull[2], tempty[2], mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -181,7 +183,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       mbar_arrive(&sh->tempty[acc]);
       epi_bar();
-      epilogue<AT, EPI, 128>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, et);
+      if constexpr (EPI == EPI_QKV) {
+        epilogue_qkv_tile<__half, 128>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, sh->rn, sh->tpos,
+                                       sh->tblk, et, EpiBar{});
+      } else {
+        epilogue<AT, EPI, 128>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, et);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -234,6 +241,7 @@ cudaError_t launch_gemm_tc(const GemvArgs& a, int epi, const void* tmW, const vo
   const CUtensorMap* x = reinterpret_cast<const CUtensorMap*>(tmX);
   switch (epi) {
     case EPI_QKV_RAW: return tc_one<bf16, EPI_QKV_RAW>(a, w, x, num_sms, err, s);
+    case EPI_QKV: return tc_one<bf16, EPI_QKV>(a, w, x, num_sms, err, s);
     case EPI_RESID: return tc_one<bf16, EPI_RESID>(a, w, x, num_sms, err, s);
     case EPI_SWIGLU: return tc_one<bf16, EPI_SWIGLU>(a, w, x, num_sms, err, s);
     default: return tc_one<bf16, EPI_LOGITS>(a, w, x, num_sms, err, s);

@@ -32,6 +32,9 @@ constexpr uint32_t kSkStageB = kSkN * kSkK * 2;  // 4 KB
 constexpr uint32_t kSkCols = 32;
 
 struct SkShared {
+  float psq[4][kSkN];  // fused QKV: partial sums of squares [head in tile][token]
+  float rn[4][kSkN];   // fused QKV: 1/rms per [head in tile][token]
+  int tpos[kSkN], tblk[kSkN];
   uint64_t full[kSkStages], empty[kSkStages], tfull, mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -165,26 +168,82 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   }
 
   cluster_sync();  // every partial tile of the cluster is in shared memory
+  const int rows_per = ks <= 8 ? kSkM / ks : 16;
+  const int r_lo = z * rows_per;
+  const bool has_rows = !*abort_flag && r_lo < kSkM;
+  const float* src = tile + r_lo * kSkLd;  // this CTA's reduced rows, [rows_per][kSkLd]
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
-    const int rows_per = ks <= 8 ? kSkM / ks : 16;
-    const int r_lo = z * rows_per;
-    if (!*abort_flag && r_lo < kSkM) {
-      const float* src = tile;
-      if (ks > 1) {
-        for (int i = et; i < rows_per * kSkN; i += 128) {
-          const int rr = i / kSkN, t = i % kSkN;
-          const float* p = tile + (r_lo + rr) * kSkLd + t;
-          float sum = 0.f;
-          for (int q = 0; q < ks; ++q) sum += dsmem_ld(dsmem_addr(p, (uint32_t)q));
-          red[rr * kSkLd + t] = sum;
+    if (has_rows && ks > 1) {
+      for (int i = et; i < rows_per * kSkN; i += 128) {
+        const int rr = i / kSkN, t = i % kSkN;
+        const float* p = tile + (r_lo + rr) * kSkLd + t;
+        float sum = 0.f;
+        for (int q = 0; q < ks; ++q) sum += dsmem_ld(dsmem_addr(p, (uint32_t)q));
+        red[rr * kSkLd + t] = sum;
+      }
+      src = red;
+    }
+    if constexpr (EPI != EPI_QKV) {
+      if (has_rows) {
+        epi_bar();
+        epilogue<AT, EPI, 128>(a, src, kSkLd, mt * kSkM + r_lo, rows_per, 0, ntok, rstd_s, et);
+      }
+    } else {
+      // partial sums of squares of this CTA's rows, per (head in the tile, token)
+      const int D = a.qf.D;
+      for (int i = et; i < 4 * kSkN; i += 128) sh->psq[i / kSkN][i % kSkN] = 0.f;
+      epi_bar();
+      if (has_rows) {
+        const int h_lo = r_lo / D, h_n = rows_per >= D ? rows_per / D : 1;
+        for (int i = et; i < h_n * ntok; i += 128) {
+          const int hl = h_lo + i / ntok, t = i % ntok;
+          const int a0 = max(hl * D, r_lo), a1 = min(hl * D + D, r_lo + rows_per);
+          float ss = 0.f;
+          for (int r = a0; r < a1; ++r) {
+            const float y = src[(r - r_lo) * kSkLd + t] * rstd_s[t];
+            ss = fmaf(y, y, ss);
+          }
+          sh->psq[hl][t] = ss;
         }
-        src = red;
-      } else {
-        src = tile + r_lo * kSkLd;
+      }
+    }
+  }
+  if constexpr (EPI == EPI_QKV) {
+    cluster_sync();  // every CTA's partial sums and reduced rows are visible
+    const QkvFuse& f = a.qf;
+    const int D = f.D, half = D / 2;
+    if (warp >= 2 && has_rows) {
+      const int et = threadIdx.x - 64;
+      // per token: position and cache block; per (head of this CTA's rows, token): 1/rms
+      for (int t = et; t < ntok; t += 128) {
+        const int pos = f.meta.tok_pos[t];
+        sh->tpos[t] = pos;
+        sh->tblk[t] = qkv_block(f, t, pos);
+      }
+      const int h_lo = r_lo / D, h_n = rows_per >= D ? rows_per / D : 1;
+      for (int i = et; i < h_n * ntok; i += 128) {
+        const int hl = h_lo + i / ntok, t = i % ntok;
+        float ss = 0.f;
+        for (int q = 0; q < ks; ++q) ss += ks > 1 ? dsmem_ld(dsmem_addr(&sh->psq[hl][t], (uint32_t)q)) : sh->psq[hl][t];
+        sh->rn[hl][t] = 1.0f / sqrtf(ss / (float)D + a.eps);
       }
       epi_bar();
-      epilogue<AT, EPI, 128>(a, src, kSkLd, mt * kSkM + r_lo, rows_per, 0, ntok, rstd_s, et);
+      for (int i = et; i < ntok * rows_per; i += 128) {
+        const int t = i / rows_per, rr = i - t * rows_per;
+        const int r = r_lo + rr, hl = r / D, j = r - hl * D;
+        const int gh = (mt * kSkM + hl * D) / D;
+        const float y = src[rr * kSkLd + t] * rstd_s[t];
+        float out = y;
+        if (gh < f.H + f.Hkv) {
+          const int rp = j < half ? r + half : r - half;
+          const int zo = rp / rows_per;
+          const float yp = zo == z ? src[(rp - r_lo) * kSkLd + t]
+                                   : dsmem_ld(dsmem_addr(red + (rp - zo * rows_per) * kSkLd + t, (uint32_t)zo));
+          out = qk_rope(f, gh, j, y, yp * rstd_s[t], sh->rn[hl][t], sh->tpos[t]);
+        }
+        qkv_store<__half>(f, t, gh, j, out, sh->tpos[t], sh->tblk[t]);
+      }
     }
   }
   cluster_sync();  // no CTA leaves while another still reads its tile
@@ -264,6 +323,7 @@ cudaError_t launch_gemm_tc_skinny(const GemvArgs& a, int epi, const void* tmW, c
   const CUtensorMap* x = reinterpret_cast<const CUtensorMap*>(tmX);
   switch (epi) {
     case EPI_QKV_RAW: return skinny_one<bf16, EPI_QKV_RAW>(a, w, x, err, pdl, s);
+    case EPI_QKV: return skinny_one<bf16, EPI_QKV>(a, w, x, err, pdl, s);
     case EPI_RESID: return skinny_one<bf16, EPI_RESID>(a, w, x, err, pdl, s);
     case EPI_SWIGLU: return skinny_one<bf16, EPI_SWIGLU>(a, w, x, err, pdl, s);
     default: return skinny_one<bf16, EPI_LOGITS>(a, w, x, err, pdl, s);

@@ -8,7 +8,20 @@
 
 namespace dec {
 
-enum Epi { EPI_QKV_RAW = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+enum Epi { EPI_QKV_RAW = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3, EPI_QKV = 4 };
+
+// What the fused QKV epilogue (EPI_QKV) needs: QK-norm gains, the RoPE table,
+// the query buffer and the KV pool with the step's positions and tables.
+struct QkvFuse {
+  const float* q_norm;
+  const float* k_norm;
+  const float* rope;  // [max_positions, D/2, 2] (cos, sin)
+  float* Q;           // [T, H, D]
+  void* kv;           // pool slabs
+  int layer;
+  StepMeta meta;
+  int H, Hkv, D, B, n_blocks, max_blocks;
+};
 
 // Token rows up to which the weight-streaming kernel runs a product.
 constexpr int kGemvMaxTokens = 32;
@@ -32,6 +45,7 @@ struct GemvArgs {
   void* act_out;          // SWIGLU output [T, F]
   int F;
   unsigned long long* keys; // LOGITS argmax keys [T]
+  QkvFuse qf;             // EPI_QKV
 };
 
 struct EmbedArgs {
@@ -70,6 +84,7 @@ struct AttnArgs {
   int S;
   float scale;      // 1/sqrt(D)
   int* counters;    // decode: finished CTAs per (sequence, kv head), zero between launches
+  uint32_t* err;    // device error word
 };
 
 // Launchers; `wbf16` selects bf16 weights / activations / f16 KV (serving

@@ -70,6 +70,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` contiguous bytes global -> shared,
+// completing on `bar` (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (stride byte offset), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -130,6 +139,11 @@ __device__ __forceinline__ bool epi_any(bool v) {
   return r != 0;
 }
 
+
+// Callable form of epi_bar for epilogue helpers that need a phase barrier.
+struct EpiBar {
+  __device__ __forceinline__ void operator()() const { epi_bar(); }
+};
 
 // ---- clusters ----------------------------------------------------------------
 __device__ __forceinline__ void cluster_sync() {
