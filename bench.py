@@ -302,10 +302,25 @@ def our_arm(args, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     pf_ms = e0.elapsed_time(e1)
-    # layer projections of 16,384 tokens + the LM head on the 32 chunk-last rows
-    proj_flops = 2 * 16384 * 440_401_920 + 2 * 32 * 155_582_464
+    # one more pass with events around every kernel class: the products' tensor-core rate
+    profile_classes(m, range(len(dec.KERNEL_CLASSES)), True)
+    prefill_pass()
+    pf_cls = {name: read_profile(m, c) for c, name in enumerate(dec.KERNEL_CLASSES)}
+    profile_classes(m, range(len(dec.KERNEL_CLASSES)), False)
+    d, H, Hkv, D, F = (shape[k] for k in ("d_model", "n_heads", "n_kv_heads", "head_dim", "ff_hidden"))
+    ntok = 16384
+    nl = shape["n_layers"]
+    flops = {"qkv": 2 * ntok * nl * (H + 2 * Hkv) * D * d, "oproj": 2 * ntok * nl * d * H * D,
+             "gateup": 2 * ntok * nl * 2 * F * d, "down": 2 * ntok * nl * d * F}
+    proj_ms = sum(pf_cls[k][0] for k in flops)
+    proj_tf = sum(flops.values()) / (proj_ms / 1e3) / 1e12
     prefill = {"tokens_per_s": round(16384 / (pf_ms / 1e3), 1), "ms": round(pf_ms, 3),
-               "projection_tflops": round(proj_flops / (pf_ms / 1e3) / 1e12, 2)}
+               "kernel_ms": {k: round(v[0], 3) for k, v in pf_cls.items() if v[1]},
+               "projection_tflops": round(proj_tf, 1),
+               "projection_tc_frac": round(proj_tf / pk["bf16_tflops"], 4),
+               "per_product_tc_frac": {k: round(flops[k] / (pf_cls[k][0] / 1e3) / 1e12 / pk["bf16_tflops"], 4)
+                                       for k in flops},
+               "tc_peak_tflops": pk["bf16_tflops"], "tc_peak_source": pk["source"]}
 
     status = m.device_status()
     m.close()

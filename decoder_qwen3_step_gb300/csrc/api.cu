@@ -69,7 +69,7 @@ int check_config(const dec_config* c) {
   if (c->vocab % 16) return fail(DEC_EINVAL, "vocab must be a multiple of 16");
   if (c->block_tokens != 16) return fail(DEC_EINVAL, "block_tokens must be 16");
   if (!(c->rope_base > 1.0) || !(c->rms_eps > 0.0)) return fail(DEC_EINVAL, "rope_base must be > 1, rms_eps > 0");
-  if (c->max_positions > (1 << 20)) return fail(DEC_EINVAL, "max_positions too large");
+  if (c->max_positions > kMaxPositions) return fail(DEC_EINVAL, "max_positions above %d", kMaxPositions);
   return DEC_OK;
 }
 
@@ -125,8 +125,10 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
   L.ACT = take((size_t)T * c.ff_hidden * a);
   L.PART = take((size_t)S * c.n_heads * max_chunks_of(c) * (c.head_dim + 2) * 4);
   L.ACNT = take((size_t)S * c.n_kv_heads * 4);
-  // ids, tok_pos, tok_seq, row_tok [T]; seq_start [S+1]; seq_ctx [S]; tables [S*MB]; work [3*(T+S)]
-  L.meta_ints = 4 * (size_t)T + 2 * (size_t)S + 1 + (size_t)S * max_blocks_of(c) + 3 * ((size_t)T + S);
+  // ids, tok_pos, tok_seq, row_tok [T]; seq_start [S+1]; seq_ctx [S]; tables [S*MB]; then either the
+  // prefill tiles [3*(T+S)] or the decode work list [1 + 2*S*chunks]
+  L.meta_ints = 4 * (size_t)T + 2 * (size_t)S + 1 + (size_t)S * max_blocks_of(c) +
+                std::max(3 * ((size_t)T + S), 1 + 2 * (size_t)S * max_chunks_of(c));
   L.META = take(L.meta_ints * 4);
   L.KEYS = take((size_t)T * 8);
   L.ERR = take(64);
@@ -873,6 +875,19 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   for (size_t i = 0; i < work.size(); ++i)
     for (int k = 0; k < 3; ++k) H[o_work + 3 * i + k] = work[i][k];
   o += 3 * work.size();
+  if (decode) {
+    // decode attention work list: n, then (sequence, 128-key chunk) pairs, chunk-major
+    int n = 0, cmax = (max_ctx + kDecodeChunk - 1) / kDecodeChunk;
+    for (int cc = 0; cc < cmax; ++cc)
+      for (int s = 0; s < S; ++s)
+        if (cc * kDecodeChunk < b->positions[b->seq_start[s + 1] - 1] + 1) {
+          H[o_work + 1 + 2 * n] = s;
+          H[o_work + 2 + 2 * n] = cc;
+          ++n;
+        }
+    H[o_work] = n;
+    o += 1 + 2 * (size_t)n;
+  }
   if (o > m->wl.meta_ints) return fail(DEC_ERANGE, "step metadata exceeds the workspace");
 
   int32_t* dmeta = (int32_t*)(m->ws + m->wl.META);
@@ -902,6 +917,8 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   sp.decode = decode;
   sp.rows_all = rows_mode == DEC_ROWS_ALL;
   sp.n_work = (int)work.size();
+  // decode attention grid: one CTA per 128-key chunk of the longest sequence, rounded
+  // up to a multiple of 4 chunks so a captured graph serves 512 positions of growth
   // decode attention grid: one CTA per 128-key chunk of the longest sequence, rounded
   // up to a multiple of 4 chunks so a captured graph serves 512 positions of growth
   sp.slots = std::min(m->NCH, ((max_ctx + kDecodeChunk - 1) / kDecodeChunk + 3) / 4 * 4);

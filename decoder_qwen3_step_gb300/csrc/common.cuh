@@ -26,6 +26,8 @@ constexpr int kDecodeChunk = 128; // keys per split-K work item of decode attent
 // Device error word bits (mirrors DEC_DEV_* in include/dec.h).
 constexpr uint32_t kErrBadId = 1u;
 constexpr uint32_t kErrTimeout = 2u;
+constexpr uint32_t kErrCapacity = 4u;  // a kernel's fixed-size list overflowed (the host sizes grids to avoid it)
+constexpr int kMaxPositions = 40960;    // the longest context a model may be built for (Qwen3's limit)
 
 using bf16 = __nv_bfloat16;
 
@@ -123,6 +125,22 @@ __device__ __forceinline__ float row_rstd(const float* ssq, int t, int d, float 
   for (int c = threadIdx.x & 31; c < nch; c += 32) s += p[c];
   s = warp_sum(s);
   return 1.0f / sqrtf(s / (float)d + eps);
+}
+
+// row_rstd for up to U consecutive token rows t0 .. t0+n-1 at once (their
+// partial loads overlap); the same summation order as row_rstd.  Whole warp.
+template <int U>
+__device__ __forceinline__ void row_rstd_n(const float* ssq, int t0, int n, int d, float eps, float* out) {
+  const int nch = d / kSsqChunk, lane = threadIdx.x & 31;
+  float s[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    s[u] = 0.f;
+    if (u < n)
+      for (int c = lane; c < nch; c += 32) s[u] += ssq[(size_t)(t0 + u) * nch + c];
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) out[u] = 1.0f / sqrtf(warp_sum(s[u]) / (float)d + eps);
 }
 
 // Order-preserving 64-bit key of (logit, id): larger logit wins, then lower id.

@@ -19,56 +19,104 @@ namespace dec {
 // product's input where that input is written (the RESID epilogue, the
 // embedding), its 1/rms scales the product's output rows here.
 // ---------------------------------------------------------------------------
+// Store 4 consecutive values of the activation type (8 bytes of bf16 or 16 of fp32).
+__device__ __forceinline__ void store4(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store4(bf16* p, float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// Every thread takes 4 consecutive weight rows of one token row: the
+// residual, activations and logits move in 128-bit pieces, and the loads of
+// U such pieces are issued before any store.
 template <typename AT, int EPI, int NT>
 __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, int ld, int r0, int nrows, int t0,
                                          int ntok, const float* rstd_s, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
-  const int total = ntok * nrows;
+  const int nq = nrows / 4;  // 4-row groups per token row
+  const int total = ntok * nq;
   if (EPI == EPI_QKV_RAW) {
     for (int i = tid; i < total; i += NT) {
-      const int t = i / nrows, r = i - t * nrows;
-      a.out_f32[(size_t)(t0 + t) * a.rows + r0 + r] = tile[r * ld + t] * rstd_s[t];
+      const int t = i / nq, r = (i - t * nq) * 4;
+      const float rs = rstd_s[t];
+      store4(a.out_f32 + (size_t)(t0 + t) * a.rows + r0 + r, tile[r * ld + t] * rs, tile[(r + 1) * ld + t] * rs,
+             tile[(r + 2) * ld + t] * rs, tile[(r + 3) * ld + t] * rs);
     }
   } else if (EPI == EPI_RESID) {
     AT* XN = reinterpret_cast<AT*>(a.XN);
     const int nch = a.d / kSsqChunk;
-    for (int base = warp * 32; base < total; base += NT) {  // whole warps; validity is per half-warp
-      const int i = base + lane;
-      const bool valid = i < total;
-      const int t = i / nrows, r = i - t * nrows;
-      float x = 0.f;
-      if (valid) {
-        const size_t off = (size_t)(t0 + t) * a.d + r0 + r;
-        x = a.X_res[off] + tile[r * ld + t];
-        a.X_res[off] = x;
-        XN[off] = from_f32<AT>(x * a.w_next[r0 + r]);
+    constexpr int U = 4;
+    // whole warps; a 16-feature chunk is 4 consecutive lanes, valid or not together
+    for (int base = warp * 32; base < total; base += NT * U) {
+      float4 xr[U], wr[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = base + u * NT + lane;
+        xr[u] = wr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < total) {
+          const int t = i / nq, r = (i - t * nq) * 4;
+          xr[u] = *reinterpret_cast<const float4*>(a.X_res + (size_t)(t0 + t) * a.d + r0 + r);
+          wr[u] = *reinterpret_cast<const float4*>(a.w_next + r0 + r);
+        }
       }
-      const float sq = half_warp_sum(x * x);
-      if (valid && (r & (kSsqChunk - 1)) == 0) a.SSQ_out[(size_t)(t0 + t) * nch + (r0 + r) / kSsqChunk] = sq;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = base + u * NT + lane;
+        const bool valid = i < total;
+        const int t = i / nq, r = (i - t * nq) * 4;
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        if (valid) {
+          x0 = xr[u].x + tile[r * ld + t];
+          x1 = xr[u].y + tile[(r + 1) * ld + t];
+          x2 = xr[u].z + tile[(r + 2) * ld + t];
+          x3 = xr[u].w + tile[(r + 3) * ld + t];
+          const size_t off = (size_t)(t0 + t) * a.d + r0 + r;
+          store4(a.X_res + off, x0, x1, x2, x3);
+          store4(XN + off, x0 * wr[u].x, x1 * wr[u].y, x2 * wr[u].z, x3 * wr[u].w);
+        }
+        float sq = (x0 * x0 + x1 * x1) + (x2 * x2 + x3 * x3);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        if (valid && (r & (kSsqChunk - 1)) == 0) a.SSQ_out[(size_t)(t0 + t) * nch + (r0 + r) / kSsqChunk] = sq;
+      }
     }
   } else if (EPI == EPI_SWIGLU) {
     AT* out = reinterpret_cast<AT*>(a.act_out);
-    const int half = nrows / 2;
-    for (int i = tid; i < ntok * half; i += NT) {
-      const int t = i / half, j = i - t * half;
-      const int grp = j / kGuGroup, jj = j % kGuGroup;
-      const float g = tile[(grp * 2 * kGuGroup + jj) * ld + t] * rstd_s[t];
-      const float u = tile[(grp * 2 * kGuGroup + kGuGroup + jj) * ld + t] * rstd_s[t];
-      out[(size_t)(t0 + t) * a.F + (r0 / (2 * kGuGroup) + grp) * kGuGroup + jj] = from_f32<AT>(silu(g) * u);
+    const int ng = nrows / 8;  // groups of 4 outputs per token row (gate/up interleave in 8s)
+    for (int i = tid; i < ntok * ng; i += NT) {
+      const int t = i / ng, q = i - t * ng;
+      const int grp = q >> 1, jj = (q & 1) * 4;
+      const float rs = rstd_s[t];
+      const int rg = grp * 2 * kGuGroup + jj, ru = rg + kGuGroup;
+      float o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = silu(tile[(rg + e) * ld + t] * rs) * (tile[(ru + e) * ld + t] * rs);
+      store4(out + (size_t)(t0 + t) * a.F + (r0 / (2 * kGuGroup) + grp) * kGuGroup + jj, o[0], o[1], o[2], o[3]);
     }
   } else {  // EPI_LOGITS
     for (int base = warp * 32; base < total; base += NT) {
       const int i = base + lane;
       const bool valid = i < total;
-      const int t = i / nrows, r = i - t * nrows;
+      const int t = i / nq, r = (i - t * nq) * 4;
       unsigned long long key = 0ull;
       if (valid) {
-        const float v = tile[r * ld + t] * rstd_s[t];
-        if (a.out_f32) a.out_f32[(size_t)(t0 + t) * a.rows + r0 + r] = v;
-        key = argmax_key(v, r0 + r);
+        const float rs = rstd_s[t];
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[e] = tile[(r + e) * ld + t] * rs;
+          const unsigned long long k = argmax_key(v[e], r0 + r + e);
+          key = k > key ? k : key;
+        }
+        if (a.out_f32) store4(a.out_f32 + (size_t)(t0 + t) * a.rows + r0 + r, v[0], v[1], v[2], v[3]);
       }
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
+      for (int o = 1; o <= 2; o <<= 1) {
         const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
         key = other > key ? other : key;
       }
@@ -109,6 +157,28 @@ __device__ __forceinline__ void qkv_store(const QkvFuse& f, int tt, int gh, int 
       from_f32<KT>(v);
 }
 
+// qkv_store for 4 consecutive rows j .. j+3 of one head (16 bytes of Q, or
+// 4 cache elements).
+template <typename KT>
+__device__ __forceinline__ void qkv_store4(const QkvFuse& f, int tt, int gh, int j, const float* v, int pos, int blk) {
+  if (gh < f.H) {
+    store4(f.Q + ((size_t)tt * f.H + gh) * f.D + j, v[0], v[1], v[2], v[3]);
+    return;
+  }
+  const int is_v = gh >= f.H + f.Hkv;
+  const int h = gh - f.H - (is_v ? f.Hkv : 0);
+  KT* p = reinterpret_cast<KT*>(f.kv) + kv_offset(f.layer, blk, is_v, h, pos % f.B, f.n_blocks, f.Hkv, f.B, f.D) + j;
+  if constexpr (sizeof(KT) == 4) {
+    store4(reinterpret_cast<float*>(p), v[0], v[1], v[2], v[3]);
+  } else {
+    __half2 lo = __floats2half2_rn(v[0], v[1]), hi = __floats2half2_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+}
+
 // Fused QKV epilogue over a tile of whole heads: y = acc * rstd; per query or
 // key head RMSNorm over its D rows with the shared gain, then split-half RoPE
 // at the token's position; queries to Q, keys and values into the cache.
@@ -135,18 +205,33 @@ __device__ __forceinline__ void epilogue_qkv_tile(const GemvArgs& a, const float
     tblk[t] = qkv_block(f, t0 + t, pos);
   }
   sync();
-  const int half = D / 2;
-  for (int i = tid; i < ntok * nrows; i += NT) {
-    const int t = i / nrows, r = i - t * nrows;
+  const int half = D / 2, nq = nrows / 4;
+  for (int i = tid; i < ntok * nq; i += NT) {
+    const int t = i / nq, r = (i - t * nq) * 4;  // rows r .. r+3 of one head (D is a multiple of 4)
     const int hh = r / D, j = r - hh * D;
     const int gh = (r0 + hh * D) / D;
-    const float y = tile[r * ld + t] * rstd_s[t];
-    float out = y;
+    const float rs = rstd_s[t];
+    float out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) out[e] = tile[(r + e) * ld + t] * rs;
     if (gh < f.H + f.Hkv) {
+      const float* g = gh < f.H ? f.q_norm : f.k_norm;
+      const int jj = j < half ? j : j - half, jp = j < half ? j + half : j - half;
       const int rp = j < half ? r + half : r - half;
-      out = qk_rope(f, gh, j, y, tile[rp * ld + t] * rstd_s[t], rn[hh * ntok + t], tpos[t]);
+      const float4 g0 = *reinterpret_cast<const float4*>(g + j);
+      const float4 g1 = *reinterpret_cast<const float4*>(g + jp);
+      const float4 cs0 = *reinterpret_cast<const float4*>(f.rope + ((size_t)tpos[t] * half + jj) * 2);
+      const float4 cs1 = *reinterpret_cast<const float4*>(f.rope + ((size_t)tpos[t] * half + jj) * 2 + 4);
+      const float rn_ = rn[hh * ntok + t];
+      const float ga[4] = {g0.x, g0.y, g0.z, g0.w}, gb[4] = {g1.x, g1.y, g1.z, g1.w};
+      const float c4[4] = {cs0.x, cs0.z, cs1.x, cs1.z}, s4[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a_ = out[e] * rn_ * ga[e], b_ = tile[(rp + e) * ld + t] * rs * rn_ * gb[e];
+        out[e] = j < half ? a_ * c4[e] - b_ * s4[e] : a_ * c4[e] + b_ * s4[e];
+      }
     }
-    qkv_store<KT>(f, t0 + t, gh, j, out, tpos[t], tblk[t]);
+    qkv_store4<KT>(f, t0 + t, gh, j, out, tpos[t], tblk[t]);
   }
 }
 

@@ -81,6 +81,7 @@ struct Raw {
 // ---------------------------------------------------------------------------
 constexpr int kDecWarps = 4;
 constexpr int kDecBlocks = kDecodeChunk / 16;  // 8
+constexpr int kMaxChunks = (kMaxPositions + kDecodeChunk - 1) / kDecodeChunk;
 
 template <typename KT, int D>
 __host__ __device__ constexpr size_t decode_smem_bytes() {
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) k_attn_decode(AttnArgs a) {
   __shared__ float qs[G][D];
   __shared__ float ms[kDecWarps][G], ls[kDecWarps][G];
   __shared__ float os[kDecWarps][G][D];
-  __shared__ float fac[G][64];
+  __shared__ float fac[G][kMaxChunks];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int last_flag, abort_flag;
   const int t = a.meta.seq_start[s];

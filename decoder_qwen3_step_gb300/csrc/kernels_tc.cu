@@ -26,7 +26,8 @@
 namespace dec {
 
 constexpr int kTcM = 128, kTcN = 128, kTcK = 64, kTcStages = 4;
-constexpr int kTcThreads = 192;
+constexpr int kTcEpiThreads = 256;  // 8 epilogue warps, two per TMEM lane quarter
+constexpr int kTcThreads = 64 + kTcEpiThreads;
 constexpr int kTcTileLd = kTcN + 1;
 constexpr uint32_t kTcStageA = kTcM * kTcK * 2;  // 16 KB
 constexpr uint32_t kTcStageB = kTcN * kTcK * 2;  // 16 KB
@@ -71,7 +72,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh->tfull[i], 1);
-      mbar_init(&sh->tempty[i], 128);
+      mbar_init(&sh->tempty[i], kTcEpiThreads);
     }
     mbar_init(&sh->mma_done, 1);
     sh->abort_flag = 0;
@@ -155,39 +156,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_commit(&sh->mma_done);
     }
   } else {
-    // epilogue warps: TMEM lane quarter (warp % 4), rows 32*(warp%4) .. +31
+    // epilogue warps: TMEM lane quarter (warp % 4), rows 32*(warp%4) .. +31; warps 2..5
+    // read columns 0..63 of the accumulator, warps 6..9 columns 64..127
     const int et = threadIdx.x - 64;
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, chalf = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile_i = blockIdx.x; tile_i < n_total; tile_i += gridDim.x) {
       const int mt = tile_i % m_tiles, nt = tile_i / m_tiles;
       const int t0 = nt * kTcN, ntok = min(kTcN, a.T - t0);
-      epi_bar();  // the previous tile's epilogue is done with tile/rstd_s
-      for (int t = et >> 5; t < kTcN; t += 4) {
-        float r = 1.0f;
-        if (a.ssq && t < ntok) r = row_rstd(a.ssq, t0 + t, a.d, a.eps);
-        if (lane == 0) rstd_s[t] = r;
+      epi_bar<kTcEpiThreads>();  // the previous tile's epilogue is done with tile/rstd_s
+      {  // 1/rms of this tile's tokens: warp w takes tokens 16w .. 16w+15, 8 at a time
+        const int wq = et >> 5;
+#pragma unroll 1
+        for (int t8 = wq * 16; t8 < wq * 16 + 16; t8 += 8) {
+          float r8[8];
+          const int n = max(0, min(8, ntok - t8));
+          if (a.ssq) {
+            row_rstd_n<8>(a.ssq, t0 + t8, n, a.d, a.eps, r8);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) r8[u] = 1.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (lane == u) rstd_s[t8 + u] = r8[u];
+        }
       }
       const bool got = mbar_wait(&sh->tfull[acc], acc_phase, abort_flag, err);
-      if (epi_any(!got)) break;
+      if (epi_any<kTcEpiThreads>(!got)) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int slab = 0; slab < kTcN / 32; ++slab) {
+      for (int slab = 0; slab < 2; ++slab) {
+        const int col = chalf * 64 + slab * 32;
         uint32_t v[32];
-        tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * kTcAccCols + slab * 32, v);
+        tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * kTcAccCols + col, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) tile[row * kTcTileLd + slab * 32 + j] = __uint_as_float(v[j]);
+        for (int j = 0; j < 32; ++j) tile[row * kTcTileLd + col + j] = __uint_as_float(v[j]);
       }
       tc_fence_before();
       mbar_arrive(&sh->tempty[acc]);
-      epi_bar();
+      epi_bar<kTcEpiThreads>();
       if constexpr (EPI == EPI_QKV) {
-        epilogue_qkv_tile<__half, 128>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, sh->rn, sh->tpos,
-                                       sh->tblk, et, EpiBar{});
+        epilogue_qkv_tile<__half, kTcEpiThreads>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, sh->rn,
+                                                 sh->tpos, sh->tblk, et, EpiBar<kTcEpiThreads>{});
       } else {
-        epilogue<AT, EPI, 128>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, et);
+        epilogue<AT, EPI, kTcEpiThreads>(a, tile, kTcTileLd, mt * kTcM, kTcM, t0, ntok, rstd_s, et);
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;

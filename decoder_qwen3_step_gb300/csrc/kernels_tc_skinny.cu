@@ -152,10 +152,19 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     pdl_wait();
-    for (int t = et >> 5; t < kSkN; t += 4) {
-      float r = 1.0f;
-      if (a.ssq && t < ntok) r = row_rstd(a.ssq, t, a.d, a.eps);
-      if (lane == 0) rstd_s[t] = r;
+    {  // 1/rms of the tokens: warp w takes tokens 8w .. 8w+7 at once
+      const int t8 = (et >> 5) * 8;
+      float r8[8];
+      const int n = max(0, min(8, ntok - t8));
+      if (a.ssq) {
+        row_rstd_n<8>(a.ssq, t8, n, a.d, a.eps, r8);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) r8[u] = 1.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (lane == u) rstd_s[t8 + u] = r8[u];
     }
     const bool got = mbar_wait(&sh->tfull, 0, abort_flag, err);
     if (!epi_any(!got)) {

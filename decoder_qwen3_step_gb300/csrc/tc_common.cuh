@@ -121,28 +121,33 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier 1 over the N epilogue threads of a CTA.
+template <int N = 128>
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
 
-// OR of a flag over the 128 epilogue threads (named barrier 1): every
+// OR of a flag over the N epilogue threads (named barrier 1): every
 // epilogue thread takes the same branch after it, so none can be left
 // waiting at a later barrier.
+template <int N = 128>
 __device__ __forceinline__ bool epi_any(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "n"(N)
       : "memory");
   return r != 0;
 }
 
-
 // Callable form of epi_bar for epilogue helpers that need a phase barrier.
+template <int N = 128>
 struct EpiBar {
-  __device__ __forceinline__ void operator()() const { epi_bar(); }
+  __device__ __forceinline__ void operator()() const { epi_bar<N>(); }
 };
 
 // ---- clusters ----------------------------------------------------------------

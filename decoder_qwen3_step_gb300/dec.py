@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libdec.so")
 DEC_OK, DEC_EINVAL, DEC_ECAPACITY, DEC_EBLOCK, DEC_ERANGE, DEC_EVOCAB, DEC_ECUDA, DEC_EDEVICE = range(8)
 DEC_FP32, DEC_BF16_F16KV = 0, 1
 DEC_ROWS_ALL, DEC_ROWS_LAST = 0, 1
-DEC_DEV_BAD_ID, DEC_DEV_TIMEOUT = 1, 2
+DEC_DEV_BAD_ID, DEC_DEV_TIMEOUT, DEC_DEV_CAPACITY = 1, 2, 4
 
 ERROR_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ECAPACITY", 3: "DEC_EBLOCK", 4: "DEC_ERANGE",
                5: "DEC_EVOCAB", 6: "DEC_ECUDA", 7: "DEC_EDEVICE"}

@@ -68,7 +68,7 @@ extern "C" {
  * DEC_EINVAL, never served wrong (tinyllm L10.1 section 2.3). */
 typedef struct dec_config {
     int32_t vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ff_hidden;
-    int32_t max_positions; /* positions 0 .. max_positions-1 are valid */
+    int32_t max_positions; /* positions 0 .. max_positions-1 are valid; at most 40,960 */
     int32_t block_tokens;  /* KV block size B; 16 */
     int32_t mode;          /* DEC_FP32 or DEC_BF16_F16KV */
     double rope_base;      /* 1e6 for Qwen3 */
@@ -125,6 +125,7 @@ const char* dec_last_error(void);
 /* Device error word bits (dec_device_status). */
 #define DEC_DEV_BAD_ID   1u /* a device-side token id was outside the vocabulary */
 #define DEC_DEV_TIMEOUT  2u /* a bounded wait in a kernel gave up */
+#define DEC_DEV_CAPACITY 4u /* a kernel's fixed-size work list overflowed */
 
 /* ---- model ---------------------------------------------------------------- */
 /* Check a config; DEC_OK if the decoder can run it. */
