@@ -8,9 +8,11 @@
 namespace dec {
 
 // ---------------------------------------------------------------------------
-// Fused epilogues of the weight products, shared by the streaming kernel and
-// the tiled kernel.  tile[r * ld + t] holds y for weight row r0 + r and token
-// row t0 + t (r < nrows, t < ntok; nrows is a multiple of 16).
+// Fused epilogues of the weight products, shared by every product kernel.
+// The staged output tile is token-major: tile[t * ld + r] holds y for weight
+// row r0 + r and token row t0 + t (r < nrows, t < ntok; nrows a multiple of
+// 16, ld a multiple of 4, the tile 16-byte aligned), so a thread's 4
+// consecutive rows are one conflict-free 128-bit shared-memory load.
 //   QKV_RAW : y * rstd -> raw q|k|v (QK-norm/RoPE/cache write follow)
 //   RESID   : x += y ; next GEMM input x * w_next ; 16-feature sum of squares
 //   SWIGLU  : silu(rstd * gate) * (rstd * up), gate/up interleaved by 8 rows
@@ -31,6 +33,10 @@ __device__ __forceinline__ void store4(bf16* p, float a, float b, float c, float
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+__device__ __forceinline__ float4 rows4(const float* tile, int ld, int r, int t) {
+  return *reinterpret_cast<const float4*>(tile + t * ld + r);
+}
+
 // Every thread takes 4 consecutive weight rows of one token row: the
 // residual, activations and logits move in 128-bit pieces, and the loads of
 // U such pieces are issued before any store.
@@ -44,8 +50,8 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
     for (int i = tid; i < total; i += NT) {
       const int t = i / nq, r = (i - t * nq) * 4;
       const float rs = rstd_s[t];
-      store4(a.out_f32 + (size_t)(t0 + t) * a.rows + r0 + r, tile[r * ld + t] * rs, tile[(r + 1) * ld + t] * rs,
-             tile[(r + 2) * ld + t] * rs, tile[(r + 3) * ld + t] * rs);
+      const float4 y = rows4(tile, ld, r, t);
+      store4(a.out_f32 + (size_t)(t0 + t) * a.rows + r0 + r, y.x * rs, y.y * rs, y.z * rs, y.w * rs);
     }
   } else if (EPI == EPI_RESID) {
     AT* XN = reinterpret_cast<AT*>(a.XN);
@@ -71,10 +77,11 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
         const int t = i / nq, r = (i - t * nq) * 4;
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
         if (valid) {
-          x0 = xr[u].x + tile[r * ld + t];
-          x1 = xr[u].y + tile[(r + 1) * ld + t];
-          x2 = xr[u].z + tile[(r + 2) * ld + t];
-          x3 = xr[u].w + tile[(r + 3) * ld + t];
+          const float4 y = rows4(tile, ld, r, t);
+          x0 = xr[u].x + y.x;
+          x1 = xr[u].y + y.y;
+          x2 = xr[u].z + y.z;
+          x3 = xr[u].w + y.w;
           const size_t off = (size_t)(t0 + t) * a.d + r0 + r;
           store4(a.X_res + off, x0, x1, x2, x3);
           store4(XN + off, x0 * wr[u].x, x1 * wr[u].y, x2 * wr[u].z, x3 * wr[u].w);
@@ -93,9 +100,11 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
       const int grp = q >> 1, jj = (q & 1) * 4;
       const float rs = rstd_s[t];
       const int rg = grp * 2 * kGuGroup + jj, ru = rg + kGuGroup;
+      const float4 g4 = rows4(tile, ld, rg, t), u4 = rows4(tile, ld, ru, t);
+      const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
       float o[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[e] = silu(tile[(rg + e) * ld + t] * rs) * (tile[(ru + e) * ld + t] * rs);
+      for (int e = 0; e < 4; ++e) o[e] = silu(gv[e] * rs) * (uv[e] * rs);
       store4(out + (size_t)(t0 + t) * a.F + (r0 / (2 * kGuGroup) + grp) * kGuGroup + jj, o[0], o[1], o[2], o[3]);
     }
   } else {  // EPI_LOGITS
@@ -106,10 +115,12 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
       unsigned long long key = 0ull;
       if (valid) {
         const float rs = rstd_s[t];
+        const float4 y = rows4(tile, ld, r, t);
+        const float yv[4] = {y.x, y.y, y.z, y.w};
         float v[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          v[e] = tile[(r + e) * ld + t] * rs;
+          v[e] = yv[e] * rs;
           const unsigned long long k = argmax_key(v[e], r0 + r + e);
           key = k > key ? k : key;
         }
@@ -193,9 +204,12 @@ __device__ __forceinline__ void epilogue_qkv_tile(const GemvArgs& a, const float
     const int t = i % ntok, hh = i / ntok;
     const float rs = rstd_s[t];
     float ss = 0.f;
-    for (int j = 0; j < D; ++j) {
-      const float y = tile[(hh * D + j) * ld + t] * rs;
-      ss = fmaf(y, y, ss);
+    for (int j = 0; j < D; j += 4) {
+      const float4 y = rows4(tile, ld, hh * D + j, t);
+      ss = fmaf(y.x * rs, y.x * rs, ss);
+      ss = fmaf(y.y * rs, y.y * rs, ss);
+      ss = fmaf(y.z * rs, y.z * rs, ss);
+      ss = fmaf(y.w * rs, y.w * rs, ss);
     }
     rn[hh * ntok + t] = 1.0f / sqrtf(ss / (float)D + a.eps);
   }
@@ -211,9 +225,8 @@ __device__ __forceinline__ void epilogue_qkv_tile(const GemvArgs& a, const float
     const int hh = r / D, j = r - hh * D;
     const int gh = (r0 + hh * D) / D;
     const float rs = rstd_s[t];
-    float out[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) out[e] = tile[(r + e) * ld + t] * rs;
+    const float4 y4 = rows4(tile, ld, r, t);
+    float out[4] = {y4.x * rs, y4.y * rs, y4.z * rs, y4.w * rs};
     if (gh < f.H + f.Hkv) {
       const float* g = gh < f.H ? f.q_norm : f.k_norm;
       const int jj = j < half ? j : j - half, jp = j < half ? j + half : j - half;
@@ -225,9 +238,11 @@ __device__ __forceinline__ void epilogue_qkv_tile(const GemvArgs& a, const float
       const float rn_ = rn[hh * ntok + t];
       const float ga[4] = {g0.x, g0.y, g0.z, g0.w}, gb[4] = {g1.x, g1.y, g1.z, g1.w};
       const float c4[4] = {cs0.x, cs0.z, cs1.x, cs1.z}, s4[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
+      const float4 p4 = rows4(tile, ld, rp, t);
+      const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float a_ = out[e] * rn_ * ga[e], b_ = tile[(rp + e) * ld + t] * rs * rn_ * gb[e];
+        const float a_ = out[e] * rn_ * ga[e], b_ = pv[e] * rs * rn_ * gb[e];
         out[e] = j < half ? a_ * c4[e] - b_ * s4[e] : a_ * c4[e] + b_ * s4[e];
       }
     }

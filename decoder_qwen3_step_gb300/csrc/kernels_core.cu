@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(GemvArgs a) {
   pdl_wait_prev();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   AT* xs = reinterpret_cast<AT*>(smem_raw);  // [kGemvTok][K]
-  __shared__ float outs[kGemvRows * kGemvTok];
+  __shared__ __align__(16) float outs[kGemvTok * kGemvRows];  // token-major [token][row]
   __shared__ float rstd_s[kGemvTok];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * kGemvRows;
@@ -116,12 +116,12 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(GemvArgs a) {
       const float v0 = warp_sum(acc0[t]);
       const float v1 = warp_sum(acc1[t]);
       if (lane == t) {
-        outs[(warp * 2) * kGemvTok + t] = v0;
-        outs[(warp * 2 + 1) * kGemvTok + t] = v1;
+        outs[t * kGemvRows + warp * 2] = v0;
+        outs[t * kGemvRows + warp * 2 + 1] = v1;
       }
     }
     __syncthreads();
-    epilogue<AT, EPI, kGemvThreads>(a, outs, kGemvTok, r0, kGemvRows, t0, tc, rstd_s, threadIdx.x);
+    epilogue<AT, EPI, kGemvThreads>(a, outs, kGemvRows, r0, kGemvRows, t0, tc, rstd_s, threadIdx.x);
     __syncthreads();
   }
 }
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kTThreads) k_gemm_tiled(GemvArgs a) {
   extern __shared__ __align__(16) float tsm[];
   float* As = tsm;                      // [2][kTK][kTLd]   tokens
   float* Bs = tsm + 2 * kTK * kTLd;     // [2][kTK][kTLd]   weight rows
-  float* tile = tsm;                    // epilogue [kTN][kTM + 1], aliases As/Bs
+  float* tile = tsm;                    // epilogue, token-major [kTM][kTN + 4], aliases As/Bs
   __shared__ float rstd_s[kTM];
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -205,18 +205,16 @@ __global__ void __launch_bounds__(kTThreads) k_gemm_tiled(GemvArgs a) {
     if (more) sstore(buf ^ 1);
     __syncthreads();
   }
-  // stage the tile as [weight row][token] for the epilogue
+  // stage the tile token-major for the epilogue: 4 consecutive rows per 128-bit store
+  constexpr int kLd = kTN + 4;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int t = (i < 4 ? 0 : 64) + ty * 4 + (i & 3);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int r = (j < 4 ? 0 : 64) + tx * 4 + (j & 3);
-      tile[r * (kTM + 1) + t] = acc[i][j];
-    }
+    *reinterpret_cast<float4*>(tile + t * kLd + tx * 4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4*>(tile + t * kLd + 64 + tx * 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
   }
   __syncthreads();
-  epilogue<AT, EPI, kTThreads>(a, tile, kTM + 1, n0, min(kTN, a.rows - n0), m0, min(kTM, a.T - m0), rstd_s,
+  epilogue<AT, EPI, kTThreads>(a, tile, kLd, n0, min(kTN, a.rows - n0), m0, min(kTM, a.T - m0), rstd_s,
                                threadIdx.x);
 }
 
@@ -322,7 +320,7 @@ static cudaError_t gemv_one(const GemvArgs& a, cudaStream_t s) {
     return cudaGetLastError();
   }
   static bool configured_t = false;
-  const int smem = kTN * (kTM + 1) * (int)sizeof(float);
+  const int smem = kTM * (kTN + 4) * (int)sizeof(float);
   if (!configured_t) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tiled<WT, AT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -28,7 +28,7 @@ namespace dec {
 constexpr int kTcM = 128, kTcN = 128, kTcK = 64, kTcStages = 4;
 constexpr int kTcEpiThreads = 256;  // 8 epilogue warps, two per TMEM lane quarter
 constexpr int kTcThreads = 64 + kTcEpiThreads;
-constexpr int kTcTileLd = kTcN + 1;
+constexpr int kTcTileLd = kTcM + 4;  // epilogue tile, token-major [kTcN tokens][kTcTileLd]
 constexpr uint32_t kTcStageA = kTcM * kTcK * 2;  // 16 KB
 constexpr uint32_t kTcStageB = kTcN * kTcK * 2;  // 16 KB
 constexpr uint32_t kTcAccCols = 128;             // fp32 columns per accumulator
@@ -42,7 +42,7 @@ struct TcShared {
 };
 
 constexpr size_t kTcSmemBytes =
-    1024 + (size_t)kTcStages * (kTcStageA + kTcStageB) + (size_t)kTcM * kTcTileLd * 4 + kTcN * 4 + sizeof(TcShared);
+    1024 + (size_t)kTcStages * (kTcStageA + kTcStageB) + (size_t)kTcN * kTcTileLd * 4 + kTcN * 4 + sizeof(TcShared);
 
 template <typename AT, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sA = base;
   uint8_t* sB = base + kTcStages * kTcStageA;
   float* tile = reinterpret_cast<float*>(sB + kTcStages * kTcStageB);
-  float* rstd_s = tile + kTcM * kTcTileLd;
+  float* rstd_s = tile + kTcN * kTcTileLd;
   TcShared* sh = reinterpret_cast<TcShared*>(rstd_s + kTcN);
   volatile int* abort_flag = &sh->abort_flag;
 
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t v[32];
         tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * kTcAccCols + col, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) tile[row * kTcTileLd + col + j] = __uint_as_float(v[j]);
+        for (int j = 0; j < 32; ++j) tile[(col + j) * kTcTileLd + row] = __uint_as_float(v[j]);
       }
       tc_fence_before();
       mbar_arrive(&sh->tempty[acc]);

@@ -26,7 +26,8 @@ namespace dec {
 
 constexpr int kSkM = 128, kSkN = 32, kSkK = 64, kSkStages = 4;
 constexpr int kSkThreads = 192;
-constexpr int kSkLd = kSkN + 1;
+constexpr int kSkLd = kSkM + 4;     // partial tile, token-major [kSkN tokens][kSkLd]
+constexpr int kSkRedLd = 64 + 4;    // reduced rows of one CTA (at most 64), token-major
 constexpr uint32_t kSkStageA = kSkM * kSkK * 2;  // 16 KB
 constexpr uint32_t kSkStageB = kSkN * kSkK * 2;  // 4 KB
 constexpr uint32_t kSkCols = 32;
@@ -41,9 +42,8 @@ struct SkShared {
   int consumed;
 };
 
-constexpr int kSkRedRows = 64;  // reduced rows per CTA when the K split is >= 2
-constexpr size_t kSkSmemBytes = 1024 + (size_t)kSkStages * (kSkStageA + kSkStageB) + (size_t)kSkM * kSkLd * 4 +
-                                (size_t)kSkRedRows * kSkLd * 4 + kSkN * 4 + sizeof(SkShared);
+constexpr size_t kSkSmemBytes = 1024 + (size_t)kSkStages * (kSkStageA + kSkStageB) + (size_t)kSkN * kSkLd * 4 +
+                                (size_t)kSkN * kSkRedLd * 4 + kSkN * 4 + sizeof(SkShared);
 
 template <typename AT, int EPI>
 __global__ void __launch_bounds__(kSkThreads, 1)
@@ -53,9 +53,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sk_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + kSkStages * kSkStageA;
-  float* tile = reinterpret_cast<float*>(sB + kSkStages * kSkStageB);  // [128][33] this CTA's partial
-  float* red = tile + kSkM * kSkLd;                                     // [<=64][33] reduced rows
-  float* rstd_s = red + kSkRedRows * kSkLd;
+  float* tile = reinterpret_cast<float*>(sB + kSkStages * kSkStageB);  // this CTA's partial, token-major
+  float* red = tile + kSkN * kSkLd;                                     // reduced rows, token-major
+  float* rstd_s = red + kSkN * kSkRedLd;
   SkShared* sh = reinterpret_cast<SkShared*>(rstd_s + kSkN);
   volatile int* abort_flag = &sh->abort_flag;
 
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       uint32_t v[32];
       tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16), v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) tile[row * kSkLd + j] = __uint_as_float(v[j]);
+      for (int j = 0; j < 32; ++j) tile[j * kSkLd + row] = __uint_as_float(v[j]);
     }
   }
 
@@ -180,23 +180,25 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int rows_per = ks <= 8 ? kSkM / ks : 16;
   const int r_lo = z * rows_per;
   const bool has_rows = !*abort_flag && r_lo < kSkM;
-  const float* src = tile + r_lo * kSkLd;  // this CTA's reduced rows, [rows_per][kSkLd]
+  const float* src = tile + r_lo;  // this CTA's reduced rows: element (row rr, token t) at src[t * src_ld + rr]
+  int src_ld = kSkLd;
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     if (has_rows && ks > 1) {
       for (int i = et; i < rows_per * kSkN; i += 128) {
-        const int rr = i / kSkN, t = i % kSkN;
-        const float* p = tile + (r_lo + rr) * kSkLd + t;
+        const int t = i / rows_per, rr = i - t * rows_per;
+        const float* p = tile + t * kSkLd + r_lo + rr;
         float sum = 0.f;
         for (int q = 0; q < ks; ++q) sum += dsmem_ld(dsmem_addr(p, (uint32_t)q));
-        red[rr * kSkLd + t] = sum;
+        red[t * kSkRedLd + rr] = sum;
       }
       src = red;
+      src_ld = kSkRedLd;
     }
     if constexpr (EPI != EPI_QKV) {
       if (has_rows) {
         epi_bar();
-        epilogue<AT, EPI, 128>(a, src, kSkLd, mt * kSkM + r_lo, rows_per, 0, ntok, rstd_s, et);
+        epilogue<AT, EPI, 128>(a, src, src_ld, mt * kSkM + r_lo, rows_per, 0, ntok, rstd_s, et);
       }
     } else {
       // partial sums of squares of this CTA's rows, per (head in the tile, token)
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           const int a0 = max(hl * D, r_lo), a1 = min(hl * D + D, r_lo + rows_per);
           float ss = 0.f;
           for (int r = a0; r < a1; ++r) {
-            const float y = src[(r - r_lo) * kSkLd + t] * rstd_s[t];
+            const float y = src[t * src_ld + (r - r_lo)] * rstd_s[t];
             ss = fmaf(y, y, ss);
           }
           sh->psq[hl][t] = ss;
@@ -242,13 +244,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const int t = i / rows_per, rr = i - t * rows_per;
         const int r = r_lo + rr, hl = r / D, j = r - hl * D;
         const int gh = (mt * kSkM + hl * D) / D;
-        const float y = src[rr * kSkLd + t] * rstd_s[t];
+        const float y = src[t * src_ld + rr] * rstd_s[t];
         float out = y;
         if (gh < f.H + f.Hkv) {
           const int rp = j < half ? r + half : r - half;
           const int zo = rp / rows_per;
-          const float yp = zo == z ? src[(rp - r_lo) * kSkLd + t]
-                                   : dsmem_ld(dsmem_addr(red + (rp - zo * rows_per) * kSkLd + t, (uint32_t)zo));
+          const float yp = zo == z ? src[t * src_ld + (rp - r_lo)]
+                                   : dsmem_ld(dsmem_addr(red + t * kSkRedLd + (rp - zo * rows_per), (uint32_t)zo));
           out = qk_rope(f, gh, j, y, yp * rstd_s[t], sh->rn[hl][t], sh->tpos[t]);
         }
         qkv_store<__half>(f, t, gh, j, out, sh->tpos[t], sh->tblk[t]);
