@@ -16,6 +16,7 @@
 
 #include "../../include/dec.h"
 #include "common.cuh"
+#include "internal.h"
 #include "launch.h"
 
 using namespace dec;
@@ -33,6 +34,15 @@ int fail(int code, const char* fmt, ...) {
   g_err = buf;
   return code;
 }
+
+}  // namespace
+
+int dec::set_error(int code, const char* msg) {
+  g_err = msg;
+  return code;
+}
+
+namespace {
 
 #define DEC_CUDA(call)                                                                  \
   do {                                                                                  \
@@ -152,13 +162,6 @@ struct GraphEntry {
 
 }  // namespace
 
-struct dec_pool {
-  dec_config cfg;
-  int n_blocks;
-  void* slabs;
-  std::vector<int32_t> refs;
-  std::vector<int32_t> free_list;  // stack; top = next id handed out
-};
 
 struct dec_model {
   dec_config cfg;

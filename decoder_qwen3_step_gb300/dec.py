@@ -26,7 +26,8 @@ EXPORTS = (
     "dec_device_status", "dec_set_dump", "dec_pool_bytes", "dec_pool_create", "dec_pool_destroy", "dec_pool_alloc",
     "dec_pool_retain", "dec_pool_release", "dec_pool_free_blocks", "dec_pool_refcount", "dec_kv_offset",
     "dec_prefill", "dec_decode", "dec_f32_to_f16", "dec_version", "dec_profile_enable", "dec_profile_read",
-    "dec_launch_count", "dec_set_graphs", "dec_set_tensor_cores", "dec_debug_product",
+    "dec_launch_count", "dec_set_graphs", "dec_set_tensor_cores", "dec_debug_product", "dec_attend_scratch_bytes",
+    "dec_attend",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax")
 
@@ -95,6 +96,8 @@ def lib() -> C.CDLL:
             "dec_set_graphs": (I, [V, C.c_int32]),
             "dec_set_tensor_cores": (I, [V, C.c_int32]),
             "dec_debug_product": (I, [V, C.c_int32, C.c_int32, V, C.c_int32, V, C.c_int32, V]),
+            "dec_attend_scratch_bytes": (I, [cfgp, C.c_int32, C.c_int32, C.c_int32, C.POINTER(SZ)]),
+            "dec_attend": (I, [V, C.c_int32, C.c_int32, V, _I32P, _I32P, C.c_int32, V, V, SZ, V]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -231,6 +231,29 @@ int dec_set_graphs(dec_model* m, int32_t on);
  * graph counts every kernel it contains. */
 int dec_launch_count(dec_model* m, int64_t* launches);
 
+/* ---- decode attention on its own ---------------------------------------------
+ * The split-K kernel dec_decode runs, callable alone: for each of n_seqs
+ * sequences, the query of its newest token (position ctx[s]-1) attends over
+ * keys 0 .. ctx[s]-1 of `layer` in the pool,
+ *   o = sum_j softmax_j(q . k_j / sqrt(D)) v_j,  query head h reading KV head
+ *   floor(h * Hkv / H)   (tinyllm L10.1 section 2.4).
+ *   q            DEVICE fp32 [n_seqs, n_heads, head_dim], after QK-norm and RoPE
+ *   ctx          HOST [n_seqs] context lengths, 1 .. max_positions
+ *   block_table  HOST [n_seqs * max_blocks] (as in dec_batch); every block a
+ *                sequence reads must be allocated in the pool (DEC_EBLOCK)
+ *   out          DEVICE [n_seqs, n_heads * head_dim], fp32 (DEC_FP32) or bf16
+ *   scratch      DEVICE, 256-byte aligned, >= dec_attend_scratch_bytes(...);
+ *                holds the call's metadata, split-K records and merge
+ *                counters; needs no initialisation and is overwritten.  Its
+ *                first 32-bit word is the call's device error word
+ *                (DEC_DEV_TIMEOUT if a bounded wait gave up).
+ * Asynchronous on `stream`; the host arrays may be reused on return. */
+int dec_attend_scratch_bytes(const dec_config* cfg, int32_t n_seqs, int32_t max_ctx, int32_t max_blocks,
+                             size_t* bytes);
+int dec_attend(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float* q, const int32_t* ctx,
+               const int32_t* block_table, int32_t max_blocks, void* out, void* scratch, size_t scratch_bytes,
+               void* stream);
+
 /* Test hook: the device conversion the f16 KV store uses (f32 -> f16 round to
  * nearest even, tinyllm L10.1 section 2.3), applied to n device floats. */
 int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream);
