@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <mutex>
 
 #include "../../include/dec.h"
 #include "common.cuh"
@@ -109,6 +110,40 @@ int attend_launch(const dec_pool* pool, int32_t layer, int32_t n_seqs, const flo
   return DEC_OK;
 }
 
+// ---- scratch that needs no allocation --------------------------------------
+// Some callers cannot allocate device memory when they want attention: code
+// embedded in a host framework that owns every device allocation and hands
+// out only the tensors it manages, plug-ins whose memory budget was fixed
+// when they were loaded, or latency-critical loops that must not pay for the
+// allocator (cudaMalloc and cudaFree can synchronise the device).  For them
+// dec_attend_noalloc keeps its scratch in the library's own device array,
+// which every GPU that loads the library holds until the process exits.
+constexpr size_t kNoAllocBytes = 4u << 20;  // 4 MiB
+constexpr int kNoAllocMaxSeqs = 256;
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];
+
+// The array's device address on the current device, looked up once per
+// device (the host-side name of the array is not a device address).
+int noalloc_scratch(char** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_msg(DEC_ECUDA, cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail_msg(DEC_EINVAL, "device index beyond the scratch table");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return fail_msg(DEC_ECUDA, "cudaGetSymbolAddress of the scratch array failed");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = static_cast<char*>(g_noalloc_ptr[dev]);
+  return DEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -133,6 +168,28 @@ int dec_attend(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float*
   for (int s = 0; s <= n_seqs; ++s) seq_start[s] = s;
   return attend_launch(pool, layer, n_seqs, q, ctx, block_table, max_blocks, out, (char*)scratch, L,
                        seq_start.data(), (cudaStream_t)stream);
+}
+
+int dec_attend_noalloc(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float* q, const int32_t* ctx,
+                       const int32_t* block_table, int32_t max_blocks, void* out, void* stream) {
+  int max_ctx = 0;
+  int rc = attend_check(pool, layer, n_seqs, q, ctx, block_table, max_blocks, out, &max_ctx);
+  if (rc) return rc;
+  if (n_seqs > kNoAllocMaxSeqs) return fail_msg(DEC_ERANGE, "dec_attend_noalloc takes at most 256 sequences");
+  const AttendLayout L = attend_layout(pool->cfg, n_seqs, max_ctx, max_blocks);
+  if (L.total > kNoAllocBytes) {
+    char msg[160];
+    snprintf(msg, sizeof msg, "dec_attend_noalloc needs %zu bytes of scratch, more than its fixed %zu; use dec_attend",
+             L.total, kNoAllocBytes);
+    return fail_msg(DEC_ERANGE, msg);
+  }
+  char* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  thread_local int32_t seq_start[kNoAllocMaxSeqs + 1];
+  for (int s = 0; s <= n_seqs; ++s) seq_start[s] = s;
+  return attend_launch(pool, layer, n_seqs, q, ctx, block_table, max_blocks, out, scratch, L, seq_start,
+                       (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ EXPORTS = (
     "dec_pool_retain", "dec_pool_release", "dec_pool_free_blocks", "dec_pool_refcount", "dec_kv_offset",
     "dec_prefill", "dec_decode", "dec_f32_to_f16", "dec_version", "dec_profile_enable", "dec_profile_read",
     "dec_launch_count", "dec_set_graphs", "dec_set_tensor_cores", "dec_debug_product", "dec_attend_scratch_bytes",
-    "dec_attend",
+    "dec_attend", "dec_attend_noalloc",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax")
 
@@ -98,6 +98,7 @@ def lib() -> C.CDLL:
             "dec_debug_product": (I, [V, C.c_int32, C.c_int32, V, C.c_int32, V, C.c_int32, V]),
             "dec_attend_scratch_bytes": (I, [cfgp, C.c_int32, C.c_int32, C.c_int32, C.POINTER(SZ)]),
             "dec_attend": (I, [V, C.c_int32, C.c_int32, V, _I32P, _I32P, C.c_int32, V, V, SZ, V]),
+            "dec_attend_noalloc": (I, [V, C.c_int32, C.c_int32, V, _I32P, _I32P, C.c_int32, V, V]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -254,6 +254,25 @@ int dec_attend(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float*
                const int32_t* block_table, int32_t max_blocks, void* out, void* scratch, size_t scratch_bytes,
                void* stream);
 
+/* dec_attend without caller scratch (no counterpart on the pages: a service
+ * of this library).  For callers that cannot allocate device memory at the
+ * moment they need attention - code inside a host framework that owns every
+ * device allocation, plug-ins with a memory budget fixed at load time, or
+ * latency-critical loops that must not pay for the allocator, whose calls can
+ * synchronise the device.  Same arguments and results as dec_attend minus the
+ * scratch, which lives in a 4 MiB array inside the library that every GPU
+ * loading the library holds until the process exits.  The call allocates
+ * nothing.  Limits: at most 256 sequences, and the dec_attend_scratch_bytes
+ * of the request must not exceed 4 MiB (e.g. 8 sequences of 2,048 keys at the
+ * Qwen3-0.6B shape); larger requests return DEC_ERANGE with a message.
+ * The first call on a device looks up the array's device address for that
+ * device (make it before any stream capture).  Every call on a device shares
+ * the one array and each call overwrites it (its counters are cleared at the
+ * start of every call), so calls that may overlap on the GPU - on different
+ * streams, or from different threads - race: order them on one stream. */
+int dec_attend_noalloc(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float* q, const int32_t* ctx,
+                       const int32_t* block_table, int32_t max_blocks, void* out, void* stream);
+
 /* Test hook: the device conversion the f16 KV store uses (f32 -> f16 round to
  * nearest even, tinyllm L10.1 section 2.3), applied to n device floats. */
 int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream);
