@@ -119,6 +119,21 @@ def read_profile(m, cls):
     return ms.value, n.value
 
 
+def max_over_ranks(ms, device):
+    """The slowest rank's elapsed time: every rank gets the maximum."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, ms, world):
+    """Units processed by all ranks per second of the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def launches(m):
     n = C.c_int64()
     m.L.dec_launch_count(m.handle, C.byref(n))
@@ -210,11 +225,8 @@ def our_arm(args, rank, world):
     dom_ms, dom_n = read_profile(m, dom)
     profile_classes(m, [dom], False)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = S * args.steps * world
-    value = tokens / (ms / 1e3)
+        ms = max_over_ranks(ms, dev)
+    value = whole_job_rate(S * args.steps, ms, world)
 
     # roofline of the dominant kernel class: algorithmic bytes per launch / event time per launch
     L = shape["n_layers"]
@@ -246,9 +258,11 @@ def our_arm(args, rank, world):
         host_ids = pinned_out.numpy().copy()
         pos = [p + 1 for p in pos]
     e2e_s = time.perf_counter() - t0
+    if world > 1:
+        e2e_s = max_over_ranks(e2e_s * 1e3, dev) / 1e3
     MB = (max_positions + 15) // 16
     h2d = 4 * (3 * S + (S + 1) + S + S + S * MB)
-    e2e = {"value": round(S * e2e_steps * world / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    e2e = {"value": round(whole_job_rate(S * e2e_steps, e2e_s * 1e3, world), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": 4 * S, "steps": e2e_steps}
 
     # ---- batch-1 decode at context 2048 (the longest sequence) ----
