@@ -231,7 +231,14 @@ def our_arm(args, rank, world):
     # roofline of the dominant kernel class: algorithmic bytes per launch / event time per launch
     L = shape["n_layers"]
     per_launch_s = (dom_ms / max(dom_n, 1)) / 1e3
-    if dom_name == "attn":
+    if dom_name == "step":
+        # the whole step in one kernel: every weight byte once, every cached K/V byte once,
+        # the new K/V rows and the logits written
+        alg_bytes = (WEIGHT_BYTES_BF16 + ctx_sum * KV_BYTES_PER_CTX_TOKEN_LAYER * L / args.steps
+                     + S * KV_BYTES_PER_CTX_TOKEN_LAYER * L + S * shape["vocab"] * 4)
+        unit_note = ("per step: 1,192,099,840 B of bf16 weights + 4,096 B of K+V per context token per layer "
+                     "(28 layers) + the new K/V rows + fp32 logits [32, 151936]")
+    elif dom_name == "attn":
         alg_bytes = ctx_sum * KV_BYTES_PER_CTX_TOKEN_LAYER / args.steps  # per launch (one layer)
         unit_note = "4,096 B of K+V per context token per layer; units = sum of the 32 context lengths"
     else:

@@ -117,9 +117,13 @@ PackedLayout packed_layout(const dec_config& c) {
 }
 
 struct WsLayout {
-  size_t X, XN, SSQ, RAW, Q, ATT, ACT, PART, ACNT, META, KEYS, ERR, total;
+  size_t X, XN, SSQ, RAW, Q, ATT, ACT, PART, ACNT, META, KEYS, ERR, SSQP, MSYNC, total;
   size_t meta_ints;
+  size_t msync_bytes;
 };
+
+// 64-key chunks of the longest context (the one-kernel decode step's split).
+int max_chunks64_of(const dec_config& c) { return (c.max_positions + kMegaKeys - 1) / kMegaKeys; }
 
 WsLayout ws_layout(const dec_config& c, int T, int S) {
   WsLayout L{};
@@ -133,7 +137,9 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
   L.Q = take((size_t)T * HD * 4);
   L.ATT = take((size_t)T * HD * a);
   L.ACT = take((size_t)T * c.ff_hidden * a);
-  L.PART = take((size_t)S * c.n_heads * max_chunks_of(c) * (c.head_dim + 2) * 4);
+  const size_t part_recs = std::max((size_t)S * max_chunks_of(c),
+                                     (size_t)std::min(S, kMegaMaxTokens) * max_chunks64_of(c));
+  L.PART = take(part_recs * c.n_heads * (c.head_dim + 2) * 4);
   L.ACNT = take((size_t)S * c.n_kv_heads * 4);
   // ids, tok_pos, tok_seq, row_tok [T]; seq_start [S+1]; seq_ctx [S]; tables [S*MB]; then either the
   // prefill tiles [3*(T+S)] or the decode work list [1 + 2*S*chunks]
@@ -142,6 +148,12 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
   L.META = take(L.meta_ints * 4);
   L.KEYS = take((size_t)T * 8);
   L.ERR = take(64);
+  // one-kernel decode step: per-CTA partial sums of x^2, then one block that
+  // is cleared before every launch (barrier counter | chunk counters | argmax keys)
+  const size_t Tm = (size_t)std::min(T, kMegaMaxTokens);
+  L.SSQP = take(Tm * kMegaMaxGrid * 4);
+  L.msync_bytes = 256 + align256(Tm * c.n_kv_heads * 4) + align256(Tm * 8);
+  L.MSYNC = take(L.msync_bytes);
   L.total = off;
   return L;
 }
@@ -192,6 +204,12 @@ struct dec_model {
   std::vector<CUtensorMap> tm_qkv, tm_o, tm_gu, tm_d;
   CUtensorMap tm_embed, tm_xn, tm_att, tm_act;
   CUtensorMap tm_xn32, tm_att32, tm_act32;  // 32-row boxes for decode products
+  // the one-kernel decode step
+  bool mega_on;
+  bool mega_shape;  // the shape and device allow it
+  unsigned long long* trace;  // per-stage timer stamps of the one-kernel step (or null)
+  size_t trace_n;
+  int smem_optin;
   // captured decode steps
   bool graphs_on;
   cudaStream_t cap_stream;
@@ -417,6 +435,21 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
   cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
   if (m->num_sms <= 0) m->num_sms = 148;
   m->graphs_on = true;
+  m->mega_on = true;
+  m->trace = nullptr;
+  m->trace_n = 0;
+  m->smem_optin = 0;
+  cudaDeviceGetAttribute(&m->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device);
+  {
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
+    const int P = m->num_sms;
+    m->mega_shape = bf && coop && P <= kMegaMaxGrid && c.n_heads == 2 * c.n_kv_heads &&
+                    (D == 32 || D == 64 || D == 128) && c.block_tokens == 16 && d <= kMegaKSlice && d % 16 == 0 &&
+                    (H * D) % 16 == 0 && F % 16 == 0 && (d + P - 1) / P <= 16 &&
+                    mega_slots(kMegaMaxTokens, D, (size_t)m->smem_optin) >= 2 &&
+                    mega_fits(kMegaMaxTokens, D, mega_slots(kMegaMaxTokens, D, (size_t)m->smem_optin));
+  }
   m->tc_on = true;
   m->tc_ready = build_tensor_maps(m);
   m->cap_stream = nullptr;
@@ -496,6 +529,27 @@ int dec_profile_read(dec_model* m, int32_t kernel_class, double* total_ms, int64
 int dec_set_tensor_cores(dec_model* m, int32_t on) {
   if (!m) return fail(DEC_EINVAL, "model is NULL");
   m->tc_on = on != 0;
+  return DEC_OK;
+}
+
+int dec_set_megakernel(dec_model* m, int32_t on) {
+  if (!m) return fail(DEC_EINVAL, "NULL model");
+  m->mega_on = on != 0;
+  return DEC_OK;
+}
+
+int dec_set_step_trace(dec_model* m, uint64_t* stamps, size_t n) {
+  if (!m) return fail(DEC_EINVAL, "NULL model");
+  if (stamps && n < (size_t)m->num_sms * kMegaTraceStride)
+    return fail(DEC_EINVAL, "the trace needs %zu stamps", (size_t)m->num_sms * kMegaTraceStride);
+  m->trace = (unsigned long long*)stamps;
+  m->trace_n = stamps ? n : 0;
+  return DEC_OK;
+}
+
+int dec_megakernel_available(const dec_model* m, int32_t* available) {
+  if (!m || !available) return fail(DEC_EINVAL, "NULL argument");
+  *available = m->mega_shape ? 1 : 0;
   return DEC_OK;
 }
 
@@ -726,6 +780,66 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   return DEC_OK;
 }
 
+// The whole decode step as one persistent kernel (serving mode, <= 32 sequences).
+static int enqueue_mega(dec_model* m, const StepPlan& sp, cudaStream_t st) {
+  const dec_config& c = m->cfg;
+  char* ws = m->ws;
+  const WsLayout& wl = m->wl;
+  const PackedLayout& pl = m->pl;
+  DEC_CUDA(cudaMemsetAsync(ws + wl.MSYNC, 0, wl.msync_bytes, st));
+  const size_t Tm = (size_t)std::min(m->Tmax, kMegaMaxTokens);
+  MegaArgs a{};
+  a.layers = m->packed + pl.layer0;
+  a.layer_stride = pl.layer_stride;
+  a.o_attn_norm = pl.attn_norm;
+  a.o_mlp_norm = pl.mlp_norm;
+  a.o_q_norm = pl.q_norm;
+  a.o_k_norm = pl.k_norm;
+  a.o_wqkv = pl.wqkv;
+  a.o_wo = pl.wo;
+  a.o_wgu = pl.wgu;
+  a.o_wd = pl.wd;
+  a.embed = (const bf16*)(m->packed + pl.embed);
+  a.final_norm = (const float*)(m->packed + pl.final_norm);
+  a.w_attn0 = (const float*)(m->packed + pl.layer0 + pl.attn_norm);
+  a.rope = (const float*)(m->packed + pl.rope);
+  a.kv = (__half*)sp.slabs;
+  a.n_blocks = sp.dm.n_blocks;
+  a.vocab = c.vocab;
+  a.d = c.d_model;
+  a.n_layers = c.n_layers;
+  a.H = c.n_heads;
+  a.Hkv = c.n_kv_heads;
+  a.D = c.head_dim;
+  a.F = c.ff_hidden;
+  a.max_blocks = sp.dm.max_blocks;
+  a.eps = sp.dm.eps;
+  a.scale = 1.0f / std::sqrt((float)c.head_dim);
+  a.T = sp.N;
+  a.ids = sp.meta.ids;
+  a.seq_ctx = sp.meta.seq_ctx;
+  a.tables = sp.meta.tables;
+  a.item_start = sp.meta.work;
+  a.X = (float*)(ws + wl.X);
+  a.XN = (bf16*)(ws + wl.XN);
+  a.RAW = (float*)(ws + wl.RAW);
+  a.ATT = (bf16*)(ws + wl.ATT);
+  a.ACT = (bf16*)(ws + wl.ACT);
+  a.SSQP = (float*)(ws + wl.SSQP);
+  a.PART = (float*)(ws + wl.PART);
+  a.nch_cap = max_chunks64_of(c);
+  a.bar = (unsigned int*)(ws + wl.MSYNC);
+  a.acnt = (int*)(ws + wl.MSYNC + 256);
+  a.keys = (unsigned long long*)(ws + wl.MSYNC + 256 + align256(Tm * c.n_kv_heads * 4));
+  a.logits = sp.logits;
+  a.argmax = sp.argmax;
+  a.err = (uint32_t*)(ws + wl.ERR);
+  a.nslots = mega_slots(sp.N, c.head_dim, (size_t)m->smem_optin);
+  a.trace = m->trace && m->trace_n >= (size_t)m->num_sms * kMegaTraceStride ? m->trace : nullptr;
+  DEC_LAUNCH(DEC_K_STEP, launch_decode_mega(a, m->num_sms, st));
+  return DEC_OK;
+}
+
 static bool profiling_any(const dec_model* m) {
   for (int i = 0; i < DEC_K_COUNT; ++i)
     if (m->prof_on[i]) return true;
@@ -878,7 +992,17 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   for (size_t i = 0; i < work.size(); ++i)
     for (int k = 0; k < 3; ++k) H[o_work + 3 * i + k] = work[i][k];
   o += 3 * work.size();
-  if (decode) {
+  const bool mega = decode && m->mega_on && m->mega_shape && N <= kMegaMaxTokens && !m->dump;
+  if (mega) {
+    // one-kernel step: the first attention item of every sequence (KV heads x 64-key chunks each)
+    int first = 0;
+    for (int s = 0; s < S; ++s) {
+      H[o_work + s] = first;
+      first += c.n_kv_heads * ((b->positions[b->seq_start[s + 1] - 1] + kMegaKeys) / kMegaKeys);
+    }
+    H[o_work + S] = first;
+    o += S + 1;
+  } else if (decode) {
     // decode attention work list: n, then (sequence, 128-key chunk) pairs, chunk-major
     int n = 0, cmax = (max_ctx + kDecodeChunk - 1) / kDecodeChunk;
     for (int cc = 0; cc < cmax; ++cc)
@@ -928,6 +1052,7 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   sp.slabs = pool->slabs;
   sp.logits = logits;
   sp.argmax = argmax;
+  if (mega) return enqueue_mega(m, sp, st);
   if (graph) return launch_decode_graph(m, sp, st);
   return enqueue_step(m, sp, st);
 }

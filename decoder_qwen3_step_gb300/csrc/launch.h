@@ -117,4 +117,60 @@ cudaError_t launch_gemm_tc_skinny(const GemvArgs& a, int epi, const void* tmW, c
 // Query rows of one prefill attention tile (query-head rows / group size).
 int prefill_tile_queries(int G);
 
+// ---- the whole decode step in one persistent kernel (serving mode) -----------
+constexpr int kMegaComputeWarps = 16;                 // + one loader warp
+constexpr int kMegaKSlice = 1024;                     // k elements per weight tile
+constexpr int kMegaRowStride = kMegaKSlice * 2 + 16;  // bytes between staged rows (padded)
+constexpr int kMegaSlotBytes = 16 * kMegaRowStride;   // one ring slot: 16 weight rows
+constexpr int kMegaKeys = 64;                         // cached keys per attention tile
+constexpr int kMegaMaxSlots = 8;
+constexpr int kMegaMaxTokens = 32;                    // sequences per step
+constexpr int kMegaMaxGrid = 256;                     // CTAs (one per SM) the partial sums are sized for
+constexpr int kMegaTraceStride = 320;                 // trace stamps per CTA (the last: the loader's end)
+
+struct MegaArgs {
+  // packed weights: layer 0 at `layers`, then every layer_stride bytes
+  const char* layers;
+  size_t layer_stride;
+  size_t o_attn_norm, o_mlp_norm, o_q_norm, o_k_norm, o_wqkv, o_wo, o_wgu, o_wd;
+  const bf16* embed;        // [vocab, d], also the LM head
+  const float* final_norm;  // [d]
+  const float* w_attn0;     // layer 0's attention RMSNorm gain [d]
+  const float* rope;        // [max_positions, D/2, 2] (cos, sin)
+  __half* kv;               // pool slabs
+  int n_blocks;
+  int vocab, d, n_layers, H, Hkv, D, F, max_blocks;
+  float eps, scale;
+  // the step: T sequences of one new token each
+  int T;
+  const int32_t* ids;         // [T]
+  const int32_t* seq_ctx;     // [T] context length after this token
+  const int32_t* tables;      // [T, max_blocks]
+  const int32_t* item_start;  // [T+1] first attention item of each sequence (Hkv * 64-key chunks each)
+  // workspace
+  float* X;                   // [T, d] residual
+  bf16* XN;                   // [T, d] next product input
+  float* RAW;                 // [T, (H+2Hkv)*D] q|k|v before QK-norm/RoPE
+  bf16* ATT;                  // [T, H*D]
+  bf16* ACT;                  // [T, F]
+  float* SSQP;                // [T, grid] per-CTA partial sums of x^2
+  float* PART;                // [T, H, nch_cap, D+2] chunk records
+  int nch_cap;
+  unsigned int* bar;          // grid barrier counter, zero at launch
+  int* acnt;                  // [T, Hkv] finished chunks, zero at launch
+  unsigned long long* keys;   // [T] argmax keys, zero at launch
+  float* logits;              // [T, vocab] or null
+  int32_t* argmax;            // [T]
+  uint32_t* err;
+  int nslots;
+  unsigned long long* trace;  // null, or [grid, kMegaTraceStride] global-timer stamps
+};
+
+size_t mega_smem_bytes(int T, int nslots, int D);
+int mega_slots(int T, int D, size_t smem_limit);
+int mega_threads();
+// Whether one CTA of the kernel for head size D fits on an SM at T tokens.
+bool mega_fits(int T, int D, int nslots);
+cudaError_t launch_decode_mega(const MegaArgs& a, int grid, cudaStream_t s);
+
 }  // namespace dec

@@ -26,10 +26,11 @@ EXPORTS = (
     "dec_device_status", "dec_set_dump", "dec_pool_bytes", "dec_pool_create", "dec_pool_destroy", "dec_pool_alloc",
     "dec_pool_retain", "dec_pool_release", "dec_pool_free_blocks", "dec_pool_refcount", "dec_kv_offset",
     "dec_prefill", "dec_decode", "dec_f32_to_f16", "dec_version", "dec_profile_enable", "dec_profile_read",
-    "dec_launch_count", "dec_set_graphs", "dec_set_tensor_cores", "dec_debug_product", "dec_attend_scratch_bytes",
-    "dec_attend", "dec_attend_noalloc",
+    "dec_launch_count", "dec_set_graphs", "dec_set_megakernel", "dec_megakernel_available", "dec_set_step_trace",
+    "dec_set_tensor_cores", "dec_debug_product", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc",
 )
-KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax")
+KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax",
+                  "step")
 
 
 class dec_config(C.Structure):
@@ -94,6 +95,9 @@ def lib() -> C.CDLL:
             "dec_profile_read": (I, [V, C.c_int32, C.POINTER(C.c_double), C.POINTER(I64)]),
             "dec_launch_count": (I, [V, C.POINTER(I64)]),
             "dec_set_graphs": (I, [V, C.c_int32]),
+            "dec_set_megakernel": (I, [V, C.c_int32]),
+            "dec_set_step_trace": (I, [V, V, C.c_size_t]),
+            "dec_megakernel_available": (I, [V, C.POINTER(C.c_int32)]),
             "dec_set_tensor_cores": (I, [V, C.c_int32]),
             "dec_debug_product": (I, [V, C.c_int32, C.c_int32, V, C.c_int32, V, C.c_int32, V]),
             "dec_attend_scratch_bytes": (I, [cfgp, C.c_int32, C.c_int32, C.c_int32, C.POINTER(SZ)]),

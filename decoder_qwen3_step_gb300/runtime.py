@@ -183,6 +183,15 @@ class Decoder:
     def set_graphs(self, on: bool) -> None:
         dec.check(self.L.dec_set_graphs(self.handle, 1 if on else 0), "dec_set_graphs")
 
+    def set_megakernel(self, on: bool):
+        """Serving-mode decode of <= 32 sequences as one persistent kernel (default on)."""
+        dec.check(self.L.dec_set_megakernel(self.handle, 1 if on else 0), "dec_set_megakernel")
+
+    def megakernel_available(self) -> bool:
+        v = C.c_int32()
+        dec.check(self.L.dec_megakernel_available(self.handle, C.byref(v)), "dec_megakernel_available")
+        return bool(v.value)
+
     def set_dump(self, buf: torch.Tensor | None):
         if buf is None:
             dec.check(self.L.dec_set_dump(self.handle, None, 0), "dec_set_dump")

@@ -195,7 +195,9 @@ int dec_prefill(dec_model* m, dec_pool* pool, const dec_batch* b, int32_t rows, 
                 int32_t* argmax, void* stream);
 
 /* Decode: exactly one new token per sequence (N == S).  Logits [S, vocab] and
- * ids [S] as for dec_prefill with DEC_ROWS_LAST.  Uses the split-K attention. */
+ * ids [S] as for dec_prefill with DEC_ROWS_LAST.  Uses the split-K attention.
+ * In the serving mode, a step of at most 32 sequences runs as one persistent
+ * kernel (see dec_set_megakernel) when the shape and the device allow it. */
 int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, int32_t* argmax,
                void* stream);
 
@@ -211,7 +213,8 @@ int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, 
 #define DEC_K_DOWN        7 /* down projection + residual */
 #define DEC_K_LMHEAD      8 /* final RMSNorm + LM head + argmax keys */
 #define DEC_K_ARGMAX      9 /* argmax keys -> ids */
-#define DEC_K_COUNT      10
+#define DEC_K_STEP       10 /* a whole decode step in one persistent kernel */
+#define DEC_K_COUNT      11
 /* Record CUDA events around every later launch of one kernel class (on the
  * step's stream) while on != 0. */
 int dec_profile_enable(dec_model* m, int32_t kernel_class, int32_t on);
@@ -227,6 +230,24 @@ int dec_set_tensor_cores(dec_model* m, int32_t on);
  * step launches its kernels one by one.  Graphs are bypassed while a dump or
  * a profiled kernel class is active. */
 int dec_set_graphs(dec_model* m, int32_t on);
+/* Serving-mode decode steps of at most 32 sequences run as one persistent
+ * cooperative kernel, one CTA per SM, with grid-wide barriers between the
+ * dependent stages of every layer (on by default).  Off: the per-operation
+ * kernels above, one launch each.  The per-layer dump and CUDA graphs do
+ * not apply to the one-kernel step.  Same tolerances as the other paths. */
+int dec_set_megakernel(dec_model* m, int32_t on);
+/* Profiling aid for the one-kernel step: while `stamps` is set (DEVICE
+ * memory, uint64 [n], n >= number of SMs x 320), every such step writes, per
+ * CTA b, the global timer (ns) at stamps[b*320 + k]: k = 0 at the start, then
+ * for each of its grid barriers in order (embedding, 5 per layer, LM head)
+ * one stamp when the CTA's share of the stage is done and one when the
+ * barrier releases; stamps[b*320 + 319] is when the CTA's loader warp issued
+ * its last tile.  NULL turns it off.  DEC_EINVAL if n is too small. */
+int dec_set_step_trace(dec_model* m, uint64_t* stamps, size_t n);
+/* *available = 1 when this model's shape and device can run the one-kernel
+ * decode step (serving mode, two query heads per KV head, head_dim 32, 64 or
+ * 128, d_model <= 1024, cooperative launch), else 0. */
+int dec_megakernel_available(const dec_model* m, int32_t* available);
 /* Kernels this model launched since the last call (then reset); a replayed
  * graph counts every kernel it contains. */
 int dec_launch_count(dec_model* m, int64_t* launches);

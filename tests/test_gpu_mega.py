@@ -1,0 +1,139 @@
+"""The serving-mode decode step as one persistent kernel (dec_set_megakernel).
+
+Its logits are checked against the float64 oracle on the bf16-rounded
+weights (the serving tolerance and argmax rule), against the per-operation
+kernels, for batch invariance (a sequence's logits are the same bits alone or
+in a batch: every reduction has one fixed order), on contexts that cross
+16-key blocks and 64-key attention chunks, and at the Qwen3-0.6B shape.  The
+kernel-class counter proves the one-kernel path is the one that ran."""
+
+import ctypes as C
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from decoder_qwen3_step_gb300 import dec, inputs  # noqa: E402
+from .helpers import check, make_pair, np_  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+STEP = dec.KERNEL_CLASSES.index("step")
+
+
+def step_launches(m):
+    ms, n = C.c_double(), C.c_int64()
+    dec.check(m.L.dec_profile_read(m.handle, STEP, C.byref(ms), C.byref(n)), "dec_profile_read")
+    return n.value
+
+
+def decode_run(m, orc, prompts, steps, start_tok=None):
+    """Prefill every prompt, then `steps` greedy decode steps at batch
+    len(prompts), teacher-forced on the oracle's ids; returns the device
+    logits and ids of every step and the oracle's rows."""
+    S = len(prompts)
+    tables = [m.blocks_for(len(p) + steps + 1) for p in prompts]
+    m.prefill([(p, 0, t) for p, t in zip(prompts, tables)], rows=dec.DEC_ROWS_LAST)
+    caches, toks = [], []
+    for p in prompts:
+        c = orc.new_cache(len(p) + steps + 1)
+        ref = orc.forward(c, p, 0, rows="last")
+        caches.append(c)
+        toks.append(int(np.argmax(ref[-1])))
+    got, ids, want = [], [], []
+    for i in range(steps):
+        refs = [orc.forward(caches[s], [toks[s]], len(prompts[s]) + i)[0] for s in range(S)]
+        lg, am = m.decode([([toks[s]], len(prompts[s]) + i, tables[s]) for s in range(S)])
+        got.append(np_(lg))
+        ids.append(np_(am))
+        want.append(np.stack(refs))
+        toks = [int(np.argmax(r)) for r in refs]
+    for t in tables:
+        m.release(t)
+    return got, ids, want
+
+
+@pytest.mark.parametrize("shape", ["tiny", "small"])
+def test_one_kernel_step_matches_the_oracle_and_the_layered_kernels(shape):
+    m, orc, w = make_pair(shape, "bf16", max_positions=256, max_tokens=512, max_seqs=8)
+    if not m.megakernel_available():
+        pytest.skip("the one-kernel step is not available for this shape on this device")
+    V = inputs.SHAPES[shape]["vocab"]
+    # contexts that end inside, and just past, 16-key blocks and 64-key chunks
+    lens = [13, 63, 64, 100] if shape == "tiny" else [60, 64, 128, 129]
+    prompts = [inputs.make_ids(V, n, seed=40 + s) for s, n in enumerate(lens)]
+    m.L.dec_profile_enable(m.handle, STEP, 1)
+    step_launches(m)
+    got, ids, want = decode_run(m, orc, prompts, steps=6)
+    assert step_launches(m) == 6  # every decode step was one launch of the persistent kernel
+    m.L.dec_profile_enable(m.handle, STEP, 0)
+    for i in range(6):
+        check(got[i], ids[i], want[i], "bf16", f"{shape} one-kernel decode step {i}")
+    # the same steps on the per-operation kernels
+    m.set_megakernel(False)
+    got2, ids2, want2 = decode_run(m, orc, prompts, steps=6)
+    for i in range(6):
+        check(got2[i], ids2[i], want2[i], "bf16", f"{shape} layered decode step {i}")
+        assert np.abs(got[i] - got2[i]).max() < 5e-2
+    assert m.device_status() == 0
+    m.close()
+
+
+def test_one_kernel_step_is_batch_invariant():
+    m, orc, w = make_pair("small", "bf16", max_positions=256, max_tokens=512, max_seqs=8)
+    if not m.megakernel_available():
+        pytest.skip("the one-kernel step is not available on this device")
+    prompts = [inputs.make_ids(8192, n, seed=70 + s) for s, n in enumerate([90, 33, 150])]
+    tables = [m.blocks_for(200) for _ in prompts]
+    alone = [m.blocks_for(200) for _ in prompts]
+    for p, t, u in zip(prompts, tables, alone):  # identical caches for both copies
+        m.prefill([(p, 0, t)], rows=dec.DEC_ROWS_LAST)
+        m.prefill([(p, 0, u)], rows=dec.DEC_ROWS_LAST)
+    tok = [5, 77, 4000]
+    for i in range(3):
+        lg_b, _ = m.decode([([tok[s]], len(prompts[s]) + i, tables[s]) for s in range(3)])
+        lg_b = np_(lg_b)
+        for s in range(3):
+            lg_1, _ = m.decode([([tok[s]], len(prompts[s]) + i, alone[s])])
+            assert np.array_equal(np_(lg_1)[0].view(np.uint32), lg_b[s].view(np.uint32)), (i, s)
+    assert m.device_status() == 0
+    m.close()
+
+
+def test_one_kernel_step_reads_ids_from_the_device():
+    """The ids of a step may come from the previous step's argmax buffer."""
+    m, orc, w = make_pair("tiny", "bf16", max_positions=128, max_tokens=128, max_seqs=4)
+    if not m.megakernel_available():
+        pytest.skip("the one-kernel step is not available on this device")
+    prompts = [inputs.make_ids(512, n, seed=90 + s) for s, n in enumerate([20, 47])]
+    tables = [m.blocks_for(80) for _ in prompts]
+    host = [m.blocks_for(80) for _ in prompts]
+    _, am = m.prefill([(p, 0, t) for p, t in zip(prompts, tables)], rows=dec.DEC_ROWS_LAST)
+    _, am_h = m.prefill([(p, 0, t) for p, t in zip(prompts, host)], rows=dec.DEC_ROWS_LAST)
+    ids_dev = am.to(torch.int32).clone()
+    ids_host = np_(am_h).astype(np.int64)
+    logits = torch.empty((2, 512), dtype=torch.float32, device=m.device)
+    out_ids = torch.empty((2,), dtype=torch.int32, device=m.device)
+    for i in range(5):
+        pos = [len(p) + i for p in prompts]
+        m.decode([([0], pos[s], tables[s]) for s in range(2)], device_ids=ids_dev, out=(logits, out_ids))
+        lg_h, am_h = m.decode([([int(ids_host[s])], pos[s], host[s]) for s in range(2)])
+        assert np.array_equal(np_(logits).view(np.uint32), np_(lg_h).view(np.uint32))
+        assert np.array_equal(np_(out_ids), np_(am_h))
+        ids_dev.copy_(out_ids)
+        ids_host = np_(am_h).astype(np.int64)
+    assert m.device_status() == 0
+    m.close()
+
+
+def test_one_kernel_step_at_the_qwen3_shape():
+    m, orc, w = make_pair("qwen3_0p6b", "bf16", max_positions=512, max_tokens=512, max_seqs=4, n_blocks=160)
+    if not m.megakernel_available():
+        pytest.skip("the one-kernel step is not available on this device")
+    prompts = [inputs.make_ids(151936, n, seed=120 + s) for s, n in enumerate([61, 190])]
+    got, ids, want = decode_run(m, orc, prompts, steps=4)
+    for i in range(4):
+        check(got[i], ids[i], want[i], "bf16", f"0.6B one-kernel decode step {i}")
+    assert m.device_status() == 0
+    m.close()
