@@ -744,6 +744,8 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
                 (int*)(ws + wl.ACNT), ERR};
     if (sp.decode) {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, sp.slots, bf, st));
+    } else if (bf && m->tc_on && attn_prefill_tc_eligible(aa)) {
+      DEC_LAUNCH(DEC_K_ATTN, launch_attn_prefill_tc(aa, sp.n_work, st));
     } else {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_prefill(aa, sp.n_work, bf, st));
     }

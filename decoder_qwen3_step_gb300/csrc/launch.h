@@ -117,6 +117,11 @@ cudaError_t launch_gemm_tc_skinny(const GemvArgs& a, int epi, const void* tmW, c
 // Query rows of one prefill attention tile (query-head rows / group size).
 int prefill_tile_queries(int G);
 
+// Serving-mode prefill attention on the warp-level tensor cores (f16 K/V,
+// f16 queries and probabilities, fp32 accumulation); same work tiles.
+bool attn_prefill_tc_eligible(const AttnArgs& a);
+cudaError_t launch_attn_prefill_tc(const AttnArgs& a, int n_work, cudaStream_t s);
+
 // ---- the whole decode step in one persistent kernel (serving mode) -----------
 constexpr int kMegaComputeWarps = 16;                 // + one loader warp
 constexpr int kMegaKSlice = 1024;                     // k elements per weight tile
