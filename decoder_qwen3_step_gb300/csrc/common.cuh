@@ -127,17 +127,30 @@ __device__ __forceinline__ float row_rstd(const float* ssq, int t, int d, float 
   return 1.0f / sqrtf(s / (float)d + eps);
 }
 
-// row_rstd for up to U consecutive token rows t0 .. t0+n-1 at once (their
-// partial loads overlap); the same summation order as row_rstd.  Whole warp.
+// row_rstd for up to U consecutive token rows t0 .. t0+n-1 at once: every
+// partial a lane adds is loaded before the first add (one round trip for
+// d <= 2048), and each lane adds its partials in the same lane-strided order
+// as row_rstd, so the result is the same.  Whole warp.
 template <int U>
 __device__ __forceinline__ void row_rstd_n(const float* ssq, int t0, int n, int d, float eps, float* out) {
+  constexpr int kK = 4;  // partials per lane per pass
   const int nch = d / kSsqChunk, lane = threadIdx.x & 31;
   float s[U];
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    s[u] = 0.f;
-    if (u < n)
-      for (int c = lane; c < nch; c += 32) s[u] += ssq[(size_t)(t0 + u) * nch + c];
+  for (int u = 0; u < U; ++u) s[u] = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += 32 * kK) {
+    float v[U][kK];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < kK; ++k) {
+        const int c = c0 + lane + 32 * k;
+        v[u][k] = (u < n && c < nch) ? ssq[(size_t)(t0 + u) * nch + c] : 0.f;
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < kK; ++k) s[u] += v[u][k];
   }
 #pragma unroll
   for (int u = 0; u < U; ++u) out[u] = 1.0f / sqrtf(warp_sum(s[u]) / (float)d + eps);
@@ -150,7 +163,9 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int id) {
   return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the fast exponential and division (relative
+// error about 1e-7); below -80 the value is below 1e-33 and is returned as 0.
+__device__ __forceinline__ float silu(float z) { return z < -80.0f ? 0.0f : __fdividef(z, 1.0f + __expf(-z)); }
 
 // Element offset of (layer, block, is_v, kv head, slot) in the KV slab buffer.
 __host__ __device__ __forceinline__ int64_t kv_offset(int layer, int block, int is_v, int kv_head, int slot,

@@ -44,11 +44,15 @@ template <typename AT, int EPI, int NT>
 __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, int ld, int r0, int nrows, int t0,
                                          int ntok, const float* rstd_s, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
-  const int nq = nrows / 4;  // 4-row groups per token row
-  const int total = ntok * nq;
+  // 4-row groups per token row, padded to a power of two so a flat index
+  // splits with a shift and a mask (groups past nrows are skipped)
+  const int nq = nrows / 4;
+  const int nq_sh = nq > 1 ? 32 - __clz(nq - 1) : 0;
+  const int total = ntok << nq_sh;
   if (EPI == EPI_QKV_RAW) {
     for (int i = tid; i < total; i += NT) {
-      const int t = i / nq, r = (i - t * nq) * 4;
+      const int t = i >> nq_sh, r = (i & ((1 << nq_sh) - 1)) * 4;
+      if (r >= nrows) continue;
       const float rs = rstd_s[t];
       const float4 y = rows4(tile, ld, r, t);
       store4(a.out_f32 + (size_t)(t0 + t) * a.rows + r0 + r, y.x * rs, y.y * rs, y.z * rs, y.w * rs);
@@ -64,8 +68,8 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
       for (int u = 0; u < U; ++u) {
         const int i = base + u * NT + lane;
         xr[u] = wr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < total) {
-          const int t = i / nq, r = (i - t * nq) * 4;
+        const int t = i >> nq_sh, r = (i & ((1 << nq_sh) - 1)) * 4;
+        if (i < total && r < nrows) {
           xr[u] = *reinterpret_cast<const float4*>(a.X_res + (size_t)(t0 + t) * a.d + r0 + r);
           wr[u] = *reinterpret_cast<const float4*>(a.w_next + r0 + r);
         }
@@ -73,8 +77,8 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = base + u * NT + lane;
-        const bool valid = i < total;
-        const int t = i / nq, r = (i - t * nq) * 4;
+        const int t = i >> nq_sh, r = (i & ((1 << nq_sh) - 1)) * 4;
+        const bool valid = i < total && r < nrows;
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
         if (valid) {
           const float4 y = rows4(tile, ld, r, t);
@@ -95,8 +99,10 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
   } else if (EPI == EPI_SWIGLU) {
     AT* out = reinterpret_cast<AT*>(a.act_out);
     const int ng = nrows / 8;  // groups of 4 outputs per token row (gate/up interleave in 8s)
-    for (int i = tid; i < ntok * ng; i += NT) {
-      const int t = i / ng, q = i - t * ng;
+    const int ng_sh = nq_sh - 1;  // padded like nq
+    for (int i = tid; i < (ntok << ng_sh); i += NT) {
+      const int t = i >> ng_sh, q = i & ((1 << ng_sh) - 1);
+      if (q >= ng) continue;
       const int grp = q >> 1, jj = (q & 1) * 4;
       const float rs = rstd_s[t];
       const int rg = grp * 2 * kGuGroup + jj, ru = rg + kGuGroup;
@@ -110,8 +116,8 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
   } else {  // EPI_LOGITS
     for (int base = warp * 32; base < total; base += NT) {
       const int i = base + lane;
-      const bool valid = i < total;
-      const int t = i / nq, r = (i - t * nq) * 4;
+      const int t = i >> nq_sh, r = (i & ((1 << nq_sh) - 1)) * 4;
+      const bool valid = i < total && r < nrows;
       unsigned long long key = 0ull;
       if (valid) {
         const float rs = rstd_s[t];
@@ -219,34 +225,52 @@ __device__ __forceinline__ void epilogue_qkv_tile(const GemvArgs& a, const float
     tblk[t] = qkv_block(f, t0 + t, pos);
   }
   sync();
-  const int half = D / 2, nq = nrows / 4;
-  for (int i = tid; i < ntok * nq; i += NT) {
-    const int t = i / nq, r = (i - t * nq) * 4;  // rows r .. r+3 of one head (D is a multiple of 4)
-    const int hh = r / D, j = r - hh * D;
-    const int gh = (r0 + hh * D) / D;
-    const float rs = rstd_s[t];
-    const float4 y4 = rows4(tile, ld, r, t);
-    float out[4] = {y4.x * rs, y4.y * rs, y4.z * rs, y4.w * rs};
-    if (gh < f.H + f.Hkv) {
-      const float* g = gh < f.H ? f.q_norm : f.k_norm;
-      const int jj = j < half ? j : j - half, jp = j < half ? j + half : j - half;
-      const int rp = j < half ? r + half : r - half;
-      const float4 g0 = *reinterpret_cast<const float4*>(g + j);
-      const float4 g1 = *reinterpret_cast<const float4*>(g + jp);
-      const float4 cs0 = *reinterpret_cast<const float4*>(f.rope + ((size_t)tpos[t] * half + jj) * 2);
-      const float4 cs1 = *reinterpret_cast<const float4*>(f.rope + ((size_t)tpos[t] * half + jj) * 2 + 4);
-      const float rn_ = rn[hh * ntok + t];
-      const float ga[4] = {g0.x, g0.y, g0.z, g0.w}, gb[4] = {g1.x, g1.y, g1.z, g1.w};
-      const float c4[4] = {cs0.x, cs0.z, cs1.x, cs1.z}, s4[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
-      const float4 p4 = rows4(tile, ld, rp, t);
-      const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+  const int half = D / 2, nq = nrows / 4;  // D: a power of two; nrows: whole heads
+  const int nq_sh = nq > 1 ? 32 - __clz(nq - 1) : 0, dsh = 31 - __clz(D);
+  constexpr int U = 4;  // row groups per thread per pass: their loads in flight together
+  for (int base = tid; base < (ntok << nq_sh); base += NT * U) {
+    float4 g0[U], g1[U], cs0[U], cs1[U];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float a_ = out[e] * rn_ * ga[e], b_ = pv[e] * rs * rn_ * gb[e];
-        out[e] = j < half ? a_ * c4[e] - b_ * s4[e] : a_ * c4[e] + b_ * s4[e];
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NT;
+      const int t = i >> nq_sh, r = (i & ((1 << nq_sh) - 1)) * 4;
+      if (i >= (ntok << nq_sh) || r >= nrows) continue;
+      const int hh = r >> dsh, j = r & (D - 1);
+      const int gh = (r0 >> dsh) + hh;
+      if (gh < f.H + f.Hkv) {
+        const float* g = gh < f.H ? f.q_norm : f.k_norm;
+        const int jj = j < half ? j : j - half, jp = j < half ? j + half : j - half;
+        g0[u] = __ldg(reinterpret_cast<const float4*>(g + j));
+        g1[u] = __ldg(reinterpret_cast<const float4*>(g + jp));
+        cs0[u] = __ldg(reinterpret_cast<const float4*>(f.rope + ((size_t)tpos[t] * half + jj) * 2));
+        cs1[u] = __ldg(reinterpret_cast<const float4*>(f.rope + ((size_t)tpos[t] * half + jj) * 2 + 4));
       }
     }
-    qkv_store4<KT>(f, t0 + t, gh, j, out, tpos[t], tblk[t]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NT;
+      const int t = i >> nq_sh, r = (i & ((1 << nq_sh) - 1)) * 4;  // rows r .. r+3 of one head (D is a multiple of 4)
+      if (i >= (ntok << nq_sh) || r >= nrows) continue;
+      const int hh = r >> dsh, j = r & (D - 1);
+      const int gh = (r0 >> dsh) + hh;
+      const float rs = rstd_s[t];
+      const float4 y4 = rows4(tile, ld, r, t);
+      float out[4] = {y4.x * rs, y4.y * rs, y4.z * rs, y4.w * rs};
+      if (gh < f.H + f.Hkv) {
+        const int rp = j < half ? r + half : r - half;
+        const float rn_ = rn[hh * ntok + t];
+        const float ga[4] = {g0[u].x, g0[u].y, g0[u].z, g0[u].w}, gb[4] = {g1[u].x, g1[u].y, g1[u].z, g1[u].w};
+        const float c4[4] = {cs0[u].x, cs0[u].z, cs1[u].x, cs1[u].z}, s4[4] = {cs0[u].y, cs0[u].w, cs1[u].y, cs1[u].w};
+        const float4 p4 = rows4(tile, ld, rp, t);
+        const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a_ = out[e] * rn_ * ga[e], b_ = pv[e] * rs * rn_ * gb[e];
+          out[e] = j < half ? a_ * c4[e] - b_ * s4[e] : a_ * c4[e] + b_ * s4[e];
+        }
+      }
+      qkv_store4<KT>(f, t0 + t, gh, j, out, tpos[t], tblk[t]);
+    }
   }
 }
 
