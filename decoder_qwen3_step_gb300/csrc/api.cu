@@ -994,7 +994,7 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   for (size_t i = 0; i < work.size(); ++i)
     for (int k = 0; k < 3; ++k) H[o_work + 3 * i + k] = work[i][k];
   o += 3 * work.size();
-  const bool mega = decode && m->mega_on && m->mega_shape && N <= kMegaMaxTokens && !m->dump;
+  const bool mega = decode && m->mega_on && m->mega_shape && N <= kMegaAutoTokens && !m->dump;
   if (mega) {
     // one-kernel step: the first attention item of every sequence (KV heads x 64-key chunks each)
     int first = 0;
@@ -1005,7 +1005,7 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
     H[o_work + S] = first;
     o += S + 1;
   } else if (decode) {
-    // decode attention work list: n, then (sequence, 128-key chunk) pairs, chunk-major
+    // decode attention work list: n, then (sequence, 64-key chunk) pairs, chunk-major
     int n = 0, cmax = (max_ctx + kDecodeChunk - 1) / kDecodeChunk;
     for (int cc = 0; cc < cmax; ++cc)
       for (int s = 0; s < S; ++s)
@@ -1046,10 +1046,8 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   sp.decode = decode;
   sp.rows_all = rows_mode == DEC_ROWS_ALL;
   sp.n_work = (int)work.size();
-  // decode attention grid: one CTA per 128-key chunk of the longest sequence, rounded
-  // up to a multiple of 4 chunks so a captured graph serves 512 positions of growth
-  // decode attention grid: one CTA per 128-key chunk of the longest sequence, rounded
-  // up to a multiple of 4 chunks so a captured graph serves 512 positions of growth
+  // decode attention grid: one CTA per 64-key chunk of the longest sequence, rounded
+  // up to a multiple of 4 chunks so a captured graph serves 256 positions of growth
   sp.slots = std::min(m->NCH, ((max_ctx + kDecodeChunk - 1) / kDecodeChunk + 3) / 4 * 4);
   sp.slabs = pool->slabs;
   sp.logits = logits;

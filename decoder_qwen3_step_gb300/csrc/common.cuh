@@ -21,7 +21,7 @@ namespace dec {
 
 constexpr int kSsqChunk = 16;    // features per sum-of-squares partial
 constexpr int kGuGroup = 8;      // gate/up rows interleave in groups of 8
-constexpr int kDecodeChunk = 128; // keys per split-K work item of decode attention (8 blocks of 16)
+constexpr int kDecodeChunk = 64;  // keys per split-K work item of decode attention (4 blocks of 16)
 
 // Device error word bits (mirrors DEC_DEV_* in include/dec.h).
 constexpr uint32_t kErrBadId = 1u;

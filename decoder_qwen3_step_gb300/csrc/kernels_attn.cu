@@ -66,7 +66,7 @@ struct Raw {
 
 // ---------------------------------------------------------------------------
 // Decode attention, split-K.  grid (chunk, kv head, sequence), 4 warps.  Keys
-// are cut into fixed 128-key chunks (8 blocks of 16; the cut depends only on
+// are cut into fixed 64-key chunks (4 blocks of 16; the cut depends only on
 // the position, never on the batch), one chunk per CTA.  One thread issues
 // bulk asynchronous copies of the chunk's K and V slabs (4 KB each per block
 // and KV head at the serving shape) into shared memory on one mbarrier, so a
@@ -80,7 +80,7 @@ struct Raw {
 // records in chunk order, writes the attention output and re-arms the counter.
 // ---------------------------------------------------------------------------
 constexpr int kDecWarps = 4;
-constexpr int kDecBlocks = kDecodeChunk / 16;  // 8
+constexpr int kDecBlocks = kDecodeChunk / 16;  // 4
 constexpr int kMaxChunks = (kMaxPositions + kDecodeChunk - 1) / kDecodeChunk;
 
 template <typename KT, int D>
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) k_attn_decode(AttnArgs a) {
   const int nch = (ctx + kDecodeChunk - 1) / kDecodeChunk;
   if (c >= nch) return;
   extern __shared__ __align__(128) uint8_t dsm[];
-  KT* Ks = reinterpret_cast<KT*>(dsm);        // [8 blocks][16 keys][D]
-  KT* Vs = Ks + kDecBlocks * 16 * D;          // [8 blocks][16 keys][D]
+  KT* Ks = reinterpret_cast<KT*>(dsm);        // [4 blocks][16 keys][D]
+  KT* Vs = Ks + kDecBlocks * 16 * D;          // [4 blocks][16 keys][D]
   __shared__ float qs[G][D];
   __shared__ float ms[kDecWarps][G], ls[kDecWarps][G];
   __shared__ float os[kDecWarps][G][D];

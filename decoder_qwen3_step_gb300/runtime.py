@@ -184,7 +184,7 @@ class Decoder:
         dec.check(self.L.dec_set_graphs(self.handle, 1 if on else 0), "dec_set_graphs")
 
     def set_megakernel(self, on: bool):
-        """Serving-mode decode of <= 32 sequences as one persistent kernel (default on)."""
+        """Serving-mode decode of <= 8 sequences as one persistent kernel (default on)."""
         dec.check(self.L.dec_set_megakernel(self.handle, 1 if on else 0), "dec_set_megakernel")
 
     def megakernel_available(self) -> bool:

@@ -196,7 +196,7 @@ int dec_prefill(dec_model* m, dec_pool* pool, const dec_batch* b, int32_t rows, 
 
 /* Decode: exactly one new token per sequence (N == S).  Logits [S, vocab] and
  * ids [S] as for dec_prefill with DEC_ROWS_LAST.  Uses the split-K attention.
- * In the serving mode, a step of at most 32 sequences runs as one persistent
+ * In the serving mode, a step of at most 8 sequences runs as one persistent
  * kernel (see dec_set_megakernel) when the shape and the device allow it. */
 int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, int32_t* argmax,
                void* stream);
@@ -230,7 +230,7 @@ int dec_set_tensor_cores(dec_model* m, int32_t on);
  * step launches its kernels one by one.  Graphs are bypassed while a dump or
  * a profiled kernel class is active. */
 int dec_set_graphs(dec_model* m, int32_t on);
-/* Serving-mode decode steps of at most 32 sequences run as one persistent
+/* Serving-mode decode steps of at most 8 sequences run as one persistent
  * cooperative kernel, one CTA per SM, with grid-wide barriers between the
  * dependent stages of every layer (on by default).  Off: the per-operation
  * kernels above, one launch each.  The per-layer dump and CUDA graphs do

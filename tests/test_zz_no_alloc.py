@@ -62,7 +62,7 @@ def test_noalloc_attention_matches_dec_attend_twice(mode):
         assert np.abs(g - w).max() <= tol * max(1.0, np.abs(w).max())
         for t in tables:
             m.release(t)
-    # beyond the fixed scratch (256 sequences x 1,024 keys: 4.4 MB): refused with a message,
+    # beyond the fixed scratch (256 sequences x 1,024 keys: 8.7 MB): refused with a message,
     # nothing launched; the sequences share one allocated table
     big = [1024] * 256
     shared = m.blocks_for(1024)
