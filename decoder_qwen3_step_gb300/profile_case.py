@@ -28,6 +28,8 @@ def main(argv=None):
     ap.add_argument("--ctx", type=int, default=2048)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--graphs", type=int, default=1)
+    ap.add_argument("--range", action="store_true",
+                    help="open a profiler range around the measured loop only (ncu --profile-from-start off)")
     args = ap.parse_args(argv)
     shape = inputs.SHAPES["qwen3_0p6b"]
     S, L = args.batch, args.ctx
@@ -45,16 +47,24 @@ def main(argv=None):
             m.prefill([(ids[s], 0, tables[s]) for s in range(g, min(S, g + per))], rows=dec.DEC_ROWS_LAST)
         logits = torch.empty((S, V), dtype=torch.float32, device=m.device)
         buf = [torch.zeros((S,), dtype=torch.int32, device=m.device) for _ in range(2)]
+        torch.cuda.synchronize()
+        if args.range:
+            torch.cuda.cudart().cudaProfilerStart()
         for i in range(args.steps):
             m.decode([([0], L + i, tables[s]) for s in range(S)], device_ids=buf[i & 1], out=(logits, buf[(i + 1) & 1]))
     else:
         logits = torch.empty((S, V), dtype=torch.float32, device=m.device)
         am = torch.empty((S,), dtype=torch.int32, device=m.device)
+        torch.cuda.synchronize()
+        if args.range:
+            torch.cuda.cudart().cudaProfilerStart()
         for _ in range(args.steps):
             for k in range(0, L, 512):
                 m.prefill([(ids[s][k:k + 512], k, tables[s]) for s in range(S)], rows=dec.DEC_ROWS_LAST,
                           out=(logits, am))
     torch.cuda.synchronize()
+    if args.range:
+        torch.cuda.cudart().cudaProfilerStop()
     status = m.device_status()
     m.close()
     if status:
