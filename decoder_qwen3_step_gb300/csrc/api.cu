@@ -596,6 +596,10 @@ int dec_pool_create(const dec_config* cfg, int32_t n_blocks, void* slabs, size_t
   p->n_blocks = n_blocks;
   p->slabs = slabs;
   p->refs.assign(n_blocks, 0);
+  p->fill.assign(n_blocks, 0);
+  p->registered.assign(n_blocks, 0);
+  p->key.assign(n_blocks, 0);
+  p->lru_pos.assign(n_blocks, p->lru.end());
   p->free_list.resize(n_blocks);
   for (int i = 0; i < n_blocks; ++i) p->free_list[i] = n_blocks - 1 - i;
   *out = p;
@@ -607,12 +611,23 @@ void dec_pool_destroy(dec_pool* p) { delete p; }
 int dec_pool_alloc(dec_pool* p, int32_t n, int32_t* ids) {
   if (!p || (!ids && n > 0)) return fail(DEC_EINVAL, "NULL argument");
   if (n < 0) return fail(DEC_EINVAL, "negative block count");
-  if ((size_t)n > p->free_list.size())
-    return fail(DEC_ECAPACITY, "pool exhausted: %d blocks asked, %zu free", n, p->free_list.size());
+  if ((size_t)n > p->free_list.size() + p->lru.size())
+    return fail(DEC_ECAPACITY, "pool exhausted: %d blocks asked, %zu free, %zu cached", n, p->free_list.size(),
+                p->lru.size());
+  // free blocks first, then the cached prefix blocks released longest ago
+  while (p->free_list.size() < (size_t)n) {
+    const int32_t id = p->lru.front();
+    p->lru.pop_front();
+    p->lru_pos[id] = p->lru.end();
+    p->index.erase(p->key[id]);
+    p->registered[id] = 0;
+    p->free_list.insert(p->free_list.begin(), id);
+  }
   for (int i = 0; i < n; ++i) {
     ids[i] = p->free_list.back();
     p->free_list.pop_back();
     p->refs[ids[i]] = 1;
+    p->fill[ids[i]] = 0;
   }
   return DEC_OK;
 }
@@ -627,7 +642,14 @@ int dec_pool_retain(dec_pool* p, int32_t id) {
 int dec_pool_release(dec_pool* p, int32_t id) {
   if (!p) return fail(DEC_EINVAL, "pool is NULL");
   if (id < 0 || id >= p->n_blocks || p->refs[id] <= 0) return fail(DEC_EBLOCK, "block %d is not allocated", id);
-  if (--p->refs[id] == 0) p->free_list.push_back(id);
+  if (--p->refs[id] == 0) {
+    if (p->registered[id]) {  // keep its keys: a later lookup of the same prefix reacquires it
+      p->lru.push_back(id);
+      p->lru_pos[id] = std::prev(p->lru.end());
+    } else {
+      p->free_list.push_back(id);
+    }
+  }
   return DEC_OK;
 }
 

@@ -28,6 +28,7 @@ EXPORTS = (
     "dec_prefill", "dec_decode", "dec_f32_to_f16", "dec_version", "dec_profile_enable", "dec_profile_read",
     "dec_launch_count", "dec_set_graphs", "dec_set_megakernel", "dec_megakernel_available", "dec_set_step_trace",
     "dec_set_tensor_cores", "dec_debug_product", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc",
+    "dec_prefix_key", "dec_pool_set_fill", "dec_pool_register", "dec_pool_lookup", "dec_pool_cached_blocks",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax",
                   "step")
@@ -87,6 +88,11 @@ def lib() -> C.CDLL:
             "dec_pool_release": (I, [V, C.c_int32]),
             "dec_pool_free_blocks": (I, [V, _I32P]),
             "dec_pool_refcount": (I, [V, C.c_int32, _I32P]),
+            "dec_pool_set_fill": (I, [V, C.c_int32, C.c_int32]),
+            "dec_pool_register": (I, [V, C.c_int32, C.c_uint64, _I32P]),
+            "dec_pool_lookup": (I, [V, C.c_uint64, _I32P]),
+            "dec_pool_cached_blocks": (I, [V, _I32P]),
+            "dec_prefix_key": (C.c_uint64, [C.c_uint64, _I32P, C.c_int32]),
             "dec_kv_offset": (I, [V, _I32P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(I64)]),
             "dec_prefill": (I, [V, V, C.POINTER(dec_batch), C.c_int32, V, V, V]),
             "dec_decode": (I, [V, V, C.POINTER(dec_batch), V, V, V]),

@@ -144,6 +144,44 @@ class Decoder:
     def blocks_for(self, n_positions: int) -> list:
         return self.alloc((n_positions + BLOCK_TOKENS - 1) // BLOCK_TOKENS)
 
+    # -- prefix cache ---------------------------------------------------------
+    def prefix_keys(self, tokens) -> list:
+        """Chained keys (dec_prefix_key) of the full blocks of a token sequence."""
+        keys, prev = [], 0
+        for i in range(len(tokens) // BLOCK_TOKENS):
+            blk = (C.c_int32 * BLOCK_TOKENS)(*[int(t) for t in tokens[i * BLOCK_TOKENS:(i + 1) * BLOCK_TOKENS]])
+            prev = self.L.dec_prefix_key(prev, blk, BLOCK_TOKENS)
+            keys.append(prev)
+        return keys
+
+    def register_prefix(self, table, tokens) -> int:
+        """Index the full blocks of a sequence whose K/V are written (positions
+        0 .. len(tokens)-1 in `table`); returns how many blocks now carry their key."""
+        n = 0
+        for k, b in zip(self.prefix_keys(tokens), table):
+            dec.check(self.L.dec_pool_set_fill(self.pool, int(b), BLOCK_TOKENS), "dec_pool_set_fill")
+            ok = C.c_int32()
+            dec.check(self.L.dec_pool_register(self.pool, int(b), k, C.byref(ok)), "dec_pool_register")
+            n += ok.value
+        return n
+
+    def lookup_prefix(self, tokens) -> list:
+        """Reacquire the cached blocks of the longest indexed prefix of tokens
+        (whole blocks, stopping at the first miss); the caller releases them."""
+        ids = []
+        for k in self.prefix_keys(tokens):
+            i = C.c_int32()
+            dec.check(self.L.dec_pool_lookup(self.pool, k, C.byref(i)), "dec_pool_lookup")
+            if i.value < 0:
+                break
+            ids.append(i.value)
+        return ids
+
+    def cached_blocks(self) -> int:
+        n = C.c_int32()
+        dec.check(self.L.dec_pool_cached_blocks(self.pool, C.byref(n)), "dec_pool_cached_blocks")
+        return n.value
+
     # -- steps ----------------------------------------------------------------
     def prefill(self, seqs, rows: int = dec.DEC_ROWS_ALL, logits: bool = True, device_ids=None,
                 out=None):

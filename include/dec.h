@@ -173,12 +173,39 @@ int dec_pool_bytes(const dec_config* cfg, int32_t n_blocks, size_t* bytes);
  * slab memory is caller-owned device memory of >= dec_pool_bytes. */
 int dec_pool_create(const dec_config* cfg, int32_t n_blocks, void* slabs, size_t bytes, dec_pool** out);
 void dec_pool_destroy(dec_pool* p);
-/* All-or-nothing: n blocks with refcount 1 into ids[0..n), or DEC_ECAPACITY and nothing taken. */
+/* All-or-nothing: n blocks with refcount 1 and fill 0 into ids[0..n), or
+ * DEC_ECAPACITY and nothing taken.  Free blocks go first; when they run short,
+ * cached prefix blocks are evicted (their keys dropped), oldest release first
+ * (kv_pool_evicts_the_oldest_cached_block). */
 int dec_pool_alloc(dec_pool* p, int32_t n, int32_t* ids);
 int dec_pool_retain(dec_pool* p, int32_t id);  /* refcount + 1; DEC_EBLOCK if not allocated */
-int dec_pool_release(dec_pool* p, int32_t id); /* refcount - 1; at 0 the block is free again */
-int dec_pool_free_blocks(const dec_pool* p, int32_t* n);
+/* refcount - 1; at 0 a registered block is cached (its K/V and key kept, in
+ * release order) and any other block is free again.  DEC_EBLOCK if not allocated. */
+int dec_pool_release(dec_pool* p, int32_t id);
+int dec_pool_free_blocks(const dec_pool* p, int32_t* n);   /* free, not counting cached blocks */
 int dec_pool_refcount(const dec_pool* p, int32_t id, int32_t* refs);
+
+/* ---- prefix cache in the pool (KvPool's hash index and LRU, tinyllm L10.1
+ * sections 1 and 4; its boundary tests kv_pool_bounds_and_cache_lifecycle) ---
+ * The pages name no hash: a block's key is the caller's.  dec_prefix_key gives
+ * a chained one: key_i = dec_prefix_key(key_{i-1}, tokens of block i,
+ * block_tokens), key_{-1} = 0, so equal keys mean equal whole prefixes (up to
+ * 64-bit collisions).  Definition: FNV-1a 64 (offset basis
+ * 0xcbf29ce484222325, prime 0x100000001b3) over the 8 bytes of prev, then the
+ * 4 bytes of every token, both little-endian. */
+uint64_t dec_prefix_key(uint64_t prev, const int32_t* tokens, int32_t n);
+/* Slots of an allocated block that hold K/V (0 .. block_tokens); a new block
+ * starts at 0.  DEC_EBLOCK if not allocated, DEC_EINVAL if n is out of range. */
+int dec_pool_set_fill(dec_pool* p, int32_t id, int32_t n);
+/* Index a full allocated block under key: *registered = 1 if the key now
+ * names this block (0: the key already names another block, which keeps it).
+ * A block carries one key (a new key replaces its old one).  DEC_EINVAL if
+ * the block is not full, DEC_EBLOCK if not allocated. */
+int dec_pool_register(dec_pool* p, int32_t id, uint64_t key, int32_t* registered);
+/* The block indexed under key, reacquired (refcount + 1; a cached block
+ * leaves the cache), or *id = -1 if none.  DEC_OK either way. */
+int dec_pool_lookup(dec_pool* p, uint64_t key, int32_t* id);
+int dec_pool_cached_blocks(const dec_pool* p, int32_t* n);
 /* Element offset (within the slab buffer) of K (is_v=0) or V of KV head h at
  * position pos of a sequence with the given block table; the same function the
  * kernels use.  DEC_ERANGE if the table is too short, DEC_EBLOCK on a bad id. */
