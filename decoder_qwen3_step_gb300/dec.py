@@ -16,6 +16,8 @@ DEC_OK, DEC_EINVAL, DEC_ECAPACITY, DEC_EBLOCK, DEC_ERANGE, DEC_EVOCAB, DEC_ECUDA
 DEC_FP32, DEC_BF16_F16KV = 0, 1
 DEC_ROWS_ALL, DEC_ROWS_LAST = 0, 1
 DEC_DEV_BAD_ID, DEC_DEV_TIMEOUT, DEC_DEV_CAPACITY = 1, 2, 4
+DEC_PURPOSE_SAMPLE = 4
+DEC_SAMPLE_BAD_ID, DEC_SAMPLE_BAD_LOGIT, DEC_SAMPLE_NO_FINITE, DEC_SAMPLE_OVERFLOW = 1, 2, 4, 8
 
 ERROR_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ECAPACITY", 3: "DEC_EBLOCK", 4: "DEC_ERANGE",
                5: "DEC_EVOCAB", 6: "DEC_ECUDA", 7: "DEC_EDEVICE"}
@@ -29,6 +31,8 @@ EXPORTS = (
     "dec_launch_count", "dec_set_graphs", "dec_set_megakernel", "dec_megakernel_available", "dec_set_step_trace",
     "dec_set_tensor_cores", "dec_debug_product", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc",
     "dec_prefix_key", "dec_pool_set_fill", "dec_pool_register", "dec_pool_lookup", "dec_pool_cached_blocks",
+    "dec_child_seed", "dec_rng_stream", "dec_rng_next_u32", "dec_rng_uniform", "dec_sampler_workspace_bytes",
+    "dec_sampler_create", "dec_sampler_destroy", "dec_sampler_status", "dec_sample",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax",
                   "step")
@@ -56,6 +60,16 @@ _I32P = C.POINTER(C.c_int32)
 class dec_batch(C.Structure):
     _fields_ = [("n_seqs", C.c_int32), ("n_tokens", C.c_int32), ("ids", _I32P), ("ids_device", C.c_void_p),
                 ("positions", _I32P), ("seq_start", _I32P), ("block_table", _I32P), ("max_blocks", C.c_int32)]
+
+
+class dec_sampling(C.Structure):
+    _fields_ = [("temperature", C.c_double), ("top_k", C.c_int32), ("top_p", C.c_double), ("min_p", C.c_double),
+                ("repetition_penalty", C.c_double), ("presence_penalty", C.c_double),
+                ("frequency_penalty", C.c_double)]
+
+
+class dec_rng(C.Structure):
+    _fields_ = [("state", C.c_uint64), ("inc", C.c_uint64)]
 
 
 _lib = None
@@ -109,6 +123,15 @@ def lib() -> C.CDLL:
             "dec_attend_scratch_bytes": (I, [cfgp, C.c_int32, C.c_int32, C.c_int32, C.POINTER(SZ)]),
             "dec_attend": (I, [V, C.c_int32, C.c_int32, V, _I32P, _I32P, C.c_int32, V, V, SZ, V]),
             "dec_attend_noalloc": (I, [V, C.c_int32, C.c_int32, V, _I32P, _I32P, C.c_int32, V, V]),
+            "dec_child_seed": (C.c_uint64, [C.c_uint64, C.c_uint64]),
+            "dec_rng_stream": (None, [C.c_uint64, C.c_uint64, C.POINTER(dec_rng)]),
+            "dec_rng_next_u32": (C.c_uint32, [C.POINTER(dec_rng)]),
+            "dec_rng_uniform": (C.c_double, [C.POINTER(dec_rng)]),
+            "dec_sampler_workspace_bytes": (I, [C.c_int32, C.c_int32, C.POINTER(SZ)]),
+            "dec_sampler_create": (I, [C.c_int32, C.c_int32, V, SZ, C.POINTER(V)]),
+            "dec_sampler_destroy": (None, [V]),
+            "dec_sampler_status": (I, [V, C.POINTER(C.c_uint32)]),
+            "dec_sample": (I, [V, V, I64, C.c_int32, C.POINTER(dec_sampling), V, _I32P, _I32P, V, V, V, V]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -249,3 +249,92 @@ class Decoder:
             self.close()
         except Exception:
             pass
+
+
+def sampling_params(temperature=1.0, top_k=0, top_p=1.0, min_p=0.0, repetition_penalty=1.0, presence_penalty=0.0,
+                    frequency_penalty=0.0) -> dec.dec_sampling:
+    """One sequence's sampling parameters (the off values are the defaults)."""
+    return dec.dec_sampling(float(temperature), int(top_k), float(top_p), float(min_p), float(repetition_penalty),
+                            float(presence_penalty), float(frequency_penalty))
+
+
+class Sampler:
+    """The device sampler (libdec's dec_sample) with its workspace from torch.
+
+    rng states live on the device as an int64 tensor [n, 2] (state, inc) whose
+    bits are the C struct dec_rng; `streams(seeds)` makes the per-request
+    streams of purpose 4.
+    """
+
+    def __init__(self, vocab: int, max_seqs: int, device="cuda"):
+        self.L = dec.lib()
+        self.device = torch.device(device)
+        self.vocab, self.max_seqs = vocab, max_seqs
+        nbytes = C.c_size_t()
+        dec.check(self.L.dec_sampler_workspace_bytes(vocab, max_seqs, C.byref(nbytes)), "dec_sampler_workspace_bytes")
+        self.ws = torch.empty(nbytes.value + 256, dtype=torch.uint8, device=self.device)
+        base = self.ws.data_ptr()
+        aligned = (base + 255) & ~255
+        h = C.c_void_p()
+        with torch.cuda.device(self.device):
+            dec.check(self.L.dec_sampler_create(vocab, max_seqs, C.c_void_p(aligned), nbytes.value, C.byref(h)),
+                      "dec_sampler_create")
+        self.handle = h
+
+    def streams(self, seeds, purpose: int = dec.DEC_PURPOSE_SAMPLE) -> torch.Tensor:
+        out = np.zeros((len(seeds), 2), dtype=np.uint64)
+        r = dec.dec_rng()
+        for i, sd in enumerate(seeds):
+            self.L.dec_rng_stream(C.c_uint64(int(sd) & (2**64 - 1)), C.c_uint64(purpose), C.byref(r))
+            out[i] = (r.state, r.inc)
+        return torch.from_numpy(out.view(np.int64)).to(self.device)
+
+    def sample(self, logits: torch.Tensor, params, histories=None, rng: torch.Tensor | None = None, stream=None,
+               out=None):
+        """params: one dec_sampling per row of `logits` [n, >= vocab] (f32,
+        on the device); histories: per row (prompt_ids, output_ids) or None.
+        Returns device (tokens int32 [n], logprobs float64 [n]); `rng` is
+        advanced in place."""
+        n = logits.shape[0]
+        assert logits.dtype == torch.float32 and logits.is_cuda and logits.stride(1) == 1
+        P = (dec.dec_sampling * max(n, 1))(*params)
+        offs = _i32([0] * (n + 1))
+        npr = _i32([0] * max(n, 1))
+        hist = None
+        if histories is not None:
+            flat = []
+            for i, (pr, ou) in enumerate(histories):
+                flat.extend(int(x) for x in pr)
+                flat.extend(int(x) for x in ou)
+                offs[i + 1] = len(flat)
+                npr[i] = len(pr)
+            if flat:
+                hist = torch.tensor(flat, dtype=torch.int32, device=self.device)
+        if out is None:
+            tokens = torch.empty(n, dtype=torch.int32, device=self.device)
+            logprobs = torch.empty(n, dtype=torch.float64, device=self.device)
+        else:
+            tokens, logprobs = out
+        code = self.L.dec_sample(self.handle, C.c_void_p(logits.data_ptr()), logits.stride(0), n, P,
+                                 C.c_void_p(hist.data_ptr() if hist is not None else 0), _ptr(offs), _ptr(npr),
+                                 C.c_void_p(rng.data_ptr()), C.c_void_p(tokens.data_ptr()),
+                                 C.c_void_p(logprobs.data_ptr()), _stream_ptr(stream))
+        dec.check(code, "dec_sample")
+        self._keep = hist  # alive until the stream has read it
+        return tokens, logprobs
+
+    def status(self) -> int:
+        f = C.c_uint32()
+        dec.check(self.L.dec_sampler_status(self.handle, C.byref(f)), "dec_sampler_status")
+        return f.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.L.dec_sampler_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -335,6 +335,92 @@ int dec_f32_to_f16(const float* in, uint16_t* out, int64_t n, void* stream);
 int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X, int32_t T, float* Y, int32_t path,
                       void* stream);
 
+/* ---- the sampler (tinyllm L10.1 section 2.6 "The sampler and PCG32") ------
+ *
+ * One sampling step per sequence after the LM head, on the device, in f64:
+ * widen the logits; repetition penalty r over the distinct ids of prompt and
+ * output (l /= r if l > 0, else l *= r); presence a_p and frequency a_f over
+ * the output only (l -= a_f * count + a_p for ids the output holds); the
+ * returned logprob is the log-softmax at that point; temperature 0 returns
+ * the argmax (ties to the lowest id) and draws nothing; otherwise l /= T,
+ * keep the top_k ids in (l desc, id asc) order, keep the nucleus up to and
+ * including the id whose running probability reaches top_p, keep ids whose
+ * probability is at least min_p times the largest, renormalise over the kept
+ * ids, draw one uniform u and return the first id, in ascending id order,
+ * whose cumulative probability exceeds u.  Off values: top_k = 0 (or >=
+ * vocab), top_p = 1, min_p = 0, repetition_penalty = 1, presence and
+ * frequency 0.  Sums run in fixed trees (the result is the same bits alone or
+ * in a batch); they round differently from plain left-to-right loops, so a
+ * token can differ from the loop form only where u or a filter threshold lies
+ * within rounding (about 1e-12) of a cumulative sum. */
+
+#define DEC_PURPOSE_SAMPLE 4 /* the stream purpose of sampling (child_seed(seed, 4)) */
+
+typedef struct dec_sampling {
+    double temperature;        /* >= 0; 0 = greedy */
+    int32_t top_k;             /* >= 0; 0 or >= vocab = off */
+    double top_p;              /* in [0, 1]; 1 = off */
+    double min_p;              /* in [0, 1]; 0 = off */
+    double repetition_penalty; /* > 0; 1 = off */
+    double presence_penalty;   /* finite */
+    double frequency_penalty;  /* finite */
+} dec_sampling;
+
+/* PCG32 state (M. E. O'Neill's XSH RR 64/32): a 64-bit LCG state and its odd
+ * increment.  One uniform takes two 32-bit outputs a, b:
+ * u = ((a >> 5) * 2^26 + (b >> 6)) * 2^-53. */
+typedef struct dec_rng {
+    uint64_t state, inc;
+} dec_rng;
+
+/* child_seed(seed, purpose) = mix64(seed + purpose * 0x9E3779B97F4A7C15),
+ * mix64 being SplitMix64's finaliser (read so from the pages' worked example:
+ * child_seed(0, 4) = 0xF88BB8A8724C81EC). */
+uint64_t dec_child_seed(uint64_t seed, uint64_t purpose);
+/* The stream of one request and purpose: PCG32 seeded (pcg32_srandom_r) with
+ * child_seed(seed, purpose) on sequence `purpose`.  Host only. */
+void dec_rng_stream(uint64_t seed, uint64_t purpose, dec_rng* out);
+uint32_t dec_rng_next_u32(dec_rng* r); /* host: one 32-bit output */
+double dec_rng_uniform(dec_rng* r);    /* host: one uniform in [0, 1), on the 2^-53 grid */
+
+typedef struct dec_sampler dec_sampler;
+
+/* Device workspace of a sampler for `vocab` ids and up to `max_seqs`
+ * sequences a call (about 26 bytes per id per sequence).  vocab in
+ * [1, 2^20]; DEC_EINVAL otherwise. */
+int dec_sampler_workspace_bytes(int32_t vocab, int32_t max_seqs, size_t* bytes);
+/* workspace: caller-owned device memory, 256-byte aligned, at least
+ * dec_sampler_workspace_bytes; it is cleared here (synchronously) and must
+ * not be touched while the sampler lives.  The sampler owns only host
+ * bookkeeping (a small pinned staging ring). */
+int dec_sampler_create(int32_t vocab, int32_t max_seqs, void* workspace, size_t bytes, dec_sampler** out);
+void dec_sampler_destroy(dec_sampler* s);
+
+/* Device error word bits of the sampler (dec_sampler_status). */
+#define DEC_SAMPLE_BAD_ID    1u /* a history id outside [0, vocab): ignored */
+#define DEC_SAMPLE_BAD_LOGIT 2u /* a NaN or +inf logit: read as -inf */
+#define DEC_SAMPLE_NO_FINITE 4u /* every logit of a sequence is -inf: token -1 */
+#define DEC_SAMPLE_OVERFLOW  8u /* internal: a candidate list outgrew shared memory */
+/* Read (synchronously) the OR of the error bits every call so far raised. */
+int dec_sampler_status(dec_sampler* s, uint32_t* flags);
+
+/* Sample one token for each of n_seqs sequences.
+ *   logits           device f32 [n_seqs, ld], ld >= vocab (the LM head's output)
+ *   params           host [n_seqs], checked on the host (DEC_EINVAL)
+ *   history          device int32: each sequence's prompt ids then its output
+ *                    ids, sequence after sequence; NULL if all are empty
+ *   history_offsets  host int32 [n_seqs + 1]: sequence i owns
+ *                    history[offsets[i] .. offsets[i+1]); NULL = no history
+ *   n_prompt         host int32 [n_seqs]: how many of those are prompt ids;
+ *                    NULL = none
+ *   rng              device dec_rng [n_seqs]: read, and advanced by exactly
+ *                    one uniform for each sequence with temperature > 0
+ *   tokens           device int32 [n_seqs]   logprobs  device f64 [n_seqs]
+ * Asynchronous on `stream`; calls on one sampler must not overlap. */
+int dec_sample(dec_sampler* s, const float* logits, int64_t ld, int32_t n_seqs, const dec_sampling* params,
+               const int32_t* history, const int32_t* history_offsets, const int32_t* n_prompt, dec_rng* rng,
+               int32_t* tokens, double* logprobs, void* stream);
+
 /* Library version string. */
 const char* dec_version(void);
 
