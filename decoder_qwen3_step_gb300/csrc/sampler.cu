@@ -1,4 +1,4 @@
-// sampler.cu - the sampling step after the LM head, on the device, in f64.
+// sampler.cu - the sampling step after the LM head, on the device.
 //
 // tinyllm L10.1 "Candle model runner (Llama + bigram, int4), Rust KV cache,
 // sampler and PCG32", section 2.6 "The sampler and PCG32": widen the logits to
@@ -15,16 +15,29 @@
 // mix64(seed + 4 * 0x9E3779B97F4A7C15) on sequence 4; mix64 is read as
 // SplitMix64's finaliser (the worked example of section 3 pins that reading).
 //
+// Arithmetic.  This GPU issues f64 at about 1/64 of its f32 rate, so the
+// per-id work avoids the f64 pipe: the penalised logit is exact f64 (an f32
+// widened, or one f64 penalty step for the few ids of the history); order
+// comparisons use integer keys of those f64 values; exponentials, sums and
+// thresholds run in double-f32 arithmetic (a float head plus a float tail,
+// Dekker's and Knuth's error-free sums and products) with a table-driven
+// exponential (Tang's method: exp(x) = 2^n * 2^(j/64) * exp(r), |r| <=
+// ln2/128, r reduced with a four-piece ln2/64 and exp(r) from its Taylor
+// polynomial of degree 5), accurate to about 2^-46.  The log-partition
+// takes one f64 logarithm per sequence.  Results agree with the plain f64
+// definition to about 1e-13 relative; a token can differ from it only where
+// u or a filter threshold sits within that of a cumulative sum.
+//
 // The device plan (per sequence; every kept set is a prefix of the
 // (logit desc, id asc) order, cut further by the min-p bound):
 //   k_mark      scatter the history into a per-sequence mark word per id:
 //               bit 0 set by the prompt, bits 1.. the output count; a
 //               non-zero word means the id was seen
 //   k_scan1     multi-CTA: penalised maximum (lowest id) and finite minimum
-//   k_scan2     multi-CTA, f64: e = exp(l - M) summed for the log-partition;
-//               when sampling, l/T, e' = exp(l/T - M/T), a linear bucket of
-//               l/T between its minimum and maximum (2048 buckets, bucket 0
-//               the top), bucket counts and fixed-point masses
+//   k_scan2     multi-CTA: e = exp(l - M) summed for the log-partition;
+//               when sampling, e' = exp((l - M)/T), the order key, a linear
+//               bucket of l between its minimum and maximum (2048 buckets,
+//               bucket 0 the top), bucket counts and fixed-point masses
 //   k_pick      one CTA: greedy ends here; otherwise the bucket histogram
 //               finds the bucket where the top-k count or the nucleus mass
 //               is reached, the candidates of the buckets up to there (or of
@@ -39,9 +52,7 @@
 //               and the id where the cumulative sum passes u.
 //   k_mark      clears the marks it set.
 // All sums are fixed trees, so the result is the same bits alone or in a
-// batch.  The sums run in another order than the plain left-to-right loops
-// of the definition, so a token can differ from it only where u or a filter
-// threshold sits within rounding of a cumulative sum.
+// batch.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -57,42 +68,48 @@ namespace {
 
 constexpr int kChunk = 1024;       // elements per scan CTA (and per final chunk)
 constexpr int kScanThreads = 256;  // 4 elements per thread
-constexpr int kBins = 2048;        // linear buckets of l/T
+constexpr int kBins = 2048;        // linear buckets of the logit
 constexpr int kCap = 4096;         // candidates held in shared memory
 constexpr int kPick = 1024;        // threads of the one-CTA kernels
 constexpr int kMaxChunks = 1024;   // chunks per sequence: vocab <= 2^20
-constexpr double kFix = 35184372088832.0;       // 2^45: fixed-point scale of bucket masses
-constexpr double kFixTol = 33554432.0;          // 2^25 = 2^-20 in e' units: slack on mass buckets
+constexpr float kFixF = 35184372088832.0f;  // 2^45: fixed-point scale of bucket masses
+constexpr double kFix = 35184372088832.0;
+constexpr double kFixTol = 33554432.0;      // 2^25 = 2^-20 in e' units: slack on mass buckets
 constexpr uint64_t kPcgMult = 6364136223846793005ull;
 constexpr int kStage = 4;
+static_assert(kBins == 2 * kPick, "the bucket scan takes two buckets per thread");
+static_assert(kCap == 4 * kPick, "list scans take four candidates per thread");
 
-struct SeqParam {  // 64 bytes, one per sequence
+struct SeqParam {  // 96 bytes, one per sequence
   double T, top_p, min_p, rep, pres, freq;
-  int32_t top_k, hist_off, n_hist, n_prompt;
+  float rTh, rTl;  // 1/T as head + tail
+  float pph, ppl;  // top_p
+  float mph, mpl;  // min_p
+  int32_t top_k, pad0;
+  int32_t hist_off, n_hist, n_prompt, pad1;
 };
 
 struct Part1 {
-  double mx, mn;
-  int32_t arg, pad;
-  double pad2;
+  uint64_t key;
+  float mn;
+  int32_t arg;
 };
 
 struct Part2 {
-  double se, se2;
+  float zh, zl, z2h, z2l;
 };
 
 struct PickState {  // hand-off from k_pick to the final kernels
-  int32_t mode;     // 0 done; 1 kept = order prefix up to `last` (if has_last) with e' >= emin
+  int32_t mode;     // 0 done; 1 kept = order prefix up to `last` (if has_last) with e' >= min_p
   int32_t has_last;
   int32_t last_id;
   int32_t pad;
   uint64_t last_key;
-  uint64_t emin_bits;
   double M, lse;
 };
 
 struct Layout {
-  size_t seqs, marks, W, E, bins, part1, part2, hcnt, hmass, state, fsum, status, total;
+  size_t seqs, marks, K, E, bins, part1, part2, hcnt, hmass, state, fsum, status, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -108,7 +125,7 @@ Layout layout_of(int V, int S) {
   };
   L.seqs = take((size_t)S * sizeof(SeqParam));
   L.marks = take((size_t)S * V * 4);
-  L.W = take((size_t)S * V * 8);
+  L.K = take((size_t)S * V * 8);
   L.E = take((size_t)S * V * 8);
   L.bins = take((size_t)S * V * 2);
   L.part1 = take((size_t)S * NB * sizeof(Part1));
@@ -116,13 +133,169 @@ Layout layout_of(int V, int S) {
   L.hcnt = take((size_t)S * kBins * 4);
   L.hmass = take((size_t)S * kBins * 8);
   L.state = take((size_t)S * sizeof(PickState));
-  L.fsum = take((size_t)S * NB * 8);
+  L.fsum = take((size_t)S * NB * sizeof(float2));
   L.status = take(256);
   L.total = o;
   return L;
 }
 
-// ---- shared device helpers ------------------------------------------------------
+// ---- double-f32 arithmetic --------------------------------------------------------
+
+struct df {
+  float h, l;
+};
+
+__device__ __forceinline__ df mk(float h, float l) {
+  df r;
+  r.h = h;
+  r.l = l;
+  return r;
+}
+
+// Knuth's two-sum: s + e == a + b exactly
+__device__ __forceinline__ df two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  const float e = (a - (s - bb)) + (b - bb);
+  return mk(s, e);
+}
+
+// Dekker's fast two-sum, |a| >= |b| (or a == 0)
+__device__ __forceinline__ df quick_two_sum(float a, float b) {
+  const float s = a + b;
+  return mk(s, b - (s - a));
+}
+
+// p + e == a * b exactly (one fused multiply-add)
+__device__ __forceinline__ df two_prod(float a, float b) {
+  const float p = a * b;
+  return mk(p, fmaf(a, b, -p));
+}
+
+__device__ __forceinline__ df df_add(df a, df b) {
+  df s = two_sum(a.h, b.h);
+  const df t = two_sum(a.l, b.l);
+  s.l += t.h;
+  s = quick_two_sum(s.h, s.l);
+  s.l += t.l;
+  return quick_two_sum(s.h, s.l);
+}
+
+__device__ __forceinline__ df df_mul(df a, df b) {
+  df p = two_prod(a.h, b.h);
+  p.l = fmaf(a.h, b.l, fmaf(a.l, b.h, p.l));
+  return quick_two_sum(p.h, p.l);
+}
+
+__device__ __forceinline__ bool df_ge(df a, df b) { return a.h > b.h || (a.h == b.h && a.l >= b.l); }
+__device__ __forceinline__ bool df_gt(df a, df b) { return a.h > b.h || (a.h == b.h && a.l > b.l); }
+
+__device__ __forceinline__ df df_of(double x) {
+  const float h = __double2float_rn(x);
+  return mk(h, __double2float_rn(x - (double)h));
+}
+
+__device__ __forceinline__ double dbl_of(df x) { return (double)x.h + (double)x.l; }
+
+// 2^(j/64) = head + tail, j = 0..63 (gen_exp_tables.py)
+__device__ const float2 kExp2Tab[64] = {
+  {0x1.0000000000000p+0f, 0x0.0p+0f},
+  {0x1.02c9a40000000p+0f, -0x1.887fa00000000p-28f},
+  {0x1.059b0e0000000p+0f, -0x1.9d4f520000000p-25f},
+  {0x1.0874520000000p+0f, -0x1.e2990e0000000p-26f},
+  {0x1.0b55860000000p+0f, 0x1.9f31220000000p-25f},
+  {0x1.0e3ec40000000p+0f, -0x1.a585cc0000000p-25f},
+  {0x1.11301e0000000p+0f, -0x1.fdb4960000000p-25f},
+  {0x1.1429aa0000000p+0f, 0x1.d525bc0000000p-25f},
+  {0x1.172b840000000p+0f, -0x1.c157420000000p-27f},
+  {0x1.1a35be0000000p+0f, 0x1.6df96e0000000p-25f},
+  {0x1.1d48740000000p+0f, -0x1.d2e8ca0000000p-25f},
+  {0x1.2063b80000000p+0f, 0x1.0c519a0000000p-25f},
+  {0x1.2387a60000000p+0f, 0x1.ceac480000000p-25f},
+  {0x1.26b4560000000p+0f, 0x1.789f380000000p-26f},
+  {0x1.29e9e00000000p+0f, -0x1.5c04240000000p-25f},
+  {0x1.2d285a0000000p+0f, 0x1.b900c20000000p-26f},
+  {0x1.306fe00000000p+0f, 0x1.4636e20000000p-25f},
+  {0x1.33c08c0000000p+0f, -0x1.b37d200000000p-25f},
+  {0x1.371a740000000p+0f, -0x1.18aac60000000p-25f},
+  {0x1.3a7db40000000p+0f, -0x1.634c020000000p-25f},
+  {0x1.3dea640000000p+0f, 0x1.8246840000000p-25f},
+  {0x1.4160a20000000p+0f, 0x1.f72e2a0000000p-28f},
+  {0x1.44e0860000000p+0f, 0x1.8624b40000000p-30f},
+  {0x1.486a2c0000000p+0f, -0x1.47d8660000000p-25f},
+  {0x1.4bfdae0000000p+0f, -0x1.593abc0000000p-25f},
+  {0x1.4f9b280000000p+0f, -0x1.2c5a6c0000000p-25f},
+  {0x1.5342b60000000p+0f, -0x1.2c56100000000p-25f},
+  {0x1.56f4740000000p+0f, -0x1.295b040000000p-25f},
+  {0x1.5ab07e0000000p+0f, -0x1.5bd5ec0000000p-27f},
+  {0x1.5e76f20000000p+0f, -0x1.4a5bd60000000p-25f},
+  {0x1.6247ec0000000p+0f, -0x1.f8b5500000000p-25f},
+  {0x1.6623880000000p+0f, 0x1.2a91120000000p-27f},
+  {0x1.6a09e60000000p+0f, 0x1.9fcef40000000p-26f},
+  {0x1.6dfb240000000p+0f, -0x1.cd72e80000000p-27f},
+  {0x1.71f75e0000000p+0f, 0x1.1d8bee0000000p-25f},
+  {0x1.75feb60000000p+0f, -0x1.37b3060000000p-25f},
+  {0x1.7a11480000000p+0f, -0x1.829fd00000000p-25f},
+  {0x1.7e2f340000000p+0f, -0x1.2616340000000p-25f},
+  {0x1.82589a0000000p+0f, -0x1.accc7c0000000p-26f},
+  {0x1.868d9a0000000p+0f, -0x1.2edb440000000p-26f},
+  {0x1.8ace540000000p+0f, 0x1.15506e0000000p-27f},
+  {0x1.8f1aea0000000p+0f, -0x1.baa2320000000p-26f},
+  {0x1.93737c0000000p+0f, -0x1.e647440000000p-25f},
+  {0x1.97d82a0000000p+0f, -0x1.0d8d840000000p-31f},
+  {0x1.9c49180000000p+0f, 0x1.51f8480000000p-27f},
+  {0x1.a0c6680000000p+0f, -0x1.2886a60000000p-26f},
+  {0x1.a5503c0000000p+0f, -0x1.b83b540000000p-25f},
+  {0x1.a9e6b60000000p+0f, -0x1.50c0480000000p-25f},
+  {0x1.ae89fa0000000p+0f, -0x1.a94b140000000p-26f},
+  {0x1.b33a2c0000000p+0f, -0x1.ec3a820000000p-26f},
+  {0x1.b7f7700000000p+0f, -0x1.a094380000000p-25f},
+  {0x1.bcc1ea0000000p+0f, -0x1.f687c60000000p-25f},
+  {0x1.c199be0000000p+0f, -0x1.3d56b20000000p-27f},
+  {0x1.c67f120000000p+0f, 0x1.cafa2a0000000p-25f},
+  {0x1.cb720e0000000p+0f, -0x1.8837cc0000000p-27f},
+  {0x1.d072d40000000p+0f, 0x1.40f1300000000p-25f},
+  {0x1.d5818e0000000p+0f, -0x1.822dbc0000000p-27f},
+  {0x1.da9e600000000p+0f, 0x1.ed99420000000p-27f},
+  {0x1.dfc9740000000p+0f, -0x1.908c940000000p-25f},
+  {0x1.e502ee0000000p+0f, 0x1.e2cffe0000000p-26f},
+  {0x1.ea4afa0000000p+0f, 0x1.52486c0000000p-27f},
+  {0x1.efa1be0000000p+0f, 0x1.cc2b440000000p-25f},
+  {0x1.f507660000000p+0f, -0x1.246eb00000000p-26f},
+  {0x1.fa7c180000000p+0f, 0x1.9e90d80000000p-28f},
+};
+
+// ln2/64 = L1 + L2 + L3 + L4; L1..L3 have 11 significant bits, so k * Li is exact for |k| < 2^13
+constexpr float kL1 = 0x1.62c0000000000p-7f;
+constexpr float kL2 = 0x1.2140000000000p-18f;
+constexpr float kL3 = 0x1.fbc0000000000p-29f;
+constexpr float kL4 = 0x1.473de60000000p-40f;
+constexpr float k64OverLn2 = 0x1.7154760000000p+6f;
+
+// exp(x) for x <= 0 in double-f32 (Tang's table-driven method); 0 below -87
+__device__ __forceinline__ df df_exp(df x) {
+  if (!(x.h > -87.0f)) return mk(0.0f, 0.0f);
+  const float kf = rintf(x.h * k64OverLn2);
+  const int k = (int)kf;
+  const float r0 = fmaf(-kf, kL1, x.h);  // exact: the two are within a factor of two
+  df r = two_sum(r0, -kf * kL2);
+  r = df_add(r, mk(-kf * kL3, 0.0f));
+  r = df_add(r, mk(-kf * kL4, 0.0f));
+  r = df_add(r, mk(x.l, 0.0f));
+  // exp(r) = 1 + r + r^2/2 + (r^3/6 + r^4/24 + r^5/120); the bracket is below 3e-8
+  const df r2 = df_mul(r, r);
+  const float rh = r.h;
+  const float c = rh * rh * rh * (0.16666667f + rh * (0.041666668f + rh * 0.0083333338f));
+  df s = df_add(r, mk(0.5f * r2.h, 0.5f * r2.l));
+  s = df_add(s, mk(c, 0.0f));
+  df e = df_add(mk(1.0f, 0.0f), s);
+  const float2 t = kExp2Tab[k & 63];
+  e = df_mul(e, mk(t.x, t.y));
+  const float sc = __int_as_float(((k >> 6) + 127) << 23);  // 2^n, n >= -126
+  return mk(e.h * sc, e.l * sc);
+}
+
+// ---- keys, penalties, generator -------------------------------------------------------
 
 __device__ __forceinline__ float load_logit(const float* x, int i, bool& bad) {
   float v = x[i];
@@ -133,22 +306,43 @@ __device__ __forceinline__ float load_logit(const float* x, int i, bool& bad) {
   return v;
 }
 
-// the penalties, with the rounding steps of the definition (no contraction)
-__device__ __forceinline__ double penalize(float x, int32_t mk, const SeqParam& q) {
+// the penalties in f64, with the rounding steps of the definition (no contraction)
+__device__ __forceinline__ double penalize(float x, int32_t mk_, const SeqParam& q) {
   double l = (double)x;
-  if (mk != 0) {
+  if (mk_ != 0) {
     l = l > 0.0 ? __ddiv_rn(l, q.rep) : __dmul_rn(l, q.rep);
-    const int c = mk >> 1;
+    const int c = mk_ >> 1;
     if (c > 0) l = __dsub_rn(l, __dadd_rn(__dmul_rn(q.freq, (double)c), q.pres));
   }
   return l;
 }
 
-// order key: larger key = earlier in (value desc); -0 and +0 share one key
-__device__ __forceinline__ uint64_t okey(double x) {
-  uint64_t b = (uint64_t)__double_as_longlong(x);
+// order key of an f64 value: larger key = larger value; -0 and +0 share one key
+__device__ __forceinline__ uint64_t okey_bits(uint64_t b) {
   if (b == 0x8000000000000000ull) b = 0;
   return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+__device__ __forceinline__ uint64_t okey(double x) { return okey_bits((uint64_t)__double_as_longlong(x)); }
+
+// okey((double)x) from the float's bits with integer operations
+__device__ __forceinline__ uint64_t okey_f32(float x) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t e = (u >> 23) & 0xFFu, m = u & 0x7FFFFFu;
+  uint64_t b;
+  if (e == 0) {
+    if (m == 0) return 0x8000000000000000ull;  // +-0
+    b = (uint64_t)__double_as_longlong((double)x);  // subnormal: rare
+  } else if (e == 0xFFu) {
+    b = ((uint64_t)(u >> 31) << 63) | 0x7FF0000000000000ull | ((uint64_t)m << 29);
+  } else {
+    b = ((uint64_t)(u >> 31) << 63) | ((uint64_t)(e + 896u) << 52) | ((uint64_t)m << 29);
+  }
+  return okey_bits(b);
+}
+
+__device__ __forceinline__ double key_value(uint64_t k) {
+  const uint64_t b = (k >> 63) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
+  return __longlong_as_double((long long)b);
 }
 
 // (key, id) a comes before (key, id) b in (value desc, id asc) order
@@ -158,6 +352,10 @@ __device__ __forceinline__ bool before(uint64_t ka, int32_t ia, uint64_t kb, int
 
 __device__ __forceinline__ unsigned __int128 ckey(uint64_t k, int32_t id) {
   return ((unsigned __int128)k << 32) | (uint32_t)(~(uint32_t)id);
+}
+
+__device__ __forceinline__ unsigned long long fix_of(float2 e) {
+  return (unsigned long long)((long long)__float2ll_rn(e.x * kFixF) + (long long)__float2ll_rn(e.y * kFixF));
 }
 
 __device__ __forceinline__ uint32_t pcg_next(uint64_t& state, uint64_t inc) {
@@ -174,62 +372,66 @@ __device__ __forceinline__ double pcg_uniform(uint64_t& state, uint64_t inc) {
   return (double)(((uint64_t)(a >> 5) << 26) + (b >> 6)) * 0x1p-53;
 }
 
-// (max, lowest id) pair: a beats b
-__device__ __forceinline__ bool better(double va, int ia, double vb, int ib) { return va > vb || (va == vb && ia < ib); }
+// ---- block reductions (fixed trees) ------------------------------------------------------
 
+__device__ __forceinline__ df shfl_xor_df(df v, int o) {
+  return mk(__shfl_xor_sync(0xffffffffu, v.h, o), __shfl_xor_sync(0xffffffffu, v.l, o));
+}
 
-// deterministic block sum of one double per thread (fixed butterfly tree)
 template <int NT>
-__device__ double block_sum(double v, double* red) {
+__device__ df block_sum_df(df v, float2* red) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o; o >>= 1) v = df_add(v, shfl_xor_df(v, o));
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
-  if (l == 0) red[w] = v;
+  if (l == 0) red[w] = make_float2(v.h, v.l);
   __syncthreads();
-  double t = l < NT / 32 ? red[l] : 0.0;
+  const float2 r = red[l & (NT / 32 - 1)];
+  df t = l < NT / 32 ? mk(r.x, r.y) : mk(0.0f, 0.0f);
 #pragma unroll
-  for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  for (int o = 16; o; o >>= 1) t = df_add(t, shfl_xor_df(t, o));
   return t;  // every thread holds the total
 }
 
+// the largest key, lowest id on ties
 template <int NT>
-__device__ void block_argmax(double& v, int& id, double* redv, int* redi) {
+__device__ void block_maxkey(uint64_t& k, int& id, unsigned long long* redk, int* redi) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
-    const double ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const uint64_t ok = __shfl_xor_sync(0xffffffffu, (unsigned long long)k, o);
     const int oi = __shfl_xor_sync(0xffffffffu, id, o);
-    if (better(ov, oi, v, id)) v = ov, id = oi;
+    if (before(ok, oi, k, id)) k = ok, id = oi;
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
-  if (l == 0) redv[w] = v, redi[w] = id;
+  if (l == 0) redk[w] = k, redi[w] = id;
   __syncthreads();
-  v = l < NT / 32 ? redv[l] : -INFINITY;
-  id = l < NT / 32 ? redi[l] : 0x7fffffff;
+  const int src = l & (NT / 32 - 1);
+  k = l < NT / 32 ? redk[src] : 0ull;
+  id = l < NT / 32 ? redi[src] : 0x7fffffff;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
-    const double ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const uint64_t ok = __shfl_xor_sync(0xffffffffu, (unsigned long long)k, o);
     const int oi = __shfl_xor_sync(0xffffffffu, id, o);
-    if (better(ov, oi, v, id)) v = ov, id = oi;
+    if (before(ok, oi, k, id)) k = ok, id = oi;
   }
 }
 
 template <int NT>
-__device__ double block_min(double v, double* red) {
+__device__ float block_minf(float v, float* red) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmin(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
   if (l == 0) red[w] = v;
   __syncthreads();
-  double t = l < NT / 32 ? red[l] : INFINITY;
+  float t = l < NT / 32 ? red[l & (NT / 32 - 1)] : INFINITY;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) t = fmin(t, __shfl_xor_sync(0xffffffffu, t, o));
+  for (int o = 16; o; o >>= 1) t = fminf(t, __shfl_xor_sync(0xffffffffu, t, o));
   return t;
 }
 
-// inclusive scan of one value per thread (1024 threads), deterministic
+// inclusive scan of one value per thread over 1024 threads (fixed tree)
 template <typename U>
 __device__ U block_scan(U v, U* red, U& total) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -261,13 +463,43 @@ __device__ U block_scan(U v, U* red, U& total) {
   return v + off;
 }
 
+// the same for double-f32 values
+__device__ df block_scan_df(df v, float2* red, df& total) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const df n = mk(__shfl_up_sync(0xffffffffu, v.h, o), __shfl_up_sync(0xffffffffu, v.l, o));
+    if (l >= o) v = df_add(v, n);
+  }
+  __syncthreads();
+  if (l == 31) red[w] = make_float2(v.h, v.l);
+  __syncthreads();
+  if (w == 0) {
+    const float2 r = red[l];
+    df t = mk(r.x, r.y);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const df n = mk(__shfl_up_sync(0xffffffffu, t.h, o), __shfl_up_sync(0xffffffffu, t.l, o));
+      if (l >= o) t = df_add(t, n);
+    }
+    red[l] = make_float2(t.h, t.l);
+  }
+  __syncthreads();
+  const float2 x = red[l];
+  total = mk(__shfl_sync(0xffffffffu, x.x, 31), __shfl_sync(0xffffffffu, x.y, 31));
+  df off = mk(__shfl_sync(0xffffffffu, x.x, (w + 31) & 31), __shfl_sync(0xffffffffu, x.y, (w + 31) & 31));
+  if (w == 0) off = mk(0.0f, 0.0f);
+  __syncthreads();
+  return df_add(v, off);
+}
+
 // ---- history marks ----------------------------------------------------------------
 
 __global__ void k_mark(const SeqParam* __restrict__ sp, const int32_t* __restrict__ hist, int32_t* marks, int V,
                        int set, uint32_t* status) {
   const int s = blockIdx.y;
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  const SeqParam q = sp[s];
+  const SeqParam& q = sp[s];
   if (j >= q.n_hist) return;
   const int id = hist[q.hist_off + j];
   if (id < 0 || id >= V) {
@@ -289,133 +521,171 @@ __global__ void __launch_bounds__(kScanThreads) k_scan1(const float* __restrict_
                                                          const int32_t* __restrict__ marks,
                                                          const SeqParam* __restrict__ sp, int V, int NB,
                                                          Part1* __restrict__ part, uint32_t* status) {
-  __shared__ double redv[32];
+  __shared__ unsigned long long redk[32];
   __shared__ int redi[32];
+  __shared__ float redf[32];
   const int s = blockIdx.y, b = blockIdx.x, t = threadIdx.x;
-  const SeqParam q = sp[s];
+  const SeqParam& q = sp[s];
   const float* x = logits + (size_t)s * ld;
-  const int32_t* mk = marks + (size_t)s * V;
-  float fmx = -INFINITY, fmn = INFINITY;
-  int fa = 0x7fffffff;
-  double dmx = -INFINITY, dmn = INFINITY;
-  int da = 0x7fffffff;
+  const int32_t* mkv = marks + (size_t)s * V;
+  uint64_t bk = 0;
+  int ba = 0x7fffffff;
+  float mn = INFINITY;
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < kChunk / kScanThreads; ++j) {
     const int i = b * kChunk + j * kScanThreads + t;
     if (i < V) {
       const float v = load_logit(x, i, bad);
-      const int32_t m = mk[i];
-      if (m == 0) {  // unpenalised: compare in f32 (the widening is exact)
-        if (v > fmx) fmx = v, fa = i;
-        if (v > -INFINITY && v < fmn) fmn = v;
+      const int32_t m = mkv[i];
+      uint64_t key;
+      float lf;
+      if (m == 0) {
+        key = okey_f32(v);
+        lf = v;
       } else {
         const double l = penalize(v, m, q);
-        if (l > dmx) dmx = l, da = i;
-        if (l > -INFINITY && l < dmn) dmn = l;
+        key = okey(l);
+        lf = __double2float_rn(l);
       }
+      if (key > bk) bk = key, ba = i;  // ids rise: ties keep the lowest
+      if (lf > -INFINITY && lf < mn) mn = lf;
     }
   }
   if (bad) atomicOr(status, (uint32_t)DEC_SAMPLE_BAD_LOGIT);
-  double mx = (double)fmx;
-  int arg = fa;
-  if (better(dmx, da, mx, arg)) mx = dmx, arg = da;
-  const double mn = fmin((double)fmn, dmn);
-  block_argmax<kScanThreads>(mx, arg, redv, redi);
-  const double mnb = block_min<kScanThreads>(mn, redv);
+  block_maxkey<kScanThreads>(bk, ba, redk, redi);
+  const float mnb = block_minf<kScanThreads>(mn, redf);
   if (t == 0) {
     Part1 p;
-    p.mx = mx;
+    p.key = bk;
     p.mn = mnb;
-    p.arg = arg;
-    p.pad = 0;
-    p.pad2 = 0;
+    p.arg = ba;
     part[(size_t)s * NB + b] = p;
   }
 }
 
-// every CTA reduces the per-chunk maxima in the same way: M, its lowest id, the finite minimum
+// every CTA reduces the per-chunk maxima the same way: the top key, its lowest id, the finite minimum
 template <int NT>
-__device__ void reduce_part1(const Part1* p, int NB, double& M, int& arg, double& mn, double* redv, int* redi) {
-  double v = -INFINITY, m = INFINITY;
+__device__ void reduce_part1(const Part1* p, int NB, uint64_t& M, int& arg, float& mn, unsigned long long* redk,
+                             int* redi, float* redf) {
+  uint64_t k = 0;
   int id = 0x7fffffff;
+  float m = INFINITY;
   for (int c = threadIdx.x; c < NB; c += NT) {
     const Part1 e = p[c];
-    if (better(e.mx, e.arg, v, id)) v = e.mx, id = e.arg;
-    m = fmin(m, e.mn);
+    if (before(e.key, e.arg, k, id)) k = e.key, id = e.arg;
+    m = fminf(m, e.mn);
   }
-  block_argmax<NT>(v, id, redv, redi);
-  mn = block_min<NT>(m, redv);
-  M = v;
+  block_maxkey<NT>(k, id, redk, redi);
+  mn = block_minf<NT>(m, redf);
+  M = k;
   arg = id;
+}
+
+// the penalised logit as a double-f32 pair, its order key and its float
+__device__ __forceinline__ void logit_of(float v, int32_t m, const SeqParam& q, df& l, uint64_t& key, float& lf) {
+  if (m == 0) {
+    l = mk(v, 0.0f);
+    key = okey_f32(v);
+    lf = v;
+  } else {
+    const double d = penalize(v, m, q);
+    l = df_of(d);
+    key = okey(d);
+    lf = l.h;
+  }
 }
 
 __global__ void __launch_bounds__(kScanThreads) k_scan2(const float* __restrict__ logits, int64_t ld,
                                                          const int32_t* __restrict__ marks,
                                                          const SeqParam* __restrict__ sp, int V, int NB,
                                                          const Part1* __restrict__ part1, Part2* __restrict__ part2,
-                                                         double* __restrict__ W, double* __restrict__ E,
+                                                         uint64_t* __restrict__ K, float2* __restrict__ E,
                                                          uint16_t* __restrict__ bins, uint32_t* __restrict__ hcnt,
                                                          unsigned long long* __restrict__ hmass, uint32_t* status) {
-  __shared__ double redv[32];
+  __shared__ unsigned long long redk[32];
   __shared__ int redi[32];
+  __shared__ float redf[32];
+  __shared__ float2 redd[32];
   __shared__ uint32_t sc[kBins];
-  __shared__ unsigned long long sm[kBins];
+  __shared__ unsigned long long smass[kBins];
+  __shared__ float s_Mh, s_Ml;
   const int s = blockIdx.y, b = blockIdx.x, t = threadIdx.x;
-  const SeqParam q = sp[s];
-  double M, mn;
+  const SeqParam& q = sp[s];
+  uint64_t Mk;
   int arg;
-  reduce_part1<kScanThreads>(part1 + (size_t)s * NB, NB, M, arg, mn, redv, redi);
-  if (!(M > -INFINITY)) {  // no finite logit
+  float mn;
+  reduce_part1<kScanThreads>(part1 + (size_t)s * NB, NB, Mk, arg, mn, redk, redi, redf);
+  if (t == 0) {  // one f64 split per CTA
+    const df Md = df_of(key_value(Mk));
+    s_Mh = Md.h;
+    s_Ml = Md.l;
+  }
+  __syncthreads();
+  const float Mh = s_Mh, Ml = s_Ml;
+  if (!(Mh > -INFINITY)) {  // no finite logit
     if (t == 0 && b == 0) atomicOr(status, (uint32_t)DEC_SAMPLE_NO_FINITE);
     return;
   }
   const bool sampling = q.T > 0.0;
   const bool unit = q.T == 1.0;
-  const double Mt = unit ? M : __ddiv_rn(M, q.T);
-  const double mtn = unit ? mn : __ddiv_rn(mn, q.T);
-  const double R = Mt - mtn;
-  double scale = R > 0.0 ? (double)kBins / R : 0.0;
-  if (!(scale < 1e300)) scale = 0.0;
+  const df rT = mk(q.rTh, q.rTl);
+  const float R = Mh - mn;
+  float scale = R > 0.0f ? (float)kBins / R : 0.0f;
+  if (!(scale < 1e30f)) scale = 0.0f;
   if (sampling) {
-    for (int i = t; i < kBins; i += kScanThreads) sc[i] = 0, sm[i] = 0;
+    for (int i = t; i < kBins; i += kScanThreads) sc[i] = 0, smass[i] = 0;
     __syncthreads();
   }
   const float* x = logits + (size_t)s * ld;
-  const int32_t* mk = marks + (size_t)s * V;
+  const int32_t* mkv = marks + (size_t)s * V;
   const size_t row = (size_t)s * V;
-  double se = 0.0, se2 = 0.0;
+  df z = mk(0.0f, 0.0f), z2 = mk(0.0f, 0.0f);
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < kChunk / kScanThreads; ++j) {
     const int i = b * kChunk + j * kScanThreads + t;
     if (i < V) {
-      const double l = penalize(load_logit(x, i, bad), mk[i], q);
-      const double e = exp(l - M);
-      se += e;
+      df l;
+      uint64_t key;
+      float lf;
+      logit_of(load_logit(x, i, bad), mkv[i], q, l, key, lf);
+      df e = mk(0.0f, 0.0f), e2 = mk(0.0f, 0.0f);
+      if (lf > -INFINITY) {
+        df d = two_sum(l.h, -Mh);
+        if (l.l != 0.0f || Ml != 0.0f) d = df_add(d, mk(l.l - Ml, 0.0f));
+        e = df_exp(d);
+        if (sampling) e2 = unit ? e : df_exp(df_mul(d, rT));
+      }
+      z = df_add(z, e);
       if (sampling) {
-        const double lt = unit ? l : __ddiv_rn(l, q.T);
-        const double et = unit ? e : exp(lt - Mt);
-        se2 += et;
-        W[row + i] = lt;
-        E[row + i] = et;
-        const int bin = scale > 0.0 ? (int)fmin((Mt - lt) * scale, (double)(kBins - 1)) : 0;
+        z2 = df_add(z2, e2);
+        K[row + i] = key;
+        E[row + i] = make_float2(e2.h, e2.l);
+        const int bin = scale > 0.0f ? (int)fminf((Mh - lf) * scale, (float)(kBins - 1)) : 0;
         bins[row + i] = (uint16_t)bin;
         atomicAdd(&sc[bin], 1u);
-        atomicAdd(&sm[bin], (unsigned long long)__double2ull_rn(et * kFix));
+        atomicAdd(&smass[bin], fix_of(make_float2(e2.h, e2.l)));
       }
     }
   }
   (void)bad;  // k_scan1 already flagged it
-  se = block_sum<kScanThreads>(se, redv);
-  se2 = block_sum<kScanThreads>(se2, redv);
-  if (t == 0) part2[(size_t)s * NB + b] = Part2{se, se2};
+  z = block_sum_df<kScanThreads>(z, redd);
+  z2 = block_sum_df<kScanThreads>(z2, redd);
+  if (t == 0) {
+    Part2 p;
+    p.zh = z.h;
+    p.zl = z.l;
+    p.z2h = z2.h;
+    p.z2l = z2.l;
+    part2[(size_t)s * NB + b] = p;
+  }
   if (sampling) {
     __syncthreads();
     for (int i = t; i < kBins; i += kScanThreads)
       if (sc[i]) {
         atomicAdd(&hcnt[(size_t)s * kBins + i], sc[i]);
-        atomicAdd(&hmass[(size_t)s * kBins + i], sm[i]);
+        atomicAdd(&hmass[(size_t)s * kBins + i], smass[i]);
       }
   }
 }
@@ -424,25 +694,26 @@ __global__ void __launch_bounds__(kScanThreads) k_scan2(const float* __restrict_
 
 struct PickSmem {
   uint64_t ck[kCap];   // order keys of the candidates
-  double ce[kCap];     // their e'
+  float2 ce[kCap];     // their e' (head, tail)
   int32_t cid[kCap];   // their ids
   uint32_t hc[kBins];  // bucket (or digit) counts
   unsigned long long hm[kBins];
-  double redd[32];
+  float2 redd[32];
+  unsigned long long redk[32];
   int redi[32];
-  unsigned long long redu[32];
-  int n;           // candidates gathered
+  float redf[32];
+  int n;
   int flag;
 };
 
-struct Frame {     // where a gathered list sits in the order
-  long long above;   // elements of the restricted set before the list
-  double m_above;    // their e' sum
+struct Frame {      // where a gathered list sits in the order
+  long long above;  // elements of the restricted set before the list
+  df m_above;       // their e' sum
 };
 
 enum { kCount = 0, kMass = 1 };
 
-struct Lim {          // restriction to the order prefix ending at (key, id), bucket `bin`
+struct Lim {  // restriction to the order prefix ending at (key, id), bucket `bin`
   int on;
   uint64_t key;
   int32_t id;
@@ -455,11 +726,13 @@ __device__ __forceinline__ bool in_lim(const Lim& L, int bin, uint64_t k, int32_
   return !before(L.key, L.id, k, id);  // (k, id) at or before the limit
 }
 
+__device__ __forceinline__ df ce_of(const PickSmem& sm, int j) { return mk(sm.ce[j].x, sm.ce[j].y); }
+
 // bitonic sort of sm.ck/ce/cid[0..n) in (key desc, id asc) order (by_id: id asc)
 __device__ void sort_list(PickSmem& sm, int n, bool by_id) {
   int P = 1;
   while (P < n) P <<= 1;
-  for (int i = n + threadIdx.x; i < P; i += kPick) sm.ck[i] = 0, sm.ce[i] = 0.0, sm.cid[i] = 0x7fffffff;
+  for (int i = n + threadIdx.x; i < P; i += kPick) sm.ck[i] = 0, sm.ce[i] = make_float2(0.f, 0.f), sm.cid[i] = 0x7fffffff;
   __syncthreads();
   for (int k = 2; k <= P; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
@@ -467,16 +740,12 @@ __device__ void sort_list(PickSmem& sm, int n, bool by_id) {
         const int p = i ^ j;
         if (p > i) {
           const bool up = (i & k) == 0;
-          bool first_is_i;
-          if (by_id)
-            first_is_i = sm.cid[i] < sm.cid[p];
-          else
-            first_is_i = before(sm.ck[i], sm.cid[i], sm.ck[p], sm.cid[p]);
+          const bool first_is_i = by_id ? sm.cid[i] < sm.cid[p] : before(sm.ck[i], sm.cid[i], sm.ck[p], sm.cid[p]);
           if (first_is_i != up) {
             const uint64_t tk = sm.ck[i];
             sm.ck[i] = sm.ck[p];
             sm.ck[p] = tk;
-            const double te = sm.ce[i];
+            const float2 te = sm.ce[i];
             sm.ce[i] = sm.ce[p];
             sm.ce[p] = te;
             const int32_t ti = sm.cid[i];
@@ -490,36 +759,48 @@ __device__ void sort_list(PickSmem& sm, int n, bool by_id) {
   }
 }
 
+__device__ __forceinline__ unsigned long long fix_target(df tm, double slack) {
+  const double v = dbl_of(tm) * kFix + slack;
+  return v <= 0.0 ? 0ull : (v >= 1.8e19 ? ~0ull : (unsigned long long)v);
+}
+
 // Gather, into shared memory and sorted, the stretch of the order where a
 // cumulative target is reached: count target `tc` elements, or e' mass `tm`,
 // over the elements allowed by `lim`.  Level 0 uses the bucket histogram in
 // sm.hc/hm (already restricted).  Returns the frame of the list.
-__device__ Frame gather(PickSmem& sm, int kind, long long tc, double tm, const Lim& lim, const uint16_t* bins,
-                        const double* W, const double* E, int V, uint32_t* status) {
+__device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& lim, const uint16_t* bins,
+                        const uint64_t* K, const float2* E, int V, uint32_t* status) {
   const int t = threadIdx.x;
   __shared__ int s_lo, s_hi;
   __shared__ long long s_cnt_hi, s_cnt_before;
   __shared__ unsigned long long s_m_before;
+  const unsigned long long lo_u = kind == kMass ? fix_target(tm, -kFixTol) : 0ull;
+  const unsigned long long hi_u = kind == kMass ? fix_target(tm, kFixTol) : 0ull;
+  const unsigned long long mid_u = kind == kMass ? fix_target(tm, 0.0) : 0ull;
   // ---- level 0: cumulative bucket counts and masses, two buckets per thread
   {
     const uint32_t c0 = sm.hc[2 * t], c1 = sm.hc[2 * t + 1];
     const unsigned long long m0 = sm.hm[2 * t], m1 = sm.hm[2 * t + 1];
     unsigned long long ctot, mtot;
-    const unsigned long long cinc = block_scan<unsigned long long>((unsigned long long)c0 + c1, sm.redu, ctot);
-    const unsigned long long minc = block_scan<unsigned long long>(m0 + m1, sm.redu, mtot);
+    const unsigned long long cinc = block_scan<unsigned long long>((unsigned long long)c0 + c1, sm.redk, ctot);
+    const unsigned long long minc = block_scan<unsigned long long>(m0 + m1, sm.redk, mtot);
     const unsigned long long cb0 = cinc - c0 - c1, mb0 = minc - m0 - m1;  // before bucket 2t
     const unsigned long long ca0 = cb0 + c0, ma0 = mb0 + m0;              // through bucket 2t
     if (t == 0) s_lo = kBins - 1, s_hi = kBins - 1;
     __syncthreads();
     if (kind == kCount) {
-      if (ca0 >= (unsigned long long)tc && cb0 < (unsigned long long)tc) atomicMin(&s_lo, 2 * t);
-      if (cinc >= (unsigned long long)tc && ca0 < (unsigned long long)tc) atomicMin(&s_lo, 2 * t + 1);
+      const unsigned long long tcu = (unsigned long long)tc;
+      if (ca0 >= tcu && cb0 < tcu) atomicMin(&s_lo, 2 * t);
+      if (cinc >= tcu && ca0 < tcu) atomicMin(&s_lo, 2 * t + 1);
     } else {
-      const double lo_t = tm * kFix - kFixTol, hi_t = tm * kFix + kFixTol;
-      if ((double)ma0 >= lo_t) atomicMin(&s_lo, 2 * t);
-      else if ((double)minc >= lo_t) atomicMin(&s_lo, 2 * t + 1);
-      if ((double)ma0 >= hi_t) atomicMin(&s_hi, 2 * t);
-      else if ((double)minc >= hi_t) atomicMin(&s_hi, 2 * t + 1);
+      if (ma0 >= lo_u)
+        atomicMin(&s_lo, 2 * t);
+      else if (minc >= lo_u)
+        atomicMin(&s_lo, 2 * t + 1);
+      if (ma0 >= hi_u)
+        atomicMin(&s_hi, 2 * t);
+      else if (minc >= hi_u)
+        atomicMin(&s_hi, 2 * t + 1);
     }
     __syncthreads();
     if (kind == kCount && t == 0) s_hi = s_lo;
@@ -545,27 +826,27 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, double tm, const L
   int shift = 96;
   unsigned __int128 pre = 0;
   long long r_above = cnt_before;
-  unsigned long long r_mabove = s_m_before;
   if (mode == 2) {
+    __shared__ int s_d;
+    __shared__ long long s_above;
+    __shared__ unsigned long long s_mabove;
+    unsigned long long r_mabove = s_m_before;
     while (true) {
       for (int i = t; i < 256; i += kPick) sm.hc[i] = 0, sm.hm[i] = 0;
       __syncthreads();
       for (int i = t; i < V; i += kPick) {
         const int bn = bins[i];
         if (bn < lo || bn > hi) continue;
-        const uint64_t k = okey(W[i]);
+        const uint64_t k = K[i];
         if (!in_lim(lim, bn, k, i)) continue;
-        const unsigned __int128 K = ckey(k, i);
-        if (shift < 96 && (K >> shift) != pre) continue;
-        const int d = (int)((K >> (shift - 8)) & 255);
+        const unsigned __int128 Kc = ckey(k, i);
+        if (shift < 96 && (Kc >> shift) != pre) continue;
+        const int d = (int)((Kc >> (shift - 8)) & 255);
         atomicAdd(&sm.hc[d], 1u);
-        if (kind == kMass) atomicAdd(&sm.hm[d], (unsigned long long)__double2ull_rn(E[i] * kFix));
+        if (kind == kMass) atomicAdd(&sm.hm[d], fix_of(E[i]));
       }
       __syncthreads();
       // walk digits from 255 (earliest) down: one thread, 256 steps
-      __shared__ int s_d;
-      __shared__ long long s_above;
-      __shared__ unsigned long long s_mabove;
       if (t == 0) {
         long long c = r_above;
         unsigned long long m = r_mabove;
@@ -575,7 +856,7 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, double tm, const L
           last = d;
           const long long c2 = c + sm.hc[d];
           const unsigned long long m2 = m + sm.hm[d];
-          const bool hit = kind == kCount ? c2 >= tc : (double)m2 >= tm * kFix;
+          const bool hit = kind == kCount ? c2 >= tc : m2 >= mid_u;
           if (hit) {
             pick = d;
             break;
@@ -611,47 +892,36 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, double tm, const L
   // ---- gather
   if (t == 0) sm.n = 0;
   __syncthreads();
-  double msum = 0.0;
+  df msum = mk(0.0f, 0.0f);
   for (int i = t; i < V; i += kPick) {
     const int bn = bins[i];
     if (bn > hi) continue;
-    bool take;
     if (mode == 0) {
-      if (lim.on && bn == lim.bin) {
-        const uint64_t k = okey(W[i]);
-        take = in_lim(lim, bn, k, i);
-        if (take) {
-          const int slot = atomicAdd(&sm.n, 1);
-          if (slot < kCap) sm.ck[slot] = k, sm.ce[slot] = E[i], sm.cid[slot] = i;
-        }
-        continue;
-      }
-      take = in_lim(lim, bn, 0, i);
+      const uint64_t k = K[i];
+      if (!in_lim(lim, bn, k, i)) continue;
     } else if (bn < lo) {
-      if (in_lim(lim, bn, 0, i)) msum += E[i];  // wholly before the list
+      if (in_lim(lim, bn, 0, i)) {  // wholly before the list
+        const float2 e = E[i];
+        msum = df_add(msum, mk(e.x, e.y));
+      }
       continue;
     } else {
-      const uint64_t k = okey(W[i]);
+      const uint64_t k = K[i];
       if (!in_lim(lim, bn, k, i)) continue;
       if (mode == 2) {
-        const unsigned __int128 K = ckey(k, i);
-        const unsigned __int128 top = K >> shift;
-        if (top > pre) {
-          msum += E[i];  // inside the buckets, before the list
+        const unsigned __int128 top = ckey(k, i) >> shift;
+        if (top > pre) {  // inside the buckets, before the list
+          const float2 e = E[i];
+          msum = df_add(msum, mk(e.x, e.y));
           continue;
         }
         if (top < pre) continue;
       }
-      const int slot = atomicAdd(&sm.n, 1);
-      if (slot < kCap) sm.ck[slot] = k, sm.ce[slot] = E[i], sm.cid[slot] = i;
-      continue;
     }
-    if (take) {
-      const int slot = atomicAdd(&sm.n, 1);
-      if (slot < kCap) sm.ck[slot] = okey(W[i]), sm.ce[slot] = E[i], sm.cid[slot] = i;
-    }
+    const int slot = atomicAdd(&sm.n, 1);
+    if (slot < kCap) sm.ck[slot] = K[i], sm.ce[slot] = E[i], sm.cid[slot] = i;
   }
-  const double m_above = block_sum<kPick>(msum, sm.redd);
+  const df m_above = block_sum_df<kPick>(msum, sm.redd);
   __syncthreads();
   if (sm.n > kCap) {
     if (t == 0) atomicOr(status, (uint32_t)DEC_SAMPLE_OVERFLOW);
@@ -662,32 +932,31 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, double tm, const L
   sort_list(sm, sm.n, false);
   Frame f;
   f.above = mode == 0 ? 0 : (mode == 1 ? cnt_before : r_above);
-  f.m_above = mode == 0 ? 0.0 : m_above;
+  f.m_above = mode == 0 ? mk(0.0f, 0.0f) : m_above;
   return f;
 }
 
-// first list index j (< n) where above/Z + sum_{i<=j} ce_i/Z >= p; n-1 if never
-__device__ int walk_mass(PickSmem& sm, int n, double Z, double start, double p) {
+// first list index j (< n) where start + sum_{i<=j} ce_i >= target; n-1 if never
+__device__ int walk_mass(PickSmem& sm, int n, df start, df target) {
   const int t = threadIdx.x;
-  double v[4];
-  double run = 0.0;
+  df v[4];
+  df run = mk(0.0f, 0.0f);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int j = 4 * t + r;
-    const double qv = j < n ? sm.ce[j] / Z : 0.0;
-    run += qv;
+    if (j < n) run = df_add(run, ce_of(sm, j));
     v[r] = run;
   }
-  double total;
-  const double inc = block_scan<double>(run, sm.redd, total);
-  const double base = start + (inc - run);
+  df total;
+  const df inc = block_scan_df(run, sm.redd, total);
+  const df base = df_add(start, df_add(inc, mk(-run.h, -run.l)));  // start + exclusive prefix
   __shared__ int s_first;
   if (t == 0) s_first = n - 1;
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int j = 4 * t + r;
-    if (j < n && base + v[r] >= p) {
+    if (j < n && df_ge(df_add(base, v[r]), target)) {
       atomicMin(&s_first, j);
       break;
     }
@@ -699,24 +968,24 @@ __device__ int walk_mass(PickSmem& sm, int n, double Z, double start, double p) 
 }
 
 // sum of ce[0..n) (fixed tree)
-__device__ double list_sum(PickSmem& sm, int n) {
-  double v = 0.0;
+__device__ df list_sum(PickSmem& sm, int n) {
+  df v = mk(0.0f, 0.0f);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int j = 4 * threadIdx.x + r;
-    if (j < n) v += sm.ce[j];
+    if (j < n) v = df_add(v, ce_of(sm, j));
   }
-  return block_sum<kPick>(v, sm.redd);
+  return block_sum_df<kPick>(v, sm.redd);
 }
 
-__device__ double logprob_of(const float* x, const int32_t* mk, int id, const SeqParam& q, double M, double lse) {
+__device__ double logprob_of(const float* x, const int32_t* mkv, int id, const SeqParam& q, double M, double lse) {
   bool bad = false;
-  return (penalize(load_logit(x, id, bad), mk[id], q) - M) - lse;
+  return (penalize(load_logit(x, id, bad), mkv[id], q) - M) - lse;
 }
 
 // the bucket histogram of one sequence, restricted to the order prefix `lim` allows
 __device__ void load_hist(PickSmem& sm, const Lim& lim, const uint32_t* hc, const unsigned long long* hm,
-                          const uint16_t* bins, const double* W, const double* E, int V) {
+                          const uint16_t* bins, const uint64_t* K, const float2* E, int V) {
   const int t = threadIdx.x;
   for (int i = t; i < kBins; i += kPick) {
     const bool cut = lim.on && i > lim.bin;
@@ -734,7 +1003,7 @@ __device__ void load_hist(PickSmem& sm, const Lim& lim, const uint32_t* hc, cons
   unsigned long long m = 0;
   for (int i = t; i < V; i += kPick) {
     if (bins[i] != lim.bin) continue;
-    if (in_lim(lim, lim.bin, okey(W[i]), i)) ++c, m += __double2ull_rn(E[i] * kFix);
+    if (in_lim(lim, lim.bin, K[i], i)) ++c, m += fix_of(E[i]);
   }
   atomicAdd(&s_c, c);
   atomicAdd(&s_m, m);
@@ -747,7 +1016,7 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
                                                     const int32_t* __restrict__ marks,
                                                     const SeqParam* __restrict__ sp, int V, int NB,
                                                     const Part1* __restrict__ part1, const Part2* __restrict__ part2,
-                                                    const double* __restrict__ Wall, const double* __restrict__ Eall,
+                                                    const uint64_t* __restrict__ Kall, const float2* __restrict__ Eall,
                                                     const uint16_t* __restrict__ ball, const uint32_t* __restrict__ hcnt,
                                                     const unsigned long long* __restrict__ hmass,
                                                     PickState* __restrict__ state, dec_rng* __restrict__ rng,
@@ -755,25 +1024,39 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
                                                     uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PickSmem& sm = *reinterpret_cast<PickSmem*>(smem_raw);
+  __shared__ double s_M, s_lse;
   const int s = blockIdx.x, t = threadIdx.x;
-  const SeqParam q = sp[s];
+  const SeqParam& q = sp[s];
   const float* x = logits + (size_t)s * ld;
-  const int32_t* mk = marks + (size_t)s * V;
+  const int32_t* mkv = marks + (size_t)s * V;
   const size_t row = (size_t)s * V;
-  const double* W = Wall + row;
-  const double* E = Eall + row;
+  const uint64_t* K = Kall + row;
+  const float2* E = Eall + row;
   const uint16_t* bins = ball + row;
 
-  double M, mn;
+  uint64_t Mk;
   int arg;
-  reduce_part1<kPick>(part1 + (size_t)s * NB, NB, M, arg, mn, sm.redd, sm.redi);
+  float mn;
+  reduce_part1<kPick>(part1 + (size_t)s * NB, NB, Mk, arg, mn, sm.redk, sm.redi, sm.redf);
+  Part2 pz;
+  pz.zh = pz.zl = pz.z2h = pz.z2l = 0.0f;
+  if (t < NB) pz = part2[(size_t)s * NB + t];
+  const df Z = block_sum_df<kPick>(mk(pz.zh, pz.zl), sm.redd);
+  const df Zall = block_sum_df<kPick>(mk(pz.z2h, pz.z2l), sm.redd);
+  if (t == 0) {  // the only f64 transcendental: one logarithm per sequence
+    s_M = key_value(Mk);
+    s_lse = log(dbl_of(Z));
+  }
+  __syncthreads();
+  const double M = s_M, lse = s_lse;
   PickState st;
   st.mode = 0;
   st.has_last = 0;
   st.last_id = 0;
   st.pad = 0;
   st.last_key = 0;
-  st.emin_bits = 0;
+  st.M = M;
+  st.lse = lse;
   if (!(M > -INFINITY)) {  // flagged by k_scan2
     if (t == 0) {
       tokens[s] = -1;
@@ -782,12 +1065,6 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     }
     return;
   }
-  const Part2 pz = t < NB ? part2[(size_t)s * NB + t] : Part2{0.0, 0.0};
-  const double Z = block_sum<kPick>(pz.se, sm.redd);
-  const double Zall = block_sum<kPick>(pz.se2, sm.redd);
-  const double lse = log(Z);
-  st.M = M;
-  st.lse = lse;
   if (q.T == 0.0) {  // greedy: no draw
     if (t == 0) {
       tokens[s] = arg;
@@ -799,20 +1076,27 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
   const long long kk = (q.top_k > 0 && q.top_k < V) ? q.top_k : V;
   const bool p_on = q.top_p < 1.0;
   const bool m_on = q.min_p > 0.0;
+  const df minp = mk(q.mph, q.mpl);
 
   // the list: (has_list) sm holds n sorted elements starting `above` into the order;
-  // the kept prefix ends at list index `end` (or, without a list, at the set's end)
+  // the kept prefix ends at list index `end`
   bool has_list = false;
   int n = 0, end = -1;
-  Frame fr{0, 0.0};
-  double Zk = Zall;
-  Lim none{0, 0, 0, 0};
+  Frame fr;
+  fr.above = 0;
+  fr.m_above = mk(0.0f, 0.0f);
+  df Zk = Zall;
+  Lim none;
+  none.on = 0;
+  none.key = 0;
+  none.id = 0;
+  none.bin = 0;
 
   // ---- top-k
   Lim klim = none;
   if (kk < V) {
-    load_hist(sm, none, hcnt + (size_t)s * kBins, hmass + (size_t)s * kBins, bins, W, E, V);
-    fr = gather(sm, kCount, kk, 0.0, none, bins, W, E, V, status);
+    load_hist(sm, none, hcnt + (size_t)s * kBins, hmass + (size_t)s * kBins, bins, K, E, V);
+    fr = gather(sm, kCount, kk, mk(0.0f, 0.0f), none, bins, K, E, V, status);
     has_list = true;
     n = sm.n;
     if (n == 0) {  // cannot happen: the bucket walk found the k-th element
@@ -822,9 +1106,7 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     end = (int)(kk - fr.above - 1);
     if (end >= n) end = n - 1;  // cannot happen unless capacity overflowed
     if (end < 0) end = 0;
-    // Zk: e' over the top-k set
-    const double in_list = list_sum(sm, end + 1);
-    Zk = fr.m_above + in_list;
+    Zk = df_add(fr.m_above, list_sum(sm, end + 1));
     klim.on = 1;
     klim.key = sm.ck[end];
     klim.id = sm.cid[end];
@@ -832,79 +1114,69 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     __syncthreads();
   }
 
-  // ---- nucleus
+  // ---- nucleus: the running e' sum reaches p * Zk
   if (p_on) {
+    const df target = df_mul(mk(q.pph, q.ppl), Zk);
     if (has_list && fr.above == 0) {
-      end = walk_mass(sm, end + 1, Zk, 0.0, q.top_p);
+      end = walk_mass(sm, end + 1, mk(0.0f, 0.0f), target);
     } else {
-      load_hist(sm, klim, hcnt + (size_t)s * kBins, hmass + (size_t)s * kBins, bins, W, E, V);
-      fr = gather(sm, kMass, 0, q.top_p * Zk, klim, bins, W, E, V, status);
+      load_hist(sm, klim, hcnt + (size_t)s * kBins, hmass + (size_t)s * kBins, bins, K, E, V);
+      fr = gather(sm, kMass, 0, target, klim, bins, K, E, V, status);
       has_list = true;
       n = sm.n;
       if (n == 0) {  // cannot happen: the restricted set holds at least the top
         if (t == 0) atomicOr(status, (uint32_t)DEC_SAMPLE_OVERFLOW), tokens[s] = arg, logprobs[s] = -lse, state[s] = st;
         return;
       }
-      end = walk_mass(sm, n, Zk, fr.m_above / Zk, q.top_p);
+      end = walk_mass(sm, n, fr.m_above, target);
     }
   }
 
-  // ---- min-p: q_i >= min_p * q_top, q_top = e'_top / Zk = 1 / Zk; as a bound on e'
-  double emin = 0.0;
-  if (m_on) {
-    const double bound = q.min_p * (1.0 / Zk);
-    double e = bound * Zk;
-    if (e > 1.0) e = 1.0;
-    for (int it = 0; it < 64 && e > 0.0 && nextafter(e, 0.0) / Zk >= bound; ++it) e = nextafter(e, 0.0);
-    for (int it = 0; it < 64 && e / Zk < bound; ++it) e = nextafter(e, 2.0);
-    emin = e;
-  }
-
-  // ---- final: in shared memory when the whole kept set is the list's head
+  // ---- final: in shared memory when the whole kept set is the list's head.
+  // min-p keeps e' >= min_p (e' of the top id is exactly 1)
   const bool whole = has_list && fr.above == 0;
   if (whole) {
     int nf = end + 1;
     if (m_on) {
       __shared__ int s_nf;
-      if (t == 0) s_nf = 0;
+      if (t == 0) s_nf = 1;
       __syncthreads();
       for (int j = t; j < nf; j += kPick)
-        if (sm.ce[j] >= emin) atomicMax(&s_nf, j + 1);
+        if (df_ge(ce_of(sm, j), minp)) atomicMax(&s_nf, j + 1);
       __syncthreads();
       nf = s_nf;
       __syncthreads();
     }
     sort_list(sm, nf, true);  // ascending ids
-    const double Zf = list_sum(sm, nf);
+    const df Zf = list_sum(sm, nf);
     __shared__ double s_u;
     __shared__ uint64_t s_state;
     if (t == 0) {
-      dec_rng r = rng[s];
+      const dec_rng r = rng[s];
       uint64_t stt = r.state;
       s_u = pcg_uniform(stt, r.inc);
       s_state = stt;
     }
     __syncthreads();
-    const double u = s_u;
-    // CDF in ascending id order: first j with u < c_j
-    double v[4];
-    double run = 0.0;
+    const df target = df_mul(df_of(s_u), Zf);  // u < c_j  <=>  u * Zf < running e' sum
+    df v[4];
+    df run = mk(0.0f, 0.0f);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int j = 4 * t + r;
-      run += j < nf ? sm.ce[j] / Zf : 0.0;
+      if (j < nf) run = df_add(run, ce_of(sm, j));
       v[r] = run;
     }
-    double total;
-    const double inc = block_scan<double>(run, sm.redd, total);
-    const double base = inc - run;
+    df total;
+    const df inc = block_scan_df(run, sm.redd, total);
+    const df base = df_add(inc, mk(-run.h, -run.l));
     __shared__ int s_tok;
     if (t == 0) s_tok = nf - 1;
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int j = 4 * t + r;
-      if (j < nf && u < base + v[r]) {
+      if (j < nf && df_gt(df_add(base, v[r]), target)) {
         atomicMin(&s_tok, j);
         break;
       }
@@ -913,114 +1185,126 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     if (t == 0) {
       const int tok = sm.cid[s_tok];
       tokens[s] = tok;
-      logprobs[s] = logprob_of(x, mk, tok, q, M, lse);
+      logprobs[s] = logprob_of(x, mkv, tok, q, M, lse);
       rng[s].state = s_state;
       state[s] = st;
     }
     return;
   }
-  // ---- hand-off: the kept set is the order prefix through `last` with e' >= emin
+  // ---- hand-off: the kept set is the order prefix through `last` with e' >= min_p
   if (t == 0) {
     st.mode = 1;
     st.has_last = has_list ? 1 : 0;
     if (has_list) st.last_key = sm.ck[end], st.last_id = sm.cid[end];
-    st.emin_bits = (uint64_t)__double_as_longlong(emin);
     state[s] = st;
   }
 }
 
-__device__ __forceinline__ bool kept_by(const PickState& st, double w, double e, int i) {
-  if (st.has_last && before(st.last_key, st.last_id, okey(w), i)) return false;
-  return (uint64_t)__double_as_longlong(e) >= st.emin_bits;  // e' >= 0: bit order is value order
+__device__ __forceinline__ bool kept_by(const PickState& st, const SeqParam& q, uint64_t k, float2 e, int i) {
+  if (st.has_last && before(st.last_key, st.last_id, k, i)) return false;
+  return !(q.min_p > 0.0) || df_ge(mk(e.x, e.y), mk(q.mph, q.mpl));
 }
 
-__global__ void __launch_bounds__(kScanThreads) k_final_sum(const PickState* __restrict__ state, int V, int NB,
-                                                             const double* __restrict__ Wall,
-                                                             const double* __restrict__ Eall,
-                                                             double* __restrict__ fsum) {
-  __shared__ double red[32];
+__global__ void __launch_bounds__(kScanThreads) k_final_sum(const SeqParam* __restrict__ sp,
+                                                             const PickState* __restrict__ state, int V, int NB,
+                                                             const uint64_t* __restrict__ Kall,
+                                                             const float2* __restrict__ Eall,
+                                                             float2* __restrict__ fsum) {
+  __shared__ float2 red[32];
   const int s = blockIdx.y, b = blockIdx.x, t = threadIdx.x;
   const PickState st = state[s];
   if (st.mode == 0) return;
+  const SeqParam& q = sp[s];
   const size_t row = (size_t)s * V;
-  double v = 0.0;
+  df v = mk(0.0f, 0.0f);
 #pragma unroll
   for (int j = 0; j < kChunk / kScanThreads; ++j) {
     const int i = b * kChunk + j * kScanThreads + t;
     if (i < V) {
-      const double e = Eall[row + i];
-      if (kept_by(st, Wall[row + i], e, i)) v += e;
+      const float2 e = Eall[row + i];
+      if (kept_by(st, q, Kall[row + i], e, i)) v = df_add(v, mk(e.x, e.y));
     }
   }
-  v = block_sum<kScanThreads>(v, red);
-  if (t == 0) fsum[(size_t)s * NB + b] = v;
+  v = block_sum_df<kScanThreads>(v, red);
+  if (t == 0) fsum[(size_t)s * NB + b] = make_float2(v.h, v.l);
 }
 
 __global__ void __launch_bounds__(kPick, 1) k_final_pick(const float* __restrict__ logits, int64_t ld,
                                                           const int32_t* __restrict__ marks,
                                                           const SeqParam* __restrict__ sp,
                                                           const PickState* __restrict__ state, int V, int NB,
-                                                          const double* __restrict__ Wall,
-                                                          const double* __restrict__ Eall,
-                                                          const double* __restrict__ fsum, dec_rng* __restrict__ rng,
+                                                          const uint64_t* __restrict__ Kall,
+                                                          const float2* __restrict__ Eall,
+                                                          const float2* __restrict__ fsum, dec_rng* __restrict__ rng,
                                                           int32_t* __restrict__ tokens, double* __restrict__ logprobs) {
-  __shared__ double redd[32];
+  __shared__ float2 redd[32];
   __shared__ double s_u;
   __shared__ uint64_t s_state;
-  __shared__ int s_chunk, s_tok, s_last;
+  __shared__ int s_chunk, s_tok, s_last, s_lastid;
+  __shared__ float2 s_base;
   const int s = blockIdx.x, t = threadIdx.x;
   const PickState st = state[s];
   if (st.mode == 0) return;
-  const SeqParam q = sp[s];
+  const SeqParam& q = sp[s];
   const size_t row = (size_t)s * V;
-  const double fs = t < NB ? fsum[(size_t)s * NB + t] : 0.0;
-  const double Zf = block_sum<kPick>(fs, redd);
-  double tot;
-  const double cinc = block_scan<double>(t < NB ? fs / Zf : 0.0, redd, tot);
+  float2 f2 = make_float2(0.f, 0.f);
+  if (t < NB) f2 = fsum[(size_t)s * NB + t];
+  const df fs = mk(f2.x, f2.y);
+  const df Zf = block_sum_df<kPick>(fs, redd);
+  df tot;
+  const df cinc = block_scan_df(fs, redd, tot);
   if (t == 0) {
-    dec_rng r = rng[s];
+    const dec_rng r = rng[s];
     uint64_t stt = r.state;
     s_u = pcg_uniform(stt, r.inc);
     s_state = stt;
     s_chunk = NB;
     s_last = -1;
     s_tok = 0x7fffffff;
+    s_lastid = -1;
   }
   __syncthreads();
-  const double u = s_u;
-  if (t < NB && u < cinc) atomicMin(&s_chunk, t);
-  if (t < NB && fs > 0.0) atomicMax(&s_last, t);
+  const df target = df_mul(df_of(s_u), Zf);  // u < c  <=>  u * Zf < running e' sum
+  if (t < NB && df_gt(cinc, target)) atomicMin(&s_chunk, t);
+  if (t < NB && fs.h > 0.0f) atomicMax(&s_last, t);
   __syncthreads();
   int c = s_chunk;
-  const bool past_end = c >= NB;  // rounding left the total at or below u
+  const bool past_end = c >= NB;  // rounding left the total at or below u * Zf
   if (past_end) c = s_last;
+  if (t == c) {
+    const df b0 = df_add(cinc, mk(-fs.h, -fs.l));  // running sum before chunk c
+    s_base = make_float2(b0.h, b0.l);
+  }
+  __syncthreads();
+  const df base = mk(s_base.x, s_base.y);
   // the chunk: one element per thread, in ascending ids
   const int i = c * kChunk + t;
-  double p = 0.0;
+  df p = mk(0.0f, 0.0f);
   bool kept = false;
   if (i < V) {
-    const double e = Eall[row + i];
-    kept = kept_by(st, Wall[row + i], e, i);
-    if (kept) p = e / Zf;
+    const float2 e = Eall[row + i];
+    kept = kept_by(st, q, Kall[row + i], e, i);
+    if (kept) p = mk(e.x, e.y);
   }
-  __shared__ double s_base;
-  __shared__ int s_lastid;
-  if (t == c) s_base = cinc - (fs / Zf);  // cumulative before chunk c
-  if (t == 0) s_lastid = -1;
-  __syncthreads();
-  const double base = s_base;
-  double ctot;
-  const double cin = block_scan<double>(p, redd, ctot);
-  if (!past_end && kept && u < base + cin) atomicMin(&s_tok, i);
+  df ctot;
+  const df cin = block_scan_df(p, redd, ctot);
+  if (!past_end && kept && df_gt(df_add(base, cin), target)) atomicMin(&s_tok, i);
   if (kept) atomicMax(&s_lastid, i);
   __syncthreads();
   if (t == 0) {
-    // nothing passed u in the chunk (rounding): its last kept id
+    // nothing passed u here (rounding): the chunk's last kept id
     const int tok = s_tok != 0x7fffffff ? s_tok : s_lastid;
     tokens[s] = tok;
     logprobs[s] = tok >= 0 ? logprob_of(logits + (size_t)s * ld, marks + row, tok, q, st.M, st.lse) : -INFINITY;
     rng[s].state = s_state;
   }
+}
+
+// ---- test hook: the double-f32 exponential on n device values --------------------------------
+
+__global__ void k_df_exp(const double* __restrict__ x, double* __restrict__ y, int64_t n) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = dbl_of(df_exp(df_of(x[i])));
 }
 
 }  // namespace
@@ -1203,6 +1487,15 @@ int dec_sample(dec_sampler* s, const float* logits, int64_t ld, int32_t n, const
     q.pres = p.presence_penalty;
     q.freq = p.frequency_penalty;
     q.top_k = p.top_k;
+    q.pad0 = q.pad1 = 0;
+    // 1/T, top_p and min_p as float head + tail (long double division where the host has it)
+    const long double rT = p.temperature > 0.0 ? 1.0L / (long double)p.temperature : 0.0L;
+    q.rTh = (float)rT;
+    q.rTl = (float)(rT - (long double)q.rTh);
+    q.pph = (float)p.top_p;
+    q.ppl = (float)(p.top_p - (double)q.pph);
+    q.mph = (float)p.min_p;
+    q.mpl = (float)(p.min_p - (double)q.mph);
     q.hist_off = history_offsets ? history_offsets[i] : 0;
     q.n_hist = history_offsets ? history_offsets[i + 1] - history_offsets[i] : 0;
     q.n_prompt = n_prompt ? n_prompt[i] : 0;
@@ -1218,23 +1511,31 @@ int dec_sample(dec_sampler* s, const float* logits, int64_t ld, int32_t n, const
   const int V = s->V, NB = s->NB;
   Part1* p1 = (Part1*)(w + s->L.part1);
   Part2* p2 = (Part2*)(w + s->L.part2);
-  double* W = (double*)(w + s->L.W);
-  double* E = (double*)(w + s->L.E);
+  uint64_t* K = (uint64_t*)(w + s->L.K);
+  float2* E = (float2*)(w + s->L.E);
   uint16_t* bins = (uint16_t*)(w + s->L.bins);
   uint32_t* hc = (uint32_t*)(w + s->L.hcnt);
   unsigned long long* hm = (unsigned long long*)(w + s->L.hmass);
   PickState* ps = (PickState*)(w + s->L.state);
-  double* fsum = (double*)(w + s->L.fsum);
+  float2* fsum = (float2*)(w + s->L.fsum);
   const dim3 hgrid((max_hist + 255) / 256, n);
   if (max_hist > 0) k_mark<<<hgrid, 256, 0, st>>>(dsp, history, marks, V, 1, status);
   const dim3 grid(NB, n);
   k_scan1<<<grid, kScanThreads, 0, st>>>(logits, ld, marks, dsp, V, NB, p1, status);
-  k_scan2<<<grid, kScanThreads, 0, st>>>(logits, ld, marks, dsp, V, NB, p1, p2, W, E, bins, hc, hm, status);
-  k_pick<<<n, kPick, sizeof(PickSmem), st>>>(logits, ld, marks, dsp, V, NB, p1, p2, W, E, bins, hc, hm, ps, rng, tokens,
+  k_scan2<<<grid, kScanThreads, 0, st>>>(logits, ld, marks, dsp, V, NB, p1, p2, K, E, bins, hc, hm, status);
+  k_pick<<<n, kPick, sizeof(PickSmem), st>>>(logits, ld, marks, dsp, V, NB, p1, p2, K, E, bins, hc, hm, ps, rng, tokens,
                                              logprobs, status);
-  k_final_sum<<<grid, kScanThreads, 0, st>>>(ps, V, NB, W, E, fsum);
-  k_final_pick<<<n, kPick, 0, st>>>(logits, ld, marks, dsp, ps, V, NB, W, E, fsum, rng, tokens, logprobs);
+  k_final_sum<<<grid, kScanThreads, 0, st>>>(dsp, ps, V, NB, K, E, fsum);
+  k_final_pick<<<n, kPick, 0, st>>>(logits, ld, marks, dsp, ps, V, NB, K, E, fsum, rng, tokens, logprobs);
   if (max_hist > 0) k_mark<<<hgrid, 256, 0, st>>>(dsp, history, marks, V, 0, status);
+  S_CUDA(cudaGetLastError());
+  return DEC_OK;
+}
+
+int dec_debug_df_exp(const double* x, double* y, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return sfail(DEC_EINVAL, "bad arguments");
+  if (n == 0) return DEC_OK;
+  k_df_exp<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(x, y, n);
   S_CUDA(cudaGetLastError());
   return DEC_OK;
 }

@@ -32,7 +32,7 @@ EXPORTS = (
     "dec_set_tensor_cores", "dec_debug_product", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc",
     "dec_prefix_key", "dec_pool_set_fill", "dec_pool_register", "dec_pool_lookup", "dec_pool_cached_blocks",
     "dec_child_seed", "dec_rng_stream", "dec_rng_next_u32", "dec_rng_uniform", "dec_sampler_workspace_bytes",
-    "dec_sampler_create", "dec_sampler_destroy", "dec_sampler_status", "dec_sample",
+    "dec_sampler_create", "dec_sampler_destroy", "dec_sampler_status", "dec_sample", "dec_debug_df_exp",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax",
                   "step")
@@ -132,6 +132,7 @@ def lib() -> C.CDLL:
             "dec_sampler_destroy": (None, [V]),
             "dec_sampler_status": (I, [V, C.POINTER(C.c_uint32)]),
             "dec_sample": (I, [V, V, I64, C.c_int32, C.POINTER(dec_sampling), V, _I32P, _I32P, V, V, V, V]),
+            "dec_debug_df_exp": (I, [V, V, I64, V]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

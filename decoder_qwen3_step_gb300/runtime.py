@@ -258,6 +258,23 @@ def sampling_params(temperature=1.0, top_k=0, top_p=1.0, min_p=0.0, repetition_p
                             float(presence_penalty), float(frequency_penalty))
 
 
+class DeviceHistory:
+    """Prompt and output ids of a batch, already on the device (a serving loop
+    appends each step's tokens there): ids [total] int32 on the device, host
+    offsets [n + 1] and prompt counts [n]."""
+
+    def __init__(self, histories, device="cuda"):
+        flat, offs, npr = [], [0], []
+        for pr, ou in histories:
+            flat.extend(int(x) for x in pr)
+            flat.extend(int(x) for x in ou)
+            offs.append(len(flat))
+            npr.append(len(pr))
+        self.ids = torch.tensor(flat or [0], dtype=torch.int32, device=device)
+        self.offsets = _i32(offs)
+        self.n_prompt = _i32(npr or [0])
+
+
 class Sampler:
     """The device sampler (libdec's dec_sample) with its workspace from torch.
 
@@ -301,7 +318,9 @@ class Sampler:
         offs = _i32([0] * (n + 1))
         npr = _i32([0] * max(n, 1))
         hist = None
-        if histories is not None:
+        if isinstance(histories, DeviceHistory):
+            hist, offs, npr = histories.ids, histories.offsets, histories.n_prompt
+        elif histories is not None:
             flat = []
             for i, (pr, ou) in enumerate(histories):
                 flat.extend(int(x) for x in pr)

@@ -421,6 +421,11 @@ int dec_sample(dec_sampler* s, const float* logits, int64_t ld, int32_t n_seqs, 
                const int32_t* history, const int32_t* history_offsets, const int32_t* n_prompt, dec_rng* rng,
                int32_t* tokens, double* logprobs, void* stream);
 
+/* Test hook: the sampler's double-f32 exponential (float head + tail; Tang's
+ * table-driven method, accurate to about 2^-46 relative down to e^-60, 0 below
+ * e^-87) on n device doubles x <= 0, written as doubles (head + tail). */
+int dec_debug_df_exp(const double* x, double* y, int64_t n, void* stream);
+
 /* Library version string. */
 const char* dec_version(void);
 

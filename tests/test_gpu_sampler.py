@@ -12,6 +12,7 @@ against p, a probability against the min-p bound) the device may decide the
 other way; such cases only have to return a kept id, and must stay rare.
 """
 
+import ctypes as C
 import math
 
 import numpy as np
@@ -61,6 +62,31 @@ def run_and_compare(sampler, logits, params, histories, seeds, label, exact=Fals
         assert abs(lp[i] - t["logprob"]) <= LP_TOL, where + f": logprob {lp[i]} vs {t['logprob']}"
     assert sampler.status() == 0
     return near
+
+
+def test_double_f32_exponential_against_f64():
+    """The sampler's exponential (double-f32, table-driven) against the f64
+    one: relative error at most 2^-44 down to e^-60 (the double-f32 tail is a
+    normal float there), 2^-30 down to e^-80, 0 below e^-87."""
+    g = np.random.default_rng(1)
+    # arguments that are exact as a float head plus a float tail, as the sampler's l - M is
+    hi = np.concatenate([-g.exponential(3.0, 200000), -g.uniform(0, 87, 200000), -g.uniform(0, 1e-3, 20000)])
+    hi = hi.astype(np.float32)
+    lo = (g.uniform(-0.5, 0.5, hi.size) * np.spacing(np.abs(hi))).astype(np.float32)
+    x = np.concatenate([hi.astype(np.float64) + lo.astype(np.float64),
+                        np.array([0.0, -0.0, -1e-30, -1e-8, -1.0, -60.0, -86.9, -87.5, -700.0, -np.inf])])
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty_like(xd)
+    dec.check(dec.lib().dec_debug_df_exp(C.c_void_p(xd.data_ptr()), C.c_void_p(yd.data_ptr()), len(x), None),
+              "dec_debug_df_exp")
+    torch.cuda.synchronize()
+    y = yd.cpu().numpy()
+    ref = np.exp(x)
+    rel = np.abs(y - ref) / np.maximum(ref, 1e-300)
+    assert np.all(y[x == 0.0] == 1.0)  # exp(0) is exactly one: the top id's weight
+    assert rel[x >= -60].max() <= 2.0**-44, rel[x >= -60].max()
+    assert rel[(x < -60) & (x >= -80)].max() <= 2.0**-30
+    assert np.all(y[x < -87] == 0.0)
 
 
 def test_worked_example_on_the_device():
