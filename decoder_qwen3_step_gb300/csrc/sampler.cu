@@ -66,17 +66,22 @@
 
 namespace {
 
-constexpr int kChunk = 1024;       // elements per scan CTA (and per final chunk)
+constexpr int kChunk1 = 2048;      // elements per CTA of the maximum scan
+constexpr int kChunk = 1024;       // elements per CTA of the exp scan (and per final chunk)
 constexpr int kScanThreads = 256;  // 4 elements per thread
 constexpr int kBins = 2048;        // linear buckets of the logit
 constexpr int kCap = 4096;         // candidates held in shared memory
 constexpr int kPick = 1024;        // threads of the one-CTA kernels
 constexpr int kMaxChunks = 1024;   // chunks per sequence: vocab <= 2^20
-constexpr float kFixF = 35184372088832.0f;  // 2^45: fixed-point scale of bucket masses
+// bucket masses are exact fixed point: an integer word in units of 2^-45 and a
+// fraction word in units of 2^-90 (integer sums: the same bits in any order)
+constexpr int kFixBits = 45;
+constexpr float kFixF = 35184372088832.0f;  // 2^45
 constexpr double kFix = 35184372088832.0;
-constexpr double kFixTol = 33554432.0;      // 2^25 = 2^-20 in e' units: slack on mass buckets
+constexpr double kFixSlack = 4096.0;        // bucket-walk slack, in 2^-45 units
 constexpr uint64_t kPcgMult = 6364136223846793005ull;
 constexpr int kStage = 4;
+enum { kSampling = 1, kUnitT = 2, kTopP = 4, kMinP = 8 };
 static_assert(kBins == 2 * kPick, "the bucket scan takes two buckets per thread");
 static_assert(kCap == 4 * kPick, "list scans take four candidates per thread");
 
@@ -85,13 +90,21 @@ struct SeqParam {  // 96 bytes, one per sequence
   float rTh, rTl;  // 1/T as head + tail
   float pph, ppl;  // top_p
   float mph, mpl;  // min_p
-  int32_t top_k, pad0;
+  int32_t top_k;
+  int32_t flags;   // kSampling | kUnitT | kTopP | kMinP, set on the host: no f64 compare on the device
   int32_t hist_off, n_hist, n_prompt, pad1;
 };
 
 struct Part1 {
   uint64_t key;
   float mn;
+  int32_t arg;
+};
+
+struct Stats {  // per sequence: the penalised maximum and the finite minimum
+  uint64_t key;
+  double M;
+  float mn, Mh, Ml;
   int32_t arg;
 };
 
@@ -109,13 +122,18 @@ struct PickState {  // hand-off from k_pick to the final kernels
 };
 
 struct Layout {
-  size_t seqs, marks, K, E, bins, part1, part2, hcnt, hmass, state, fsum, status, total;
+  size_t seqs, marks, K, E, bins, part1, stats, part2, hcnt, hmh, hml, state, fsum, status, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// rows of the per-id arrays are padded to 8 ids (16-byte loads of the buckets)
+int padded(int V) { return (V + 7) & ~7; }
+
 Layout layout_of(int V, int S) {
   const size_t NB = (size_t)(V + kChunk - 1) / kChunk;
+  const size_t NB1 = (size_t)(V + kChunk1 - 1) / kChunk1;
+  const size_t Vp = (size_t)padded(V);
   Layout L;
   size_t o = 0;
   auto take = [&o](size_t bytes) {
@@ -125,13 +143,15 @@ Layout layout_of(int V, int S) {
   };
   L.seqs = take((size_t)S * sizeof(SeqParam));
   L.marks = take((size_t)S * V * 4);
-  L.K = take((size_t)S * V * 8);
-  L.E = take((size_t)S * V * 8);
-  L.bins = take((size_t)S * V * 2);
-  L.part1 = take((size_t)S * NB * sizeof(Part1));
+  L.K = take((size_t)S * Vp * 8);
+  L.E = take((size_t)S * Vp * 8);
+  L.bins = take((size_t)S * Vp * 2);
+  L.part1 = take((size_t)S * NB1 * sizeof(Part1));
+  L.stats = take((size_t)S * sizeof(Stats));
   L.part2 = take((size_t)S * NB * sizeof(Part2));
   L.hcnt = take((size_t)S * kBins * 4);
-  L.hmass = take((size_t)S * kBins * 8);
+  L.hmh = take((size_t)S * kBins * 8);
+  L.hml = take((size_t)S * kBins * 8);
   L.state = take((size_t)S * sizeof(PickState));
   L.fsum = take((size_t)S * NB * sizeof(float2));
   L.status = take(256);
@@ -181,6 +201,20 @@ __device__ __forceinline__ df df_add(df a, df b) {
   return quick_two_sum(s.h, s.l);
 }
 
+// a + b where no leading digits cancel (same signs, or |b| far below |a|):
+// Dekker's shorter sum, error about 2^-47 relative
+__device__ __forceinline__ df df_add_fast(df a, df b) {
+  df s = two_sum(a.h, b.h);
+  s.l += a.l + b.l;
+  return quick_two_sum(s.h, s.l);
+}
+
+__device__ __forceinline__ df df_add_f(df a, float b) {  // a + b, b a float
+  df s = two_sum(a.h, b);
+  s.l += a.l;
+  return quick_two_sum(s.h, s.l);
+}
+
 __device__ __forceinline__ df df_mul(df a, df b) {
   df p = two_prod(a.h, b.h);
   p.l = fmaf(a.h, b.l, fmaf(a.l, b.h, p.l));
@@ -196,6 +230,36 @@ __device__ __forceinline__ df df_of(double x) {
 }
 
 __device__ __forceinline__ double dbl_of(df x) { return (double)x.h + (double)x.l; }
+
+// Rounding without conversion instructions (they issue on the f64 pipe here):
+// adding 1.5 * 2^23 rounds a float below 2^22 in magnitude to the nearest
+// integer, which then sits in the low mantissa bits.
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kMagicBits = 0x4B400000;
+
+// nearest integer (ties to even) of |x| < 2^22, as a float and an int
+__device__ __forceinline__ int round_i(float x, float& r) {
+  const float y = x + kMagic;
+  r = y - kMagic;
+  return __float_as_int(y) - kMagicBits;
+}
+
+// floor of |x| < 2^22, as a float and an int
+__device__ __forceinline__ int floor_i(float x, float& f) {
+  float y = x + kMagic;
+  f = y - kMagic;
+  int i = __float_as_int(y) - kMagicBits;
+  if (f > x) f -= 1.0f, --i;
+  return i;
+}
+
+// floor of 0 <= x < 2^23 (adding 2^23 leaves the integer part in the mantissa)
+__device__ __forceinline__ uint32_t floor_u(float x, float& f) {
+  float y = x + 8388608.0f;
+  f = y - 8388608.0f;
+  if (f > x) f -= 1.0f, y -= 1.0f;
+  return __float_as_uint(y) & 0x7FFFFFu;
+}
 
 // 2^(j/64) = head + tail, j = 0..63 (gen_exp_tables.py)
 __device__ const float2 kExp2Tab[64] = {
@@ -275,20 +339,23 @@ constexpr float k64OverLn2 = 0x1.7154760000000p+6f;
 // exp(x) for x <= 0 in double-f32 (Tang's table-driven method); 0 below -87
 __device__ __forceinline__ df df_exp(df x) {
   if (!(x.h > -87.0f)) return mk(0.0f, 0.0f);
-  const float kf = rintf(x.h * k64OverLn2);
-  const int k = (int)kf;
+  float kf;
+  const int k = round_i(x.h * k64OverLn2, kf);
   const float r0 = fmaf(-kf, kL1, x.h);  // exact: the two are within a factor of two
   df r = two_sum(r0, -kf * kL2);
-  r = df_add(r, mk(-kf * kL3, 0.0f));
-  r = df_add(r, mk(-kf * kL4, 0.0f));
-  r = df_add(r, mk(x.l, 0.0f));
-  // exp(r) = 1 + r + r^2/2 + (r^3/6 + r^4/24 + r^5/120); the bracket is below 3e-8
+  r = df_add_f(r, -kf * kL3);
+  r = df_add_f(r, -kf * kL4);
+  r = df_add_f(r, x.l);
+  // exp(r) = 1 + r + r^2/2 + (r^3/6 + r^4/24 + r^5/120); |r^2/2| <= |r|/360 and the
+  // bracket is below 3e-8, so no sum below cancels leading digits
   const df r2 = df_mul(r, r);
   const float rh = r.h;
   const float c = rh * rh * rh * (0.16666667f + rh * (0.041666668f + rh * 0.0083333338f));
-  df s = df_add(r, mk(0.5f * r2.h, 0.5f * r2.l));
-  s = df_add(s, mk(c, 0.0f));
-  df e = df_add(mk(1.0f, 0.0f), s);
+  df s = df_add_fast(r, mk(0.5f * r2.h, 0.5f * r2.l));
+  s = df_add_f(s, c);
+  df e = quick_two_sum(1.0f, s.h);
+  e.l += s.l;
+  e = quick_two_sum(e.h, e.l);
   const float2 t = kExp2Tab[k & 63];
   e = df_mul(e, mk(t.x, t.y));
   const float sc = __int_as_float(((k >> 6) + 127) << 23);  // 2^n, n >= -126
@@ -331,7 +398,9 @@ __device__ __forceinline__ uint64_t okey_f32(float x) {
   uint64_t b;
   if (e == 0) {
     if (m == 0) return 0x8000000000000000ull;  // +-0
-    b = (uint64_t)__double_as_longlong((double)x);  // subnormal: rare
+    // subnormal m * 2^-149: the top bit p of m sets the f64 exponent p - 149
+    const uint32_t pbit = 31u - (uint32_t)__clz(m);
+    b = ((uint64_t)(u >> 31) << 63) | ((uint64_t)(pbit + 874u) << 52) | ((uint64_t)(m ^ (1u << pbit)) << (52u - pbit));
   } else if (e == 0xFFu) {
     b = ((uint64_t)(u >> 31) << 63) | 0x7FF0000000000000ull | ((uint64_t)m << 29);
   } else {
@@ -354,8 +423,61 @@ __device__ __forceinline__ unsigned __int128 ckey(uint64_t k, int32_t id) {
   return ((unsigned __int128)k << 32) | (uint32_t)(~(uint32_t)id);
 }
 
-__device__ __forceinline__ unsigned long long fix_of(float2 e) {
-  return (unsigned long long)((long long)__float2ll_rn(e.x * kFixF) + (long long)__float2ll_rn(e.y * kFixF));
+struct Fix {
+  unsigned long long h, l;
+};
+
+// a float in [0, 2^45] as floor (an integer, from two 22/23-bit pieces) and its
+// exact fraction, with no conversion instructions
+__device__ __forceinline__ unsigned long long floor45(float x, float& frac) {
+  if (x >= 0x1p45f) {  // e' = 1 exactly
+    frac = 0.0f;
+    return 1ull << 45;
+  }
+  float a;
+  const uint32_t ai = floor_u(x * 0x1p-22f, a);  // < 2^23
+  const float r = fmaf(-a, 0x1p22f, x);           // exact, in [0, 2^22)
+  float b;
+  const uint32_t bi = floor_u(r, b);
+  frac = r - b;                                   // exact, in [0, 1)
+  return ((unsigned long long)ai << 22) + bi;
+}
+
+// a fraction f in [0, 1) in units of 2^-45, rounded: the same two-piece split
+__device__ __forceinline__ unsigned long long frac45(float f) {
+  float c;
+  const uint32_t ci = floor_u(f * 0x1p23f, c);  // < 2^23
+  const float r = fmaf(-c, 0x1p-23f, f);         // exact, in [0, 2^-23)
+  float rr;
+  const int ri = round_i(r * 0x1p45f, rr);       // <= 2^22
+  return ((unsigned long long)ci << 22) + (uint32_t)ri;
+}
+
+// e' (head + tail, >= 0) as fixed point: h units of 2^-45 plus l units of 2^-90
+__device__ __forceinline__ Fix fix_of(float2 e) {
+  const float xh = e.x * kFixF, xl = e.y * kFixF;  // exact scalings; |xl| <= 2^21
+  float fh, il;
+  const unsigned long long ih = floor45(xh, fh);
+  const int ili = floor_i(xl, il);
+  const float fl = xl - il;                        // exact, in [0, 1)
+  Fix f;
+  f.h = ih + (unsigned long long)(long long)ili;
+  f.l = frac45(fh) + frac45(fl);
+  return f;
+}
+
+__device__ __forceinline__ df u64_df(unsigned long long x) {  // x < 2^63
+  const float h = __ull2float_rn(x);
+  return mk(h, __ll2float_rn((long long)(x - (unsigned long long)h)));
+}
+
+// h * 2^-45 + l * 2^-90 as double-f32
+__device__ __forceinline__ df fix_df(unsigned long long h, unsigned long long l) {
+  h += l >> kFixBits;
+  l &= (1ull << kFixBits) - 1;
+  const df a = u64_df(h);
+  const float s = 1.0f / kFixF;
+  return df_add(mk(a.h * s, a.l * s), mk(__ull2float_rn(l) * (s * s), 0.0f));
 }
 
 __device__ __forceinline__ uint32_t pcg_next(uint64_t& state, uint64_t inc) {
@@ -493,6 +615,37 @@ __device__ df block_scan_df(df v, float2* red, df& total) {
   return df_add(v, off);
 }
 
+struct Pen {
+  uint64_t key;
+  float h, l;
+};
+
+// a penalised id (a rare branch: kept out of line so that its f64 work is
+// never issued, predicated off, for the other ids)
+__device__ __noinline__ Pen penalized_logit(float v, int32_t m, const SeqParam& q) {
+  const double d = penalize(v, m, q);
+  const df l = df_of(d);
+  Pen r;
+  r.key = okey(d);
+  r.h = l.h;
+  r.l = l.l;
+  return r;
+}
+
+// the penalised logit as a double-f32 pair, its order key and its float
+__device__ __forceinline__ void logit_of(float v, int32_t m, const SeqParam& q, df& l, uint64_t& key, float& lf) {
+  if (m == 0) {
+    l = mk(v, 0.0f);
+    key = okey_f32(v);
+    lf = v;
+  } else {
+    const Pen r = penalized_logit(v, m, q);
+    l = mk(r.h, r.l);
+    key = r.key;
+    lf = r.h;
+  }
+}
+
 // ---- history marks ----------------------------------------------------------------
 
 __global__ void k_mark(const SeqParam* __restrict__ sp, const int32_t* __restrict__ hist, int32_t* marks, int V,
@@ -532,22 +685,26 @@ __global__ void __launch_bounds__(kScanThreads) k_scan1(const float* __restrict_
   int ba = 0x7fffffff;
   float mn = INFINITY;
   bool bad = false;
+  constexpr int kPer = kChunk1 / kScanThreads;
+  float xv[kPer];
+  int32_t mv[kPer];
 #pragma unroll
-  for (int j = 0; j < kChunk / kScanThreads; ++j) {
-    const int i = b * kChunk + j * kScanThreads + t;
+  for (int j = 0; j < kPer; ++j) {  // every load first, then the work
+    const int i = b * kChunk1 + j * kScanThreads + t;
+    xv[j] = i < V ? x[i] : -INFINITY;
+    mv[j] = i < V ? mkv[i] : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = b * kChunk1 + j * kScanThreads + t;
     if (i < V) {
-      const float v = load_logit(x, i, bad);
-      const int32_t m = mkv[i];
+      float v = xv[j];
+      if (!(v < INFINITY)) bad = true, v = -INFINITY;  // NaN or +inf: flagged, read as -inf
+      const int32_t m = mv[j];
+      df l;
       uint64_t key;
       float lf;
-      if (m == 0) {
-        key = okey_f32(v);
-        lf = v;
-      } else {
-        const double l = penalize(v, m, q);
-        key = okey(l);
-        lf = __double2float_rn(l);
-      }
+      logit_of(v, m, q, l, key, lf);
       if (key > bk) bk = key, ba = i;  // ids rise: ties keep the lowest
       if (lf > -INFINITY && lf < mn) mn = lf;
     }
@@ -582,64 +739,66 @@ __device__ void reduce_part1(const Part1* p, int NB, uint64_t& M, int& arg, floa
   arg = id;
 }
 
-// the penalised logit as a double-f32 pair, its order key and its float
-__device__ __forceinline__ void logit_of(float v, int32_t m, const SeqParam& q, df& l, uint64_t& key, float& lf) {
-  if (m == 0) {
-    l = mk(v, 0.0f);
-    key = okey_f32(v);
-    lf = v;
-  } else {
-    const double d = penalize(v, m, q);
-    l = df_of(d);
-    key = okey(d);
-    lf = l.h;
-  }
-}
-
-__global__ void __launch_bounds__(kScanThreads) k_scan2(const float* __restrict__ logits, int64_t ld,
-                                                         const int32_t* __restrict__ marks,
-                                                         const SeqParam* __restrict__ sp, int V, int NB,
-                                                         const Part1* __restrict__ part1, Part2* __restrict__ part2,
-                                                         uint64_t* __restrict__ K, float2* __restrict__ E,
-                                                         uint16_t* __restrict__ bins, uint32_t* __restrict__ hcnt,
-                                                         unsigned long long* __restrict__ hmass, uint32_t* status) {
+// one CTA per sequence: the maximum and minimum over the per-chunk partials
+__global__ void __launch_bounds__(kScanThreads) k_stats(const Part1* __restrict__ part1, int NB1,
+                                                         Stats* __restrict__ stats, uint32_t* status) {
   __shared__ unsigned long long redk[32];
   __shared__ int redi[32];
   __shared__ float redf[32];
-  __shared__ float2 redd[32];
-  __shared__ uint32_t sc[kBins];
-  __shared__ unsigned long long smass[kBins];
-  __shared__ float s_Mh, s_Ml;
-  const int s = blockIdx.y, b = blockIdx.x, t = threadIdx.x;
-  const SeqParam& q = sp[s];
+  const int s = blockIdx.x;
   uint64_t Mk;
   int arg;
   float mn;
-  reduce_part1<kScanThreads>(part1 + (size_t)s * NB, NB, Mk, arg, mn, redk, redi, redf);
-  if (t == 0) {  // one f64 split per CTA
-    const df Md = df_of(key_value(Mk));
-    s_Mh = Md.h;
-    s_Ml = Md.l;
+  reduce_part1<kScanThreads>(part1 + (size_t)s * NB1, NB1, Mk, arg, mn, redk, redi, redf);
+  if (threadIdx.x == 0) {
+    Stats st;
+    st.key = Mk;
+    st.M = key_value(Mk);
+    const df Md = df_of(st.M);
+    st.Mh = Md.h;
+    st.Ml = Md.l;
+    st.mn = mn;
+    st.arg = arg;
+    if (!(st.M > -INFINITY)) {  // no finite logit
+      atomicOr(status, (uint32_t)DEC_SAMPLE_NO_FINITE);
+      st.Mh = -INFINITY;
+      st.Ml = 0.0f;
+    }
+    stats[s] = st;
   }
-  __syncthreads();
-  const float Mh = s_Mh, Ml = s_Ml;
-  if (!(Mh > -INFINITY)) {  // no finite logit
-    if (t == 0 && b == 0) atomicOr(status, (uint32_t)DEC_SAMPLE_NO_FINITE);
-    return;
-  }
-  const bool sampling = q.T > 0.0;
-  const bool unit = q.T == 1.0;
+}
+
+
+__global__ void __launch_bounds__(kScanThreads) k_scan2(const float* __restrict__ logits, int64_t ld,
+                                                         const int32_t* __restrict__ marks,
+                                                         const SeqParam* __restrict__ sp, int V, int Vp, int NB,
+                                                         const Stats* __restrict__ stats, Part2* __restrict__ part2,
+                                                         uint64_t* __restrict__ K, float2* __restrict__ E,
+                                                         uint16_t* __restrict__ bins, uint32_t* __restrict__ hcnt,
+                                                         unsigned long long* __restrict__ hmh,
+                                                         unsigned long long* __restrict__ hml) {
+  __shared__ float2 redd[32];
+  __shared__ uint32_t sc[kBins];
+  __shared__ unsigned long long sh[kBins], sl[kBins];
+  const int s = blockIdx.y, b = blockIdx.x, t = threadIdx.x;
+  const SeqParam& q = sp[s];
+  const Stats stt = stats[s];
+  const float Mh = stt.Mh, Ml = stt.Ml, mn = stt.mn;
+  if (!(Mh > -INFINITY)) return;  // no finite logit (flagged by k_stats)
+  const int flags = q.flags;
+  const bool sampling = flags & kSampling;
+  const bool unit = flags & kUnitT;
   const df rT = mk(q.rTh, q.rTl);
   const float R = Mh - mn;
   float scale = R > 0.0f ? (float)kBins / R : 0.0f;
   if (!(scale < 1e30f)) scale = 0.0f;
   if (sampling) {
-    for (int i = t; i < kBins; i += kScanThreads) sc[i] = 0, smass[i] = 0;
+    for (int i = t; i < kBins; i += kScanThreads) sc[i] = 0, sh[i] = 0, sl[i] = 0;
     __syncthreads();
   }
   const float* x = logits + (size_t)s * ld;
   const int32_t* mkv = marks + (size_t)s * V;
-  const size_t row = (size_t)s * V;
+  const size_t row = (size_t)s * Vp;
   df z = mk(0.0f, 0.0f), z2 = mk(0.0f, 0.0f);
   bool bad = false;
 #pragma unroll
@@ -657,15 +816,18 @@ __global__ void __launch_bounds__(kScanThreads) k_scan2(const float* __restrict_
         e = df_exp(d);
         if (sampling) e2 = unit ? e : df_exp(df_mul(d, rT));
       }
-      z = df_add(z, e);
+      z = df_add_fast(z, e);
       if (sampling) {
-        z2 = df_add(z2, e2);
+        z2 = df_add_fast(z2, e2);
         K[row + i] = key;
         E[row + i] = make_float2(e2.h, e2.l);
-        const int bin = scale > 0.0f ? (int)fminf((Mh - lf) * scale, (float)(kBins - 1)) : 0;
+        float bf;
+        const int bin = scale > 0.0f ? (int)floor_u(fminf((Mh - lf) * scale, (float)(kBins - 1)), bf) : 0;
         bins[row + i] = (uint16_t)bin;
         atomicAdd(&sc[bin], 1u);
-        atomicAdd(&smass[bin], fix_of(make_float2(e2.h, e2.l)));
+        const Fix f = fix_of(make_float2(e2.h, e2.l));
+        atomicAdd(&sh[bin], f.h);
+        atomicAdd(&sl[bin], f.l);
       }
     }
   }
@@ -685,7 +847,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan2(const float* __restrict_
     for (int i = t; i < kBins; i += kScanThreads)
       if (sc[i]) {
         atomicAdd(&hcnt[(size_t)s * kBins + i], sc[i]);
-        atomicAdd(&hmass[(size_t)s * kBins + i], smass[i]);
+        atomicAdd(&hmh[(size_t)s * kBins + i], sh[i]);
+        atomicAdd(&hml[(size_t)s * kBins + i], sl[i]);
       }
   }
 }
@@ -697,7 +860,7 @@ struct PickSmem {
   float2 ce[kCap];     // their e' (head, tail)
   int32_t cid[kCap];   // their ids
   uint32_t hc[kBins];  // bucket (or digit) counts
-  unsigned long long hm[kBins];
+  unsigned long long hmh[kBins], hml[kBins];  // bucket masses: integer and fraction words
   float2 redd[32];
   unsigned long long redk[32];
   int redi[32];
@@ -759,6 +922,7 @@ __device__ void sort_list(PickSmem& sm, int n, bool by_id) {
   }
 }
 
+// a mass target in the integer word's units (2^-45), floored, with `slack` units either side
 __device__ __forceinline__ unsigned long long fix_target(df tm, double slack) {
   const double v = dbl_of(tm) * kFix + slack;
   return v <= 0.0 ? 0ull : (v >= 1.8e19 ? ~0ull : (unsigned long long)v);
@@ -767,25 +931,31 @@ __device__ __forceinline__ unsigned long long fix_target(df tm, double slack) {
 // Gather, into shared memory and sorted, the stretch of the order where a
 // cumulative target is reached: count target `tc` elements, or e' mass `tm`,
 // over the elements allowed by `lim`.  Level 0 uses the bucket histogram in
-// sm.hc/hm (already restricted).  Returns the frame of the list.
+// sm.hc/hmh/hml (already restricted).  Returns the frame of the list.
 __device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& lim, const uint16_t* bins,
                         const uint64_t* K, const float2* E, int V, uint32_t* status) {
   const int t = threadIdx.x;
   __shared__ int s_lo, s_hi;
   __shared__ long long s_cnt_hi, s_cnt_before;
-  __shared__ unsigned long long s_m_before;
-  const unsigned long long lo_u = kind == kMass ? fix_target(tm, -kFixTol) : 0ull;
-  const unsigned long long hi_u = kind == kMass ? fix_target(tm, kFixTol) : 0ull;
+  __shared__ unsigned long long s_mh_before, s_ml_before;
+  const unsigned long long lo_u = kind == kMass ? fix_target(tm, -kFixSlack) : 0ull;
+  const unsigned long long hi_u = kind == kMass ? fix_target(tm, kFixSlack) : 0ull;
   const unsigned long long mid_u = kind == kMass ? fix_target(tm, 0.0) : 0ull;
   // ---- level 0: cumulative bucket counts and masses, two buckets per thread
   {
     const uint32_t c0 = sm.hc[2 * t], c1 = sm.hc[2 * t + 1];
-    const unsigned long long m0 = sm.hm[2 * t], m1 = sm.hm[2 * t + 1];
-    unsigned long long ctot, mtot;
+    const unsigned long long h0 = sm.hmh[2 * t], h1 = sm.hmh[2 * t + 1];
+    const unsigned long long l0 = sm.hml[2 * t], l1 = sm.hml[2 * t + 1];
+    // the walk compares integer words with the fraction words' carries folded in
+    const unsigned long long m0 = h0 + (l0 >> kFixBits), m1 = h1 + (l1 >> kFixBits);
+    unsigned long long ctot, mtot, htot, ltot;
     const unsigned long long cinc = block_scan<unsigned long long>((unsigned long long)c0 + c1, sm.redk, ctot);
     const unsigned long long minc = block_scan<unsigned long long>(m0 + m1, sm.redk, mtot);
+    const unsigned long long hinc = block_scan<unsigned long long>(h0 + h1, sm.redk, htot);
+    const unsigned long long linc = block_scan<unsigned long long>(l0 + l1, sm.redk, ltot);
     const unsigned long long cb0 = cinc - c0 - c1, mb0 = minc - m0 - m1;  // before bucket 2t
     const unsigned long long ca0 = cb0 + c0, ma0 = mb0 + m0;              // through bucket 2t
+    const unsigned long long hb0 = hinc - h0 - h1, lb0 = linc - l0 - l1;
     if (t == 0) s_lo = kBins - 1, s_hi = kBins - 1;
     __syncthreads();
     if (kind == kCount) {
@@ -806,8 +976,8 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& 
     if (kind == kCount && t == 0) s_hi = s_lo;
     __syncthreads();
     const int lo = s_lo, hi = s_hi;
-    if (2 * t == lo) s_cnt_before = (long long)cb0, s_m_before = mb0;
-    if (2 * t + 1 == lo) s_cnt_before = (long long)ca0, s_m_before = ma0;
+    if (2 * t == lo) s_cnt_before = (long long)cb0, s_mh_before = hb0, s_ml_before = lb0;
+    if (2 * t + 1 == lo) s_cnt_before = (long long)ca0, s_mh_before = hb0 + h0, s_ml_before = lb0 + l0;
     if (2 * t == hi) s_cnt_hi = (long long)ca0;
     if (2 * t + 1 == hi) s_cnt_hi = (long long)cinc;
     __syncthreads();
@@ -826,13 +996,13 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& 
   int shift = 96;
   unsigned __int128 pre = 0;
   long long r_above = cnt_before;
+  unsigned long long r_h = s_mh_before, r_l = s_ml_before;
   if (mode == 2) {
     __shared__ int s_d;
     __shared__ long long s_above;
-    __shared__ unsigned long long s_mabove;
-    unsigned long long r_mabove = s_m_before;
+    __shared__ unsigned long long s_h, s_l;
     while (true) {
-      for (int i = t; i < 256; i += kPick) sm.hc[i] = 0, sm.hm[i] = 0;
+      for (int i = t; i < 256; i += kPick) sm.hc[i] = 0, sm.hmh[i] = 0, sm.hml[i] = 0;
       __syncthreads();
       for (int i = t; i < V; i += kPick) {
         const int bn = bins[i];
@@ -843,31 +1013,35 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& 
         if (shift < 96 && (Kc >> shift) != pre) continue;
         const int d = (int)((Kc >> (shift - 8)) & 255);
         atomicAdd(&sm.hc[d], 1u);
-        if (kind == kMass) atomicAdd(&sm.hm[d], fix_of(E[i]));
+        const Fix f = fix_of(E[i]);
+        atomicAdd(&sm.hmh[d], f.h);
+        atomicAdd(&sm.hml[d], f.l);
       }
       __syncthreads();
       // walk digits from 255 (earliest) down: one thread, 256 steps
       if (t == 0) {
         long long c = r_above;
-        unsigned long long m = r_mabove;
+        unsigned long long h = r_h, l = r_l;
         int pick = -1, last = -1;
         for (int d = 255; d >= 0; --d) {
           if (!sm.hc[d]) continue;
           last = d;
           const long long c2 = c + sm.hc[d];
-          const unsigned long long m2 = m + sm.hm[d];
-          const bool hit = kind == kCount ? c2 >= tc : m2 >= mid_u;
+          const unsigned long long h2 = h + sm.hmh[d], l2 = l + sm.hml[d];
+          const bool hit = kind == kCount ? c2 >= tc : h2 + (l2 >> kFixBits) >= mid_u;
           if (hit) {
             pick = d;
             break;
           }
           c = c2;
-          m = m2;
+          h = h2;
+          l = l2;
         }
         if (pick < 0 && last >= 0) {  // target beyond the set (rounding): the last digit holds the end
           pick = last;
           c -= sm.hc[last];
-          m -= sm.hm[last];
+          h -= sm.hmh[last];
+          l -= sm.hml[last];
         }
         if (pick < 0) {  // no element matched (cannot happen: the digit was non-empty)
           atomicOr(status, (uint32_t)DEC_SAMPLE_OVERFLOW);
@@ -875,13 +1049,15 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& 
         }
         s_d = pick;
         s_above = c;
-        s_mabove = m;
+        s_h = h;
+        s_l = l;
       }
       __syncthreads();
       const int d = s_d;
       const uint32_t cd = sm.hc[d];
       r_above = s_above;
-      r_mabove = s_mabove;
+      r_h = s_h;
+      r_l = s_l;
       pre = (pre << 8) | (unsigned __int128)d;
       shift -= 8;
       __syncthreads();
@@ -889,39 +1065,26 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& 
     }
   }
 
-  // ---- gather
+  // ---- gather: eight buckets per 16-byte load
   if (t == 0) sm.n = 0;
   __syncthreads();
-  df msum = mk(0.0f, 0.0f);
-  for (int i = t; i < V; i += kPick) {
-    const int bn = bins[i];
-    if (bn > hi) continue;
-    if (mode == 0) {
+  const uint4* b4 = reinterpret_cast<const uint4*>(bins);
+  const int n8 = (V + 7) >> 3;
+  for (int g = t; g < n8; g += kPick) {
+    const uint4 w = b4[g];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = 8 * g + q;
+      const int bn = (int)((ws[q >> 1] >> ((q & 1) * 16)) & 0xFFFFu);
+      if (i >= V || bn > hi || (mode != 0 && bn < lo)) continue;
       const uint64_t k = K[i];
       if (!in_lim(lim, bn, k, i)) continue;
-    } else if (bn < lo) {
-      if (in_lim(lim, bn, 0, i)) {  // wholly before the list
-        const float2 e = E[i];
-        msum = df_add(msum, mk(e.x, e.y));
-      }
-      continue;
-    } else {
-      const uint64_t k = K[i];
-      if (!in_lim(lim, bn, k, i)) continue;
-      if (mode == 2) {
-        const unsigned __int128 top = ckey(k, i) >> shift;
-        if (top > pre) {  // inside the buckets, before the list
-          const float2 e = E[i];
-          msum = df_add(msum, mk(e.x, e.y));
-          continue;
-        }
-        if (top < pre) continue;
-      }
+      if (mode == 2 && (ckey(k, i) >> shift) != pre) continue;
+      const int slot = atomicAdd(&sm.n, 1);
+      if (slot < kCap) sm.ck[slot] = k, sm.ce[slot] = E[i], sm.cid[slot] = i;
     }
-    const int slot = atomicAdd(&sm.n, 1);
-    if (slot < kCap) sm.ck[slot] = K[i], sm.ce[slot] = E[i], sm.cid[slot] = i;
   }
-  const df m_above = block_sum_df<kPick>(msum, sm.redd);
   __syncthreads();
   if (sm.n > kCap) {
     if (t == 0) atomicOr(status, (uint32_t)DEC_SAMPLE_OVERFLOW);
@@ -931,8 +1094,8 @@ __device__ Frame gather(PickSmem& sm, int kind, long long tc, df tm, const Lim& 
   }
   sort_list(sm, sm.n, false);
   Frame f;
-  f.above = mode == 0 ? 0 : (mode == 1 ? cnt_before : r_above);
-  f.m_above = mode == 0 ? mk(0.0f, 0.0f) : m_above;
+  f.above = mode == 0 ? 0 : r_above;
+  f.m_above = mode == 0 ? mk(0.0f, 0.0f) : fix_df(r_h, r_l);
   return f;
 }
 
@@ -984,71 +1147,75 @@ __device__ double logprob_of(const float* x, const int32_t* mkv, int id, const S
 }
 
 // the bucket histogram of one sequence, restricted to the order prefix `lim` allows
-__device__ void load_hist(PickSmem& sm, const Lim& lim, const uint32_t* hc, const unsigned long long* hm,
-                          const uint16_t* bins, const uint64_t* K, const float2* E, int V) {
+__device__ void load_hist(PickSmem& sm, const Lim& lim, const uint32_t* hc, const unsigned long long* hh,
+                          const unsigned long long* hl, const uint16_t* bins, const uint64_t* K, const float2* E,
+                          int V) {
   const int t = threadIdx.x;
   for (int i = t; i < kBins; i += kPick) {
     const bool cut = lim.on && i > lim.bin;
     sm.hc[i] = cut ? 0u : hc[i];
-    sm.hm[i] = cut ? 0ull : hm[i];
+    sm.hmh[i] = cut ? 0ull : hh[i];
+    sm.hml[i] = cut ? 0ull : hl[i];
   }
   __syncthreads();
   if (!lim.on) return;
   // the limit's own bucket: only the elements at or before the limit
   __shared__ unsigned int s_c;
-  __shared__ unsigned long long s_m;
-  if (t == 0) s_c = 0, s_m = 0;
+  __shared__ unsigned long long s_h, s_l;
+  if (t == 0) s_c = 0, s_h = 0, s_l = 0;
   __syncthreads();
   unsigned int c = 0;
-  unsigned long long m = 0;
+  unsigned long long h = 0, l = 0;
   for (int i = t; i < V; i += kPick) {
     if (bins[i] != lim.bin) continue;
-    if (in_lim(lim, lim.bin, K[i], i)) ++c, m += fix_of(E[i]);
+    if (in_lim(lim, lim.bin, K[i], i)) {
+      const Fix f = fix_of(E[i]);
+      ++c, h += f.h, l += f.l;
+    }
   }
   atomicAdd(&s_c, c);
-  atomicAdd(&s_m, m);
+  atomicAdd(&s_h, h);
+  atomicAdd(&s_l, l);
   __syncthreads();
-  if (t == 0) sm.hc[lim.bin] = s_c, sm.hm[lim.bin] = s_m;
+  if (t == 0) sm.hc[lim.bin] = s_c, sm.hmh[lim.bin] = s_h, sm.hml[lim.bin] = s_l;
   __syncthreads();
 }
 
 __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ logits, int64_t ld,
                                                     const int32_t* __restrict__ marks,
-                                                    const SeqParam* __restrict__ sp, int V, int NB,
-                                                    const Part1* __restrict__ part1, const Part2* __restrict__ part2,
+                                                    const SeqParam* __restrict__ sp, int V, int Vp, int NB,
+                                                    const Stats* __restrict__ stats, const Part2* __restrict__ part2,
                                                     const uint64_t* __restrict__ Kall, const float2* __restrict__ Eall,
                                                     const uint16_t* __restrict__ ball, const uint32_t* __restrict__ hcnt,
-                                                    const unsigned long long* __restrict__ hmass,
+                                                    const unsigned long long* __restrict__ hmh,
+                                                    const unsigned long long* __restrict__ hml,
                                                     PickState* __restrict__ state, dec_rng* __restrict__ rng,
                                                     int32_t* __restrict__ tokens, double* __restrict__ logprobs,
                                                     uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PickSmem& sm = *reinterpret_cast<PickSmem*>(smem_raw);
-  __shared__ double s_M, s_lse;
+  __shared__ double s_lse;
   const int s = blockIdx.x, t = threadIdx.x;
   const SeqParam& q = sp[s];
+  const Stats stt = stats[s];
   const float* x = logits + (size_t)s * ld;
   const int32_t* mkv = marks + (size_t)s * V;
-  const size_t row = (size_t)s * V;
+  const size_t row = (size_t)s * Vp;
   const uint64_t* K = Kall + row;
   const float2* E = Eall + row;
   const uint16_t* bins = ball + row;
+  const size_t hrow = (size_t)s * kBins;
 
-  uint64_t Mk;
-  int arg;
-  float mn;
-  reduce_part1<kPick>(part1 + (size_t)s * NB, NB, Mk, arg, mn, sm.redk, sm.redi, sm.redf);
+  const double M = stt.M;
+  const int arg = stt.arg;
   Part2 pz;
   pz.zh = pz.zl = pz.z2h = pz.z2l = 0.0f;
   if (t < NB) pz = part2[(size_t)s * NB + t];
   const df Z = block_sum_df<kPick>(mk(pz.zh, pz.zl), sm.redd);
   const df Zall = block_sum_df<kPick>(mk(pz.z2h, pz.z2l), sm.redd);
-  if (t == 0) {  // the only f64 transcendental: one logarithm per sequence
-    s_M = key_value(Mk);
-    s_lse = log(dbl_of(Z));
-  }
+  if (t == 0) s_lse = log(dbl_of(Z));  // the only f64 transcendental: one logarithm per sequence
   __syncthreads();
-  const double M = s_M, lse = s_lse;
+  const double lse = s_lse;
   PickState st;
   st.mode = 0;
   st.has_last = 0;
@@ -1057,7 +1224,7 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
   st.last_key = 0;
   st.M = M;
   st.lse = lse;
-  if (!(M > -INFINITY)) {  // flagged by k_scan2
+  if (!(M > -INFINITY)) {  // flagged by k_stats
     if (t == 0) {
       tokens[s] = -1;
       logprobs[s] = -INFINITY;
@@ -1065,7 +1232,8 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     }
     return;
   }
-  if (q.T == 0.0) {  // greedy: no draw
+  const int flags = q.flags;
+  if (!(flags & kSampling)) {  // greedy: no draw
     if (t == 0) {
       tokens[s] = arg;
       logprobs[s] = (M - M) - lse;
@@ -1074,8 +1242,8 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     return;
   }
   const long long kk = (q.top_k > 0 && q.top_k < V) ? q.top_k : V;
-  const bool p_on = q.top_p < 1.0;
-  const bool m_on = q.min_p > 0.0;
+  const bool p_on = flags & kTopP;
+  const bool m_on = flags & kMinP;
   const df minp = mk(q.mph, q.mpl);
 
   // the list: (has_list) sm holds n sorted elements starting `above` into the order;
@@ -1095,7 +1263,7 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
   // ---- top-k
   Lim klim = none;
   if (kk < V) {
-    load_hist(sm, none, hcnt + (size_t)s * kBins, hmass + (size_t)s * kBins, bins, K, E, V);
+    load_hist(sm, none, hcnt + hrow, hmh + hrow, hml + hrow, bins, K, E, V);
     fr = gather(sm, kCount, kk, mk(0.0f, 0.0f), none, bins, K, E, V, status);
     has_list = true;
     n = sm.n;
@@ -1120,7 +1288,7 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     if (has_list && fr.above == 0) {
       end = walk_mass(sm, end + 1, mk(0.0f, 0.0f), target);
     } else {
-      load_hist(sm, klim, hcnt + (size_t)s * kBins, hmass + (size_t)s * kBins, bins, K, E, V);
+      load_hist(sm, klim, hcnt + hrow, hmh + hrow, hml + hrow, bins, K, E, V);
       fr = gather(sm, kMass, 0, target, klim, bins, K, E, V, status);
       has_list = true;
       n = sm.n;
@@ -1153,9 +1321,9 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
     __shared__ uint64_t s_state;
     if (t == 0) {
       const dec_rng r = rng[s];
-      uint64_t stt = r.state;
-      s_u = pcg_uniform(stt, r.inc);
-      s_state = stt;
+      uint64_t g = r.state;
+      s_u = pcg_uniform(g, r.inc);
+      s_state = g;
     }
     __syncthreads();
     const df target = df_mul(df_of(s_u), Zf);  // u < c_j  <=>  u * Zf < running e' sum
@@ -1202,12 +1370,12 @@ __global__ void __launch_bounds__(kPick, 1) k_pick(const float* __restrict__ log
 
 __device__ __forceinline__ bool kept_by(const PickState& st, const SeqParam& q, uint64_t k, float2 e, int i) {
   if (st.has_last && before(st.last_key, st.last_id, k, i)) return false;
-  return !(q.min_p > 0.0) || df_ge(mk(e.x, e.y), mk(q.mph, q.mpl));
+  return !(q.flags & kMinP) || df_ge(mk(e.x, e.y), mk(q.mph, q.mpl));
 }
 
 __global__ void __launch_bounds__(kScanThreads) k_final_sum(const SeqParam* __restrict__ sp,
-                                                             const PickState* __restrict__ state, int V, int NB,
-                                                             const uint64_t* __restrict__ Kall,
+                                                             const PickState* __restrict__ state, int V, int Vp,
+                                                             int NB, const uint64_t* __restrict__ Kall,
                                                              const float2* __restrict__ Eall,
                                                              float2* __restrict__ fsum) {
   __shared__ float2 red[32];
@@ -1215,14 +1383,14 @@ __global__ void __launch_bounds__(kScanThreads) k_final_sum(const SeqParam* __re
   const PickState st = state[s];
   if (st.mode == 0) return;
   const SeqParam& q = sp[s];
-  const size_t row = (size_t)s * V;
+  const size_t row = (size_t)s * Vp;
   df v = mk(0.0f, 0.0f);
 #pragma unroll
   for (int j = 0; j < kChunk / kScanThreads; ++j) {
     const int i = b * kChunk + j * kScanThreads + t;
     if (i < V) {
       const float2 e = Eall[row + i];
-      if (kept_by(st, q, Kall[row + i], e, i)) v = df_add(v, mk(e.x, e.y));
+      if (kept_by(st, q, st.has_last ? Kall[row + i] : 0ull, e, i)) v = df_add(v, mk(e.x, e.y));
     }
   }
   v = block_sum_df<kScanThreads>(v, red);
@@ -1232,7 +1400,7 @@ __global__ void __launch_bounds__(kScanThreads) k_final_sum(const SeqParam* __re
 __global__ void __launch_bounds__(kPick, 1) k_final_pick(const float* __restrict__ logits, int64_t ld,
                                                           const int32_t* __restrict__ marks,
                                                           const SeqParam* __restrict__ sp,
-                                                          const PickState* __restrict__ state, int V, int NB,
+                                                          const PickState* __restrict__ state, int V, int Vp, int NB,
                                                           const uint64_t* __restrict__ Kall,
                                                           const float2* __restrict__ Eall,
                                                           const float2* __restrict__ fsum, dec_rng* __restrict__ rng,
@@ -1246,7 +1414,7 @@ __global__ void __launch_bounds__(kPick, 1) k_final_pick(const float* __restrict
   const PickState st = state[s];
   if (st.mode == 0) return;
   const SeqParam& q = sp[s];
-  const size_t row = (size_t)s * V;
+  const size_t row = (size_t)s * Vp;
   float2 f2 = make_float2(0.f, 0.f);
   if (t < NB) f2 = fsum[(size_t)s * NB + t];
   const df fs = mk(f2.x, f2.y);
@@ -1255,9 +1423,9 @@ __global__ void __launch_bounds__(kPick, 1) k_final_pick(const float* __restrict
   const df cinc = block_scan_df(fs, redd, tot);
   if (t == 0) {
     const dec_rng r = rng[s];
-    uint64_t stt = r.state;
-    s_u = pcg_uniform(stt, r.inc);
-    s_state = stt;
+    uint64_t g = r.state;
+    s_u = pcg_uniform(g, r.inc);
+    s_state = g;
     s_chunk = NB;
     s_last = -1;
     s_tok = 0x7fffffff;
@@ -1295,7 +1463,8 @@ __global__ void __launch_bounds__(kPick, 1) k_final_pick(const float* __restrict
     // nothing passed u here (rounding): the chunk's last kept id
     const int tok = s_tok != 0x7fffffff ? s_tok : s_lastid;
     tokens[s] = tok;
-    logprobs[s] = tok >= 0 ? logprob_of(logits + (size_t)s * ld, marks + row, tok, q, st.M, st.lse) : -INFINITY;
+    logprobs[s] = tok >= 0 ? logprob_of(logits + (size_t)s * ld, marks + (size_t)s * V, tok, q, st.M, st.lse)
+                           : -INFINITY;
     rng[s].state = s_state;
   }
 }
@@ -1487,7 +1656,9 @@ int dec_sample(dec_sampler* s, const float* logits, int64_t ld, int32_t n, const
     q.pres = p.presence_penalty;
     q.freq = p.frequency_penalty;
     q.top_k = p.top_k;
-    q.pad0 = q.pad1 = 0;
+    q.pad1 = 0;
+    q.flags = (p.temperature > 0.0 ? kSampling : 0) | (p.temperature == 1.0 ? kUnitT : 0) | (p.top_p < 1.0 ? kTopP : 0) |
+              (p.min_p > 0.0 ? kMinP : 0);
     // 1/T, top_p and min_p as float head + tail (long double division where the host has it)
     const long double rT = p.temperature > 0.0 ? 1.0L / (long double)p.temperature : 0.0L;
     q.rTh = (float)rT;
@@ -1505,7 +1676,8 @@ int dec_sample(dec_sampler* s, const float* logits, int64_t ld, int32_t n, const
   S_CUDA(cudaMemcpyAsync(dsp, H, (size_t)n * sizeof(SeqParam), cudaMemcpyHostToDevice, st));
   S_CUDA(cudaEventRecord(s->stage_ev[slot], st));
   S_CUDA(cudaMemsetAsync(w + s->L.hcnt, 0, (size_t)n * kBins * 4, st));
-  S_CUDA(cudaMemsetAsync(w + s->L.hmass, 0, (size_t)n * kBins * 8, st));
+  S_CUDA(cudaMemsetAsync(w + s->L.hmh, 0, (size_t)n * kBins * 8, st));
+  S_CUDA(cudaMemsetAsync(w + s->L.hml, 0, (size_t)n * kBins * 8, st));
   int32_t* marks = (int32_t*)(w + s->L.marks);
   uint32_t* status = (uint32_t*)(w + s->L.status);
   const int V = s->V, NB = s->NB;
@@ -1515,18 +1687,22 @@ int dec_sample(dec_sampler* s, const float* logits, int64_t ld, int32_t n, const
   float2* E = (float2*)(w + s->L.E);
   uint16_t* bins = (uint16_t*)(w + s->L.bins);
   uint32_t* hc = (uint32_t*)(w + s->L.hcnt);
-  unsigned long long* hm = (unsigned long long*)(w + s->L.hmass);
+  unsigned long long* hh = (unsigned long long*)(w + s->L.hmh);
+  unsigned long long* hl = (unsigned long long*)(w + s->L.hml);
+  Stats* stats = (Stats*)(w + s->L.stats);
+  const int Vp = padded(s->V), NB1 = (s->V + kChunk1 - 1) / kChunk1;
   PickState* ps = (PickState*)(w + s->L.state);
   float2* fsum = (float2*)(w + s->L.fsum);
   const dim3 hgrid((max_hist + 255) / 256, n);
   if (max_hist > 0) k_mark<<<hgrid, 256, 0, st>>>(dsp, history, marks, V, 1, status);
-  const dim3 grid(NB, n);
-  k_scan1<<<grid, kScanThreads, 0, st>>>(logits, ld, marks, dsp, V, NB, p1, status);
-  k_scan2<<<grid, kScanThreads, 0, st>>>(logits, ld, marks, dsp, V, NB, p1, p2, K, E, bins, hc, hm, status);
-  k_pick<<<n, kPick, sizeof(PickSmem), st>>>(logits, ld, marks, dsp, V, NB, p1, p2, K, E, bins, hc, hm, ps, rng, tokens,
-                                             logprobs, status);
-  k_final_sum<<<grid, kScanThreads, 0, st>>>(dsp, ps, V, NB, K, E, fsum);
-  k_final_pick<<<n, kPick, 0, st>>>(logits, ld, marks, dsp, ps, V, NB, K, E, fsum, rng, tokens, logprobs);
+  const dim3 grid(NB, n), grid1(NB1, n);
+  k_scan1<<<grid1, kScanThreads, 0, st>>>(logits, ld, marks, dsp, V, NB1, p1, status);
+  k_stats<<<n, kScanThreads, 0, st>>>(p1, NB1, stats, status);
+  k_scan2<<<grid, kScanThreads, 0, st>>>(logits, ld, marks, dsp, V, Vp, NB, stats, p2, K, E, bins, hc, hh, hl);
+  k_pick<<<n, kPick, sizeof(PickSmem), st>>>(logits, ld, marks, dsp, V, Vp, NB, stats, p2, K, E, bins, hc, hh, hl, ps,
+                                             rng, tokens, logprobs, status);
+  k_final_sum<<<grid, kScanThreads, 0, st>>>(dsp, ps, V, Vp, NB, K, E, fsum);
+  k_final_pick<<<n, kPick, 0, st>>>(logits, ld, marks, dsp, ps, V, Vp, NB, K, E, fsum, rng, tokens, logprobs);
   if (max_hist > 0) k_mark<<<hgrid, 256, 0, st>>>(dsp, history, marks, V, 0, status);
   S_CUDA(cudaGetLastError());
   return DEC_OK;
