@@ -12,6 +12,7 @@ numerics  bf16 / f16 rounding written out from their bit-level definitions
 model     the vectorised float64 decoder (numpy), the plain definition
 brute     the same decoder in scalar Python loops, for tiny shapes only
 compare   the parity metrics (max / mean abs error, argmax with near ties)
+int4      int4 group-symmetric weights: quantize, pack, dequantize
 sampler   the f64 sampler (penalties, logprob, temperature, top-k, top-p,
           min-p, CDF walk) and its PCG32 streams
 """

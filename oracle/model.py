@@ -32,6 +32,10 @@ Readings where the pages are silent (each is listed in the design doc):
   heads share a key/value head).
 * In the bf16 mode the oracle uses the bf16-rounded weights widened to
   float64; activations and the cache stay float64.
+* In the int4 mode the seven projections of every layer are the int4
+  effective weights (``oracle.int4``: groups of 32 input columns, f16
+  scales) and the tied embedding is bf16-rounded; activations and the cache
+  stay float64.
 
 ``mutant`` plants one named mistake (tinyllm L10.1 section 5 "Pitfalls",
 and octlm's neighbour pairing) so that tests can show the parity harness
@@ -44,6 +48,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
+from . import int4
 from .numerics import bf16_round
 
 MUTANTS = ("s13", "s14", "s15", "s16", "s20", "s22", "neighbour")
@@ -143,11 +148,13 @@ class Oracle:
     weights: dict name -> float32 (or float64) array, names as in
     ``decoder_qwen3_step_gb300.inputs.weight_names``.  mode "fp32" widens
     the weights as given; mode "bf16" first rounds every matrix (embedding
-    included) to bfloat16, keeping the RMSNorm gains as given.
+    included) to bfloat16, keeping the RMSNorm gains as given; mode "int4"
+    quantizes the projections (q, k, v, o, gate, up, down) to int4 with
+    f16 group scales and rounds the embedding to bfloat16.
     """
 
     def __init__(self, cfg: DecoderConfig, weights: dict, mode: str = "fp32"):
-        if mode not in ("fp32", "bf16"):
+        if mode not in ("fp32", "bf16", "int4"):
             raise ValueError(mode)
         if cfg.n_heads % cfg.n_kv_heads or cfg.head_dim % 2:
             raise ValueError("n_heads must be a multiple of n_kv_heads and head_dim even")
@@ -156,7 +163,9 @@ class Oracle:
 
         def mat(name):
             w = np.asarray(weights[name], dtype=np.float32)
-            if mode == "bf16":
+            if mode == "int4" and name != "embed":
+                return int4.effective(w)
+            if mode in ("bf16", "int4"):
                 w = bf16_round(w)
             return w.astype(np.float64)
 
