@@ -55,12 +55,20 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int act_bytes(const dec_config& c) { return c.mode == DEC_FP32 ? 4 : 2; }
 int kv_bytes(const dec_config& c) { return c.mode == DEC_FP32 ? 4 : 2; }
 int qkv_rows(const dec_config& c) { return (c.n_heads + 2 * c.n_kv_heads) * c.head_dim; }
+bool serving(const dec_config& c) { return c.mode != DEC_FP32; }       // bf16 GEMM inputs, f16 KV
+bool int4_proj(const dec_config& c) { return c.mode == DEC_INT4_F16KV; } // int4 projections
+// bytes of one projection matrix in the packed buffer: elements, or int4 codes then f16 group scales
+size_t mat_bytes(const dec_config& c, size_t rows, size_t K) {
+  if (int4_proj(c)) return rows * K / 2 + rows * (K / 32) * 2;
+  return rows * K * (c.mode == DEC_FP32 ? 4 : 2);
+}
 int max_blocks_of(const dec_config& c) { return (c.max_positions + c.block_tokens - 1) / c.block_tokens; }
 int max_chunks_of(const dec_config& c) { return (c.max_positions + kDecodeChunk - 1) / kDecodeChunk; }
 
 int check_config(const dec_config* c) {
   if (!c) return fail(DEC_EINVAL, "config is NULL");
-  if (c->mode != DEC_FP32 && c->mode != DEC_BF16_F16KV) return fail(DEC_EINVAL, "unknown mode %d", c->mode);
+  if (c->mode != DEC_FP32 && c->mode != DEC_BF16_F16KV && c->mode != DEC_INT4_F16KV)
+    return fail(DEC_EINVAL, "unknown mode %d", c->mode);
   if (c->rope_scaling) return fail(DEC_EINVAL, "unsupported: scaled RoPE");
   if (c->sliding_window) return fail(DEC_EINVAL, "unsupported: sliding-window attention");
   if (c->attention_bias) return fail(DEC_EINVAL, "unsupported: attention biases");
@@ -80,6 +88,8 @@ int check_config(const dec_config* c) {
   if (c->block_tokens != 16) return fail(DEC_EINVAL, "block_tokens must be 16");
   if (!(c->rope_base > 1.0) || !(c->rms_eps > 0.0)) return fail(DEC_EINVAL, "rope_base must be > 1, rms_eps > 0");
   if (c->max_positions > kMaxPositions) return fail(DEC_EINVAL, "max_positions above %d", kMaxPositions);
+  if (c->mode == DEC_INT4_F16KV && (c->ff_hidden % 32 || (c->n_heads * c->head_dim) % 32))
+    return fail(DEC_EINVAL, "int4 weights need every input width (d_model, n_heads*head_dim, ff_hidden) a multiple of 32");
   return DEC_OK;
 }
 
@@ -93,7 +103,7 @@ struct PackedLayout {
 
 PackedLayout packed_layout(const dec_config& c) {
   PackedLayout L{};
-  const size_t wb = c.mode == DEC_FP32 ? 4 : 2;
+  const size_t wb = c.mode == DEC_FP32 ? 4 : 2;  // the embedding: f32, else bf16
   const size_t d = c.d_model, D = c.head_dim, F = c.ff_hidden, HD = (size_t)c.n_heads * D;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
@@ -107,10 +117,10 @@ PackedLayout packed_layout(const dec_config& c) {
   L.mlp_norm = ltake(d * 4);
   L.q_norm = ltake(D * 4);
   L.k_norm = ltake(D * 4);
-  L.wqkv = ltake((size_t)qkv_rows(c) * d * wb);
-  L.wo = ltake(d * HD * wb);
-  L.wgu = ltake(2 * F * d * wb);
-  L.wd = ltake(d * F * wb);
+  L.wqkv = ltake(mat_bytes(c, qkv_rows(c), d));
+  L.wo = ltake(mat_bytes(c, d, HD));
+  L.wgu = ltake(mat_bytes(c, 2 * F, d));
+  L.wd = ltake(mat_bytes(c, d, F));
   L.layer_stride = lo;
   L.total = L.layer0 + (size_t)c.n_layers * lo;
   return L;
@@ -369,7 +379,8 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
       return fail(DEC_EINVAL, "missing weight pointer in layer %d", l);
 
   cudaStream_t s = (cudaStream_t)stream;
-  const bool bf = c.mode == DEC_BF16_F16KV;
+  const bool bf = serving(c);
+  const bool i4 = int4_proj(c);
   char* P = (char*)packed_buf;
   const int d = c.d_model, D = c.head_dim, F = c.ff_hidden, H = c.n_heads, Hkv = c.n_kv_heads;
   const size_t wb = bf ? 2 : 4;
@@ -398,6 +409,21 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
     DEC_CUDA(cudaMemcpyAsync(Lb + pl.q_norm, w->q_norm[l], D * 4, cudaMemcpyDeviceToDevice, s));
     DEC_CUDA(cudaMemcpyAsync(Lb + pl.k_norm, w->k_norm[l], D * 4, cudaMemcpyDeviceToDevice, s));
     char* qkv = Lb + pl.wqkv;
+    if (i4) {  // quantize at load: codes, then the scales of the whole matrix
+      const size_t R = qkv_rows(c), dG = d / 32;
+      char* qs = qkv + R * d / 2;
+      DEC_CUDA(launch_quant_i4(qkv, qs, w->wq[l], H * D, d, PACK_IDENTITY, s));
+      DEC_CUDA(launch_quant_i4(qkv + (size_t)H * D * d / 2, qs + (size_t)H * D * dG * 2, w->wk[l], Hkv * D, d,
+                               PACK_IDENTITY, s));
+      DEC_CUDA(launch_quant_i4(qkv + (size_t)(H + Hkv) * D * d / 2, qs + (size_t)(H + Hkv) * D * dG * 2, w->wv[l],
+                               Hkv * D, d, PACK_IDENTITY, s));
+      DEC_CUDA(launch_quant_i4(Lb + pl.wo, Lb + pl.wo + (size_t)d * H * D / 2, w->wo[l], d, H * D, PACK_IDENTITY, s));
+      char* gu = Lb + pl.wgu;
+      DEC_CUDA(launch_quant_i4(gu, gu + (size_t)2 * F * d / 2, w->w_gate[l], F, d, PACK_GATE, s));
+      DEC_CUDA(launch_quant_i4(gu, gu + (size_t)2 * F * d / 2, w->w_up[l], F, d, PACK_UP, s));
+      DEC_CUDA(launch_quant_i4(Lb + pl.wd, Lb + pl.wd + (size_t)d * F / 2, w->w_down[l], d, F, PACK_IDENTITY, s));
+      continue;
+    }
     DEC_CUDA(launch_pack(qkv, w->wq[l], H * D, d, PACK_IDENTITY, bf, s));
     DEC_CUDA(launch_pack(qkv + (size_t)H * D * d * wb, w->wk[l], Hkv * D, d, PACK_IDENTITY, bf, s));
     DEC_CUDA(launch_pack(qkv + (size_t)(H + Hkv) * D * d * wb, w->wv[l], Hkv * D, d, PACK_IDENTITY, bf, s));
@@ -444,7 +470,7 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
     const int P = m->num_sms;
-    m->mega_shape = bf && coop && P <= kMegaMaxGrid && c.n_heads == 2 * c.n_kv_heads &&
+    m->mega_shape = c.mode == DEC_BF16_F16KV && coop && P <= kMegaMaxGrid && c.n_heads == 2 * c.n_kv_heads &&
                     (D == 32 || D == 64 || D == 128) && c.block_tokens == 16 && d <= kMegaKSlice && d % 16 == 0 &&
                     (H * D) % 16 == 0 && F % 16 == 0 && (d + P - 1) / P <= 16 &&
                     mega_slots(kMegaMaxTokens, D, (size_t)m->smem_optin) >= 2 &&
@@ -705,7 +731,8 @@ struct StepPlan {
 // Queue the kernels of one step on `st` (eager, or into a capture).
 static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   const dec_config& c = m->cfg;
-  const bool bf = c.mode == DEC_BF16_F16KV;
+  const bool bf = serving(c);
+  const bool i4 = int4_proj(c);
   char* P = m->packed;
   char* ws = m->ws;
   const PackedLayout& pl = m->pl;
@@ -726,7 +753,8 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   const bool dumping = m->dump && m->dump_floats >= (size_t)(c.n_layers + 1) * N * d;
   // many-token products go to the tensor cores in the serving mode
   auto product = [&](const GemvArgs& g, int epi, const CUtensorMap* tw, const CUtensorMap* tx,
-                     const CUtensorMap* tx32) -> cudaError_t {
+                     const CUtensorMap* tx32, bool proj = true) -> cudaError_t {
+    if (i4 && proj) return launch_gemv_i4(g, epi, st);  // int4 projections: dequantized in registers
     if (bf && m->tc_on && m->tc_ready && g.T > kGemvMaxTokens && tc_eligible(g))
       return launch_gemm_tc(g, epi, tw, tx, m->num_sms, ERR, st);
     if (bf && m->tc_on && m->tc_ready && tc_skinny_eligible(g))
@@ -799,7 +827,7 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   gl.W = P + pl.embed; gl.rows = c.vocab; gl.K = d; gl.X = XN; gl.x_row = (sp.rows_all || sp.decode) ? nullptr : sp.meta.row_tok;
   gl.T = R; gl.ssq = SSQ;
   gl.out_f32 = sp.logits; gl.keys = KEYS;
-  DEC_LAUNCH(DEC_K_LMHEAD, product(gl, EPI_LOGITS, &m->tm_embed, &m->tm_xn, &m->tm_xn32));
+  DEC_LAUNCH(DEC_K_LMHEAD, product(gl, EPI_LOGITS, &m->tm_embed, &m->tm_xn, &m->tm_xn32, false));
   DEC_LAUNCH(DEC_K_ARGMAX, launch_argmax_finalize(KEYS, sp.argmax, R, st));
   return DEC_OK;
 }
@@ -1095,6 +1123,7 @@ int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X,
   const dec_config& c = m->cfg;
   if (which < 4 && (layer < 0 || layer >= c.n_layers)) return fail(DEC_EINVAL, "bad layer");
   const bool bf = c.mode == DEC_BF16_F16KV;
+  const bool i4 = int4_proj(c) && which < 4;
   const int d = c.d_model, HD = c.n_heads * c.head_dim, F = c.ff_hidden;
   char* Lb = m->packed + m->pl.layer0 + (size_t)(which < 4 ? layer : 0) * m->pl.layer_stride;
   GemvArgs g{};
@@ -1127,10 +1156,19 @@ int dec_debug_product(dec_model* m, int32_t which, int32_t layer, const void* X,
     CUtensorMap tx;
     if (!bf16_map(&tx, X, T, g.K)) return fail(DEC_ECUDA, "tensor map for X failed");
     DEC_CUDA(launch_gemm_tc(g, EPI_QKV_RAW, tw, &tx, m->num_sms, ERR, st));
+  } else if (i4) {
+    DEC_CUDA(launch_gemv_i4(g, EPI_QKV_RAW, st));
   } else {
-    DEC_CUDA(launch_gemv(g, EPI_QKV_RAW, bf, st));
+    DEC_CUDA(launch_gemv(g, EPI_QKV_RAW, serving(c), st));
   }
   m->last_stream = st;
+  return DEC_OK;
+}
+
+int dec_quantize_int4(const float* W, int32_t rows, int32_t K, void* codes, void* scales, void* stream) {
+  if (!W || !codes || !scales || rows < 1 || K < 32 || K % 32) return fail(DEC_EINVAL, "bad arguments");
+  if (((uintptr_t)codes & 15) || ((uintptr_t)scales & 1)) return fail(DEC_EINVAL, "codes need 16-byte alignment");
+  DEC_CUDA(launch_quant_i4(codes, scales, W, rows, K, PACK_IDENTITY, (cudaStream_t)stream));
   return DEC_OK;
 }
 

@@ -105,7 +105,7 @@ int attend_launch(const dec_pool* pool, int32_t layer, int32_t n_seqs, const flo
   a.scale = 1.0f / std::sqrt((float)c.head_dim);
   a.counters = reinterpret_cast<int*>(scratch + L.counters);
   a.err = reinterpret_cast<uint32_t*>(scratch);
-  e = launch_attn_decode(a, L.chunks, c.mode == DEC_BF16_F16KV, st);
+  e = launch_attn_decode(a, L.chunks, c.mode != DEC_FP32, st);
   if (e != cudaSuccess) return fail_msg(DEC_ECUDA, cudaGetErrorString(e));
   return DEC_OK;
 }

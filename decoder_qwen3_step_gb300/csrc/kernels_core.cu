@@ -50,9 +50,6 @@ __global__ void __launch_bounds__(256) k_embed(EmbedArgs a) {
 // once and every token row staged in shared memory is read once per pair of
 // rows.  Token rows go 8 at a time.
 // ---------------------------------------------------------------------------
-constexpr int kGemvRows = 16;
-constexpr int kGemvTok = 8;
-constexpr int kGemvThreads = 256;
 constexpr int kGemvMaxT = kGemvMaxTokens;  // above this the tiled kernel runs
 
 template <typename WT, typename AT, int EPI>

@@ -25,6 +25,10 @@ struct QkvFuse {
 
 // Token rows up to which the weight-streaming kernel runs a product.
 constexpr int kGemvMaxTokens = 32;
+// weight-streaming products: rows per CTA (two per warp), token rows per pass, threads
+constexpr int kGemvRows = 16;
+constexpr int kGemvTok = 8;
+constexpr int kGemvThreads = 256;
 
 // One weight-streaming product Y[t, r] = sum_k X[row(t), k] W[r, k] with a
 // fused epilogue.  W is [rows, K] (fp32 or bf16), X is [*, K] (act type).
@@ -98,6 +102,11 @@ cudaError_t launch_attn_prefill(const AttnArgs& a, int n_work, bool wbf16, cudaS
 // Packing: dst row map modes.
 enum PackMode { PACK_IDENTITY = 0, PACK_GATE = 1, PACK_UP = 2 };
 cudaError_t launch_pack(void* dst, const float* src, int rows, int cols, int mode, bool wbf16, cudaStream_t s);
+// int4 projections (kernels_int4.cu): the product reads codes then scales (rows * K/2 bytes,
+// then rows * K/32 f16 values) at GemvArgs::W; the quantizer writes one source matrix
+// (rows x K f32, row mapping as launch_pack) into such a layout's codes and scales.
+cudaError_t launch_gemv_i4(const GemvArgs& a, int epi, cudaStream_t s);
+cudaError_t launch_quant_i4(void* nib, void* scl, const float* src, int rows, int K, int mode, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 
 // tcgen05 products (bf16 weights and activations): eligible shapes and launch.

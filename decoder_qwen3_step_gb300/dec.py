@@ -13,7 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdec.so")
 
 DEC_OK, DEC_EINVAL, DEC_ECAPACITY, DEC_EBLOCK, DEC_ERANGE, DEC_EVOCAB, DEC_ECUDA, DEC_EDEVICE = range(8)
-DEC_FP32, DEC_BF16_F16KV = 0, 1
+DEC_FP32, DEC_BF16_F16KV, DEC_INT4_F16KV = 0, 1, 2
 DEC_ROWS_ALL, DEC_ROWS_LAST = 0, 1
 DEC_DEV_BAD_ID, DEC_DEV_TIMEOUT, DEC_DEV_CAPACITY = 1, 2, 4
 DEC_PURPOSE_SAMPLE = 4
@@ -33,6 +33,7 @@ EXPORTS = (
     "dec_prefix_key", "dec_pool_set_fill", "dec_pool_register", "dec_pool_lookup", "dec_pool_cached_blocks",
     "dec_child_seed", "dec_rng_stream", "dec_rng_next_u32", "dec_rng_uniform", "dec_sampler_workspace_bytes",
     "dec_sampler_create", "dec_sampler_destroy", "dec_sampler_status", "dec_sample", "dec_debug_df_exp",
+    "dec_quantize_int4",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax",
                   "step")
@@ -133,6 +134,7 @@ def lib() -> C.CDLL:
             "dec_sampler_status": (I, [V, C.POINTER(C.c_uint32)]),
             "dec_sample": (I, [V, V, I64, C.c_int32, C.POINTER(dec_sampling), V, _I32P, _I32P, V, V, V, V]),
             "dec_debug_df_exp": (I, [V, V, I64, V]),
+            "dec_quantize_int4": (I, [V, C.c_int32, C.c_int32, V, V, V]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

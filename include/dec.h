@@ -58,6 +58,17 @@ extern "C" {
 /* ---- numeric modes -------------------------------------------------------- */
 #define DEC_FP32       0 /* fp32 weights, fp32 activations, fp32 KV: parity mode, true fp32 (no TF32) */
 #define DEC_BF16_F16KV 1 /* bf16 weights and GEMM inputs, fp32 accumulation and residual, f16 KV */
+/* int4 projections and bf16 embedding, bf16 GEMM inputs, fp32 accumulation and
+ * residual, f16 KV (tinyllm L10.1 section 2.5 "Int4 weights"): dec_create
+ * quantizes the seven projections of every layer at load, per group of 32
+ * input columns: s = f16(max|W| / 7) (f32 division, one rounding to f16),
+ * q = clamp(rint(W / s), -8, 7) (ties to even), effective weight q * s; two
+ * codes a byte, even column in the low nibble.  Each quantized matrix is its
+ * codes (rows x K/2 bytes) followed by its scales (rows x K/32 f16).  Every
+ * input width must be a multiple of 32.  Products run on CUDA cores with the
+ * codes dequantized in registers; the one-kernel decode step and the tensor-
+ * core products are bf16-only. */
+#define DEC_INT4_F16KV 2
 
 /* which rows of a prefill get logits */
 #define DEC_ROWS_ALL  0 /* every new token (octlm "Proving it's the same model": every position) */
@@ -70,7 +81,7 @@ typedef struct dec_config {
     int32_t vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ff_hidden;
     int32_t max_positions; /* positions 0 .. max_positions-1 are valid; at most 40,960 */
     int32_t block_tokens;  /* KV block size B; 16 */
-    int32_t mode;          /* DEC_FP32 or DEC_BF16_F16KV */
+    int32_t mode;          /* DEC_FP32, DEC_BF16_F16KV or DEC_INT4_F16KV */
     double rope_base;      /* 1e6 for Qwen3 */
     double rms_eps;        /* 1e-6; inside the square root */
     int32_t qk_norm;       /* must be 1 */
@@ -320,6 +331,12 @@ int dec_attend(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float*
  * streams, or from different threads - race: order them on one stream. */
 int dec_attend_noalloc(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float* q, const int32_t* ctx,
                        const int32_t* block_table, int32_t max_blocks, void* out, void* stream);
+
+/* Quantize one f32 matrix to int4 as DEC_INT4_F16KV does at load (tinyllm L10.1
+ * section 2.5): W device [rows, K] f32, K a multiple of 32; codes device
+ * [rows, K/2] bytes (16-byte aligned), scales device [rows, K/32] f16 bits.
+ * Asynchronous on `stream`. */
+int dec_quantize_int4(const float* W, int32_t rows, int32_t K, void* codes, void* scales, void* stream);
 
 /* Test hook: the device conversion the f16 KV store uses (f32 -> f16 round to
  * nearest even, tinyllm L10.1 section 2.3), applied to n device floats. */

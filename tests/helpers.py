@@ -9,8 +9,8 @@ from decoder_qwen3_step_gb300 import dec, inputs
 from oracle.compare import TOL_BF16, TOL_FP32, compare
 from oracle.model import DecoderConfig, Oracle
 
-MODES = {"fp32": dec.DEC_FP32, "bf16": dec.DEC_BF16_F16KV}
-TOLS = {"fp32": TOL_FP32, "bf16": TOL_BF16}
+MODES = {"fp32": dec.DEC_FP32, "bf16": dec.DEC_BF16_F16KV, "int4": dec.DEC_INT4_F16KV}
+TOLS = {"fp32": TOL_FP32, "bf16": TOL_BF16, "int4": TOL_BF16}
 
 
 def make_pair(shape_name, mode, max_positions, max_tokens=4096, max_seqs=64, n_blocks=None, weights=None):
