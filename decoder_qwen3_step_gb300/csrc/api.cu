@@ -90,6 +90,9 @@ int check_config(const dec_config* c) {
   if (c->max_positions > kMaxPositions) return fail(DEC_EINVAL, "max_positions above %d", kMaxPositions);
   if (c->mode == DEC_INT4_F16KV && (c->ff_hidden % 32 || (c->n_heads * c->head_dim) % 32))
     return fail(DEC_EINVAL, "int4 weights need every input width (d_model, n_heads*head_dim, ff_hidden) a multiple of 32");
+  if (c->mode == DEC_INT4_F16KV &&
+      (c->d_model > kInt4MaxK || c->ff_hidden > kInt4MaxK || c->n_heads * c->head_dim > kInt4MaxK))
+    return fail(DEC_EINVAL, "int4 weights: input widths above %d are not supported", kInt4MaxK);
   return DEC_OK;
 }
 

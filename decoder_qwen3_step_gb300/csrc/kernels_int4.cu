@@ -52,7 +52,7 @@ __global__ void k_quant_i4(uint8_t* __restrict__ nib, __half* __restrict__ scl, 
 }
 
 // 16 codes (8 bytes, column order) as floats: the nibble xor 8 is q + 8 in
-// [0, 15]; placed in the mantissa of 2^23 and the offset taken off, exactly.
+// [0, 15]; placed in the mantissa of 2^23, the offset comes off exactly
 __device__ __forceinline__ void unpack16(uint2 q, float* w) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -61,32 +61,49 @@ __device__ __forceinline__ void unpack16(uint2 q, float* w) {
   }
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Weight-streaming product on int4 weights, any number of token rows (8 at a
-// time).  As the bf16 product: a CTA owns 16 consecutive rows, two per warp;
-// each lane takes 16 codes (8 bytes) of both rows per step, so a warp step
-// covers 512 input columns and every code byte comes from HBM once.  The dot
-// product of a 16-code piece is scaled once by its group's scale.
+// time).  A CTA owns 16 consecutive rows (contiguous codes and scales), two
+// per warp.  Its codes and scales are copied to shared memory asynchronously
+// before the wait on the previous kernel: weights do not depend on it, so
+// with programmatic dependent launch the copy overlaps that kernel's tail.
+// Each code byte comes from HBM once, whatever the number of tokens.  A lane
+// takes 16 codes of both rows per step (a warp step covers 512 columns); the
+// dot product of each 16-code piece is scaled once by its group's scale.
 // ---------------------------------------------------------------------------
 template <typename AT, int EPI>
-__global__ void __launch_bounds__(kGemvThreads) k_gemv_i4(GemvArgs a) {
+__global__ void __launch_bounds__(kGemvThreads, 3) k_gemv_i4(GemvArgs a) {
   pdl_launch_next();
-  pdl_wait_prev();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  AT* xs = reinterpret_cast<AT*>(smem_raw);  // [kGemvTok][K]
+  const int K = a.K, KB = K / 2, G = K / kI4Group;
+  uint8_t* cs = smem_raw;                                          // [16][K/2] codes
+  __half* ss = reinterpret_cast<__half*>(smem_raw + kGemvRows * KB);  // [16][K/32] scales
+  AT* xs = reinterpret_cast<AT*>(smem_raw + kGemvRows * KB + kGemvRows * G * 2);  // [kGemvTok][K]
   __shared__ __align__(16) float outs[kGemvTok * kGemvRows];
   __shared__ float rstd_s[kGemvTok];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * kGemvRows;
-  const int K = a.K, KB = K / 2, G = K / kI4Group;
   const uint8_t* Wn = reinterpret_cast<const uint8_t*>(a.W);
-  const __half* Ws = reinterpret_cast<const __half*>(Wn + (size_t)a.rows * KB);
-  const int ra = r0 + warp * 2;
-  const uint8_t* na = Wn + (size_t)ra * KB;
-  const uint8_t* nb = na + KB;
-  const __half* sa = Ws + (size_t)ra * G;
-  const __half* sb = sa + G;
+  const uint8_t* Ws = Wn + (size_t)a.rows * KB;
+  {
+    const uint8_t* src = Wn + (size_t)r0 * KB;
+    for (int i = threadIdx.x; i < kGemvRows * KB / 16; i += kGemvThreads) cp_async16(cs + 16 * i, src + 16 * i);
+    const uint8_t* ssrc = Ws + (size_t)r0 * G * 2;
+    for (int i = threadIdx.x; i < kGemvRows * G * 2 / 16; i += kGemvThreads)
+      cp_async16(reinterpret_cast<uint8_t*>(ss) + 16 * i, ssrc + 16 * i);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  pdl_wait_prev();
   const AT* X = reinterpret_cast<const AT*>(a.X);
+  const uint8_t* na = cs + (warp * 2) * KB;
+  const uint8_t* nb = na + KB;
+  const __half* sa = ss + (warp * 2) * G;
+  const __half* sb = sa + G;
 
   for (int t0 = 0; t0 < a.T; t0 += kGemvTok) {
     const int tc = min(kGemvTok, a.T - t0);
@@ -102,6 +119,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv_i4(GemvArgs a) {
       if (a.ssq) r = row_rstd(a.ssq, a.x_row ? a.x_row[t0 + warp] : t0 + warp, a.d, a.eps);
       if (lane == 0) rstd_s[warp] = r;
     }
+    if (t0 == 0) asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
 
     float acc0[kGemvTok], acc1[kGemvTok];
@@ -111,7 +129,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv_i4(GemvArgs a) {
     for (int k = lane * 16; k < K; k += 512) {
       const uint2 qa = *reinterpret_cast<const uint2*>(na + k / 2);
       const uint2 qb = *reinterpret_cast<const uint2*>(nb + k / 2);
-      const float fa = __half2float(sa[k >> 5]), fb = __half2float(sb[k >> 5]);
+      const float fa = __half2float(sa[k / kI4Group]), fb = __half2float(sb[k / kI4Group]);
       float wa[16], wb[16];
       unpack16(qa, wa);
       unpack16(qb, wb);
@@ -150,14 +168,24 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv_i4(GemvArgs a) {
 template <int EPI>
 static cudaError_t gemv_i4_one(const GemvArgs& a, cudaStream_t s) {
   static int configured = 0;
-  const int smem = (int)((size_t)kGemvTok * a.K * sizeof(bf16));
+  const int smem = (int)((size_t)kGemvRows * (a.K / 2) + (size_t)kGemvRows * (a.K / kI4Group) * 2 +
+                         (size_t)kGemvTok * a.K * sizeof(bf16));
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(k_gemv_i4<bf16, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  k_gemv_i4<bf16, EPI><<<a.rows / kGemvRows, kGemvThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.rows / kGemvRows, 1, 1);
+  cfg.blockDim = dim3(kGemvThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // weight loads overlap the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemv_i4<bf16, EPI>, a);
 }
 
 cudaError_t launch_gemv_i4(const GemvArgs& a, int epi, cudaStream_t s) {

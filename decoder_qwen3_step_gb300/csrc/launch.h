@@ -29,6 +29,7 @@ constexpr int kGemvMaxTokens = 32;
 constexpr int kGemvRows = 16;
 constexpr int kGemvTok = 8;
 constexpr int kGemvThreads = 256;
+constexpr int kInt4MaxK = 4096;  // int4 products keep a lane's codes in registers: input widths up to this
 
 // One weight-streaming product Y[t, r] = sum_k X[row(t), k] W[r, k] with a
 // fused epilogue.  W is [rows, K] (fp32 or bf16), X is [*, K] (act type).

@@ -78,6 +78,8 @@ def main(argv=None):
     ap.add_argument("--ctx", type=int, default=2048)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--graphs", type=int, default=1)
+    ap.add_argument("--mode", choices=["bf16", "int4"], default="bf16", help="weight format of the serving mode")
+    ap.add_argument("--time", action="store_true", help="print the mean ms per measured step (CUDA events)")
     ap.add_argument("--range", action="store_true",
                     help="open a profiler range around the measured loop only (ncu --profile-from-start off)")
     args = ap.parse_args(argv)
@@ -87,7 +89,8 @@ def main(argv=None):
     S, L = args.batch, args.ctx
     max_pos = ((L + args.steps + 16 + 15) // 16) * 16
     blocks = S * ((max_pos + 15) // 16) + 8
-    m = Decoder(shape, inputs.make_weights(shape), mode=dec.DEC_BF16_F16KV, max_positions=max_pos, max_tokens=8192,
+    mode = dec.DEC_INT4_F16KV if args.mode == "int4" else dec.DEC_BF16_F16KV
+    m = Decoder(shape, inputs.make_weights(shape), mode=mode, max_positions=max_pos, max_tokens=8192,
                 max_seqs=max(S, 1), n_blocks=blocks)
     m.set_graphs(bool(args.graphs))
     tables = [m.blocks_for(max_pos) for _ in range(S)]
@@ -99,11 +102,20 @@ def main(argv=None):
             m.prefill([(ids[s], 0, tables[s]) for s in range(g, min(S, g + per))], rows=dec.DEC_ROWS_LAST)
         logits = torch.empty((S, V), dtype=torch.float32, device=m.device)
         buf = [torch.zeros((S,), dtype=torch.int32, device=m.device) for _ in range(2)]
+        for i in range(3 if args.time else 0):  # warm-up steps (graph capture) at the timed positions' shape
+            m.decode([([0], L, tables[s]) for s in range(S)], device_ids=buf[0], out=(logits, buf[1]))
         torch.cuda.synchronize()
         if args.range:
             torch.cuda.cudart().cudaProfilerStart()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
         for i in range(args.steps):
             m.decode([([0], L + i, tables[s]) for s in range(S)], device_ids=buf[i & 1], out=(logits, buf[(i + 1) & 1]))
+        ev[1].record()
+        if args.time:
+            torch.cuda.synchronize()
+            ms = ev[0].elapsed_time(ev[1]) / args.steps
+            print(f"decode {args.mode} batch {S} context {L}: {ms:.3f} ms/step, {S / ms * 1000:.0f} tokens/s")
     else:
         logits = torch.empty((S, V), dtype=torch.float32, device=m.device)
         am = torch.empty((S,), dtype=torch.int32, device=m.device)

@@ -65,7 +65,7 @@ extern "C" {
  * q = clamp(rint(W / s), -8, 7) (ties to even), effective weight q * s; two
  * codes a byte, even column in the low nibble.  Each quantized matrix is its
  * codes (rows x K/2 bytes) followed by its scales (rows x K/32 f16).  Every
- * input width must be a multiple of 32.  Products run on CUDA cores with the
+ * input width must be a multiple of 32 and at most 4096.  Products run on CUDA cores with the
  * codes dequantized in registers; the one-kernel decode step and the tensor-
  * core products are bf16-only. */
 #define DEC_INT4_F16KV 2
