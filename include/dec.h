@@ -403,7 +403,7 @@ double dec_rng_uniform(dec_rng* r);    /* host: one uniform in [0, 1), on the 2^
 typedef struct dec_sampler dec_sampler;
 
 /* Device workspace of a sampler for `vocab` ids and up to `max_seqs`
- * sequences a call (about 26 bytes per id per sequence).  vocab in
+ * sequences a call (about 22 bytes per id per sequence).  vocab in
  * [1, 2^20]; DEC_EINVAL otherwise. */
 int dec_sampler_workspace_bytes(int32_t vocab, int32_t max_seqs, size_t* bytes);
 /* workspace: caller-owned device memory, 256-byte aligned, at least
