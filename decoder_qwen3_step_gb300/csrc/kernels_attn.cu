@@ -107,7 +107,6 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 template <typename KT, typename AT, int D, int G>
 __global__ void __launch_bounds__(kDecWarps * 32) k_attn_decode(AttnArgs a) {
   pdl_launch_next();
-  pdl_wait_prev();
   constexpr int kThreads = kDecWarps * 32, kDim = D / 32;
   const Dims& dm = a.dims;
   const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
@@ -135,9 +134,9 @@ __global__ void __launch_bounds__(kDecWarps * 32) k_attn_decode(AttnArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (warp == 0) {
-    // lane b looks up block b's pool id and issues its two copies: the table
-    // reads are independent, so their latencies overlap
+  // lane b looks up block b's pool id and issues its two copies: the table
+  // reads are independent, so their latencies overlap
+  auto issue = [&]() {
     if (lane == 0) mbar_expect_tx(&bar, 2 * kSlab * nblk);
     __syncwarp();
     if (lane < nblk) {
@@ -146,7 +145,16 @@ __global__ void __launch_bounds__(kDecWarps * 32) k_attn_decode(AttnArgs a) {
       bulk_g2s(Ks + lane * 16 * D, kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D), kSlab, &bar);
       bulk_g2s(Vs + lane * 16 * D, kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D), kSlab, &bar);
     }
-  }
+  };
+  // Every key of a chunk before the last was written by an earlier step (a
+  // decode step writes position ctx - 1 only) and the metadata before this
+  // step's first kernel, so those copies start before the wait on the
+  // previous kernel (programmatic dependent launch: they overlap its tail).
+  // The last chunk holds this step's key: its copy waits; so does Q.
+  const bool old_chunk = c < nch - 1;
+  if (warp == 0 && old_chunk) issue();
+  pdl_wait_prev();
+  if (warp == 0 && !old_chunk) issue();
   for (int i = threadIdx.x; i < G * D; i += kThreads)
     qs[i / D][i % D] = a.Q[((size_t)t * dm.H + g * G + i / D) * D + i % D];
   __syncthreads();
@@ -493,9 +501,17 @@ static cudaError_t attn_decode_t(const AttnArgs& a, int nchunk, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(nchunk, a.dims.Hkv, a.S);
-  k_attn_decode<KT, AT, D, G><<<grid, kDecWarps * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nchunk, a.dims.Hkv, a.S);
+  cfg.blockDim = dim3(kDecWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // older chunks' copies overlap the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attn_decode<KT, AT, D, G>, a);
 }
 
 template <typename KT, typename AT, int D, int G>
