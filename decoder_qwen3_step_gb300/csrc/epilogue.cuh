@@ -137,7 +137,9 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, const float* tile, i
         const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
         key = other > key ? other : key;
       }
-      if (valid && (r & 15) == 0) atomicMax(a.keys + t0 + t, key);
+      // keys only grow: a local maximum at or below the key already stored (read
+      // from L2, possibly stale, so never above the true value) cannot raise it
+      if (valid && (r & 15) == 0 && key > __ldcg(a.keys + t0 + t)) atomicMax(a.keys + t0 + t, key);
     }
   }
 }
