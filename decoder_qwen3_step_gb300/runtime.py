@@ -339,7 +339,9 @@ class Sampler:
                                  C.c_void_p(rng.data_ptr()), C.c_void_p(tokens.data_ptr()),
                                  C.c_void_p(logprobs.data_ptr()), _stream_ptr(stream))
         dec.check(code, "dec_sample")
-        self._keep = hist  # alive until the stream has read it
+        if hist is not None and stream is not None:
+            hist.record_stream(stream)  # the allocator must not reuse it before `stream` has read it
+        self._keep = hist
         return tokens, logprobs
 
     def status(self) -> int:
