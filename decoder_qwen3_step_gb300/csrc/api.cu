@@ -779,8 +779,10 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     // RMSNorm + [Wq;Wk;Wv]
     g.W = Lb + pl.wqkv; g.rows = qkv_rows(c); g.K = d; g.X = XN; g.x_row = nullptr; g.T = N; g.ssq = SSQ;
     g.out_f32 = RAW;
+    // the skinny product fuses QK-norm/RoPE/cache write up to 16 token rows;
+    // from 17 to 32 its raw output and k_qkv_post measure faster
     const bool tc_qkv = bf && m->tc_on && m->tc_ready &&
-                        ((N > kGemvMaxTokens && tc_eligible(g)) || tc_skinny_eligible(g));
+                        ((N > kGemvMaxTokens && tc_eligible(g)) || (N <= kQkvFuseMaxSkinny && tc_skinny_eligible(g)));
     if (tc_qkv) {
       // tensor-core product with QK-norm, RoPE and the cache write in its epilogue
       g.qf = QkvFuse{(const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope), Q,

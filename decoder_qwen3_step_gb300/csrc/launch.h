@@ -25,6 +25,7 @@ struct QkvFuse {
 
 // Token rows up to which the weight-streaming kernel runs a product.
 constexpr int kGemvMaxTokens = 32;
+constexpr int kQkvFuseMaxSkinny = 16;  // decode-size QKV products fuse their epilogue up to this many token rows
 // weight-streaming products: rows per CTA (two per warp), token rows per pass, threads
 constexpr int kGemvRows = 16;
 constexpr int kGemvTok = 8;
