@@ -246,9 +246,9 @@ def our_arm(args, rank, world):
         unit_note = "weight bytes of this projection (bf16), read once per launch"
     achieved = alg_bytes / per_launch_s / 1e9
     # DRAM bytes (read + write) per launch over algorithmic bytes, from one ncu capture of the same
-    # kernel on a smaller case (attention: 32 sequences x 2,050 keys, 278.8 MB for 268.7 MB; the
+    # kernel on a smaller case (attention: 32 sequences x 2,050 keys, 277.6 MB for 268.7 MB; the
     # one-kernel step: batch 1 at context 2,048, 1.441 GB for 1.427 GB), scaled to this launch
-    traffic_ratio = {"attn": 278.8 / 268.7, "step": 1.441 / 1.427}.get(dom_name)
+    traffic_ratio = {"attn": 277.6 / 268.7, "step": 1.441 / 1.427}.get(dom_name)
     traffic = int(alg_bytes * traffic_ratio) if traffic_ratio else None
     roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
