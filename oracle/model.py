@@ -23,7 +23,7 @@ Sources (page title, section):
 * octlm "Proving it's the same model", section "Every logit, every position":
   logits at every position; the cached path splits the prompt in half.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 * QK-norm gains have head_dim entries shared by all heads (this is what the
   published parameter count 596,049,920 requires).
 * RoPE rotates like multiplication of (x_j + i x_{j+D/2}) by exp(i phi_j):
