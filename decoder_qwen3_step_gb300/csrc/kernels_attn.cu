@@ -493,14 +493,10 @@ int prefill_tile_queries(int G) { return kPfRows / G; }
 // ---------------------------------------------------------------------------
 template <typename KT, typename AT, int D, int G>
 static cudaError_t attn_decode_t(const AttnArgs& a, int nchunk, cudaStream_t s) {
-  static bool configured = false;
+  static SmemOptIn opt;
   constexpr size_t smem = decode_smem_bytes<KT, D>();
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_decode<KT, AT, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = opt.ensure(k_attn_decode<KT, AT, D, G>, (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nchunk, a.dims.Hkv, a.S);
   cfg.blockDim = dim3(kDecWarps * 32, 1, 1);
@@ -518,8 +514,8 @@ template <typename KT, typename AT, int D, int G>
 static cudaError_t attn_prefill_t(const AttnArgs& a, int n_work, cudaStream_t s) {
   constexpr int LD = D + 4;
   const size_t smem = ((size_t)kPfRows * LD + 2 * kPfKeys * LD + kPfRows * (kPfKeys + 1)) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<KT, AT, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  static SmemOptIn opt;
+  cudaError_t e = opt.ensure(k_attn_prefill<KT, AT, D, G>, (int)smem);
   if (e != cudaSuccess) return e;
   k_attn_prefill<KT, AT, D, G><<<dim3(n_work, a.dims.Hkv), 128, smem, s>>>(a);
   return cudaGetLastError();

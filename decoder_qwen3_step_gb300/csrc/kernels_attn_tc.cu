@@ -240,14 +240,10 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) k_attn_prefill_tc(AttnArgs a
 
 template <typename AT, int D, int G>
 cudaError_t launch_tc(const AttnArgs& a, int n_work, cudaStream_t s) {
-  static bool configured = false;
+  static SmemOptIn opt;
   constexpr size_t smem = TcLayout<D>::total;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_attn_prefill_tc<AT, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = opt.ensure(k_attn_prefill_tc<AT, D, G>, (int)smem);
+  if (e != cudaSuccess) return e;
   k_attn_prefill_tc<AT, D, G><<<dim3(n_work, a.dims.Hkv), kTcWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -306,23 +306,17 @@ cudaError_t launch_embed(const EmbedArgs& a, bool wbf16, cudaStream_t s) {
 template <typename WT, typename AT, int EPI>
 static cudaError_t gemv_one(const GemvArgs& a, cudaStream_t s) {
   if (a.T <= kGemvMaxT) {
-    static int configured = 0;
+    static SmemOptIn opt;
     const int smem = (int)((size_t)kGemvTok * a.K * sizeof(AT));
-    if (smem > configured) {
-      cudaError_t e = cudaFuncSetAttribute(k_gemv<WT, AT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      configured = smem;
-    }
+    cudaError_t e = opt.ensure(k_gemv<WT, AT, EPI>, smem);
+    if (e != cudaSuccess) return e;
     k_gemv<WT, AT, EPI><<<a.rows / kGemvRows, kGemvThreads, smem, s>>>(a);
     return cudaGetLastError();
   }
-  static bool configured_t = false;
+  static SmemOptIn opt_t;
   const int smem = kTM * (kTN + 4) * (int)sizeof(float);
-  if (!configured_t) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tiled<WT, AT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured_t = true;
-  }
+  cudaError_t e = opt_t.ensure(k_gemm_tiled<WT, AT, EPI>, smem);
+  if (e != cudaSuccess) return e;
   dim3 grid((a.rows + kTN - 1) / kTN, (a.T + kTM - 1) / kTM);
   k_gemm_tiled<WT, AT, EPI><<<grid, kTThreads, smem, s>>>(a);
   return cudaGetLastError();

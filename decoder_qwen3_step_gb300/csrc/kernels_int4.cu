@@ -167,14 +167,11 @@ __global__ void __launch_bounds__(kGemvThreads, 3) k_gemv_i4(GemvArgs a) {
 
 template <int EPI>
 static cudaError_t gemv_i4_one(const GemvArgs& a, cudaStream_t s) {
-  static int configured = 0;
+  static SmemOptIn opt;
   const int smem = (int)((size_t)kGemvRows * (a.K / 2) + (size_t)kGemvRows * (a.K / kI4Group) * 2 +
                          (size_t)kGemvTok * a.K * sizeof(bf16));
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv_i4<bf16, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  cudaError_t e = opt.ensure(k_gemv_i4<bf16, EPI>, smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.rows / kGemvRows, 1, 1);
   cfg.blockDim = dim3(kGemvThreads, 1, 1);

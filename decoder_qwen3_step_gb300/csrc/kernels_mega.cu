@@ -1032,16 +1032,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_mega(const __grid_consta
   }
 }
 
-// Allow the kernel the device's whole opt-in shared memory, once per head size.
+// Allow the kernel the current device's whole opt-in shared memory, once per
+// head size and device (the occupancy check counts on that limit).
 template <int D>
 cudaError_t configure() {
-  static bool done = false;
-  if (done) return cudaSuccess;
+  static SmemOptIn opt;
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decode_mega<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  if (e == cudaSuccess) done = true;
+  if (e == cudaSuccess) e = opt.ensure(k_decode_mega<D>, optin);
   return e;
 }
 

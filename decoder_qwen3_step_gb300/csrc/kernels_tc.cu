@@ -235,13 +235,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <typename AT, int EPI>
 static cudaError_t tc_one(const GemvArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX, int num_sms, uint32_t* err,
                           cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<AT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kTcSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemOptIn opt;
+  cudaError_t e = opt.ensure(k_gemm_tc<AT, EPI>, (int)kTcSmemBytes);
+  if (e != cudaSuccess) return e;
   const int tiles = (a.rows / kTcM) * ((a.T + kTcN - 1) / kTcN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   k_gemm_tc<AT, EPI><<<grid, kTcThreads, kTcSmemBytes, s>>>(*tmW, *tmX, a, err);

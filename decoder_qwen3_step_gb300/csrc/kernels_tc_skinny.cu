@@ -296,15 +296,9 @@ bool tc_skinny_eligible(const GemvArgs& a) {
 template <typename AT, int EPI>
 static cudaError_t skinny_one(const GemvArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX, uint32_t* err,
                               bool pdl, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc_skinny<AT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSkSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_gemm_tc_skinny<AT, EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static SmemOptIn opt;
+  cudaError_t e = opt.ensure(k_gemm_tc_skinny<AT, EPI>, (int)kSkSmemBytes, /*nonportable_cluster=*/true);
+  if (e != cudaSuccess) return e;
   const int ks = skinny_splits(a.rows, a.K);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.rows / kSkM) * ks, 1, 1);

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "optin.h"
 
 namespace dec {
 
@@ -30,7 +31,7 @@ constexpr int kQkvFuseMaxSkinny = 16;  // decode-size QKV products fuse their ep
 constexpr int kGemvRows = 16;
 constexpr int kGemvTok = 8;
 constexpr int kGemvThreads = 256;
-constexpr int kInt4MaxK = 4096;  // int4 products keep a lane's codes in registers: input widths up to this
+constexpr int kInt4MaxK = 4096;  // int4 products stage 16 rows of codes and 8 token rows in shared memory (25 bytes per input column)
 
 // One weight-streaming product Y[t, r] = sum_k X[row(t), k] W[r, k] with a
 // fused epilogue.  W is [rows, K] (fp32 or bf16), X is [*, K] (act type).

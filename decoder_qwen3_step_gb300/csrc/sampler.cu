@@ -63,6 +63,7 @@
 
 #include "../../include/dec.h"
 #include "internal.h"
+#include "optin.h"
 
 namespace {
 
@@ -1592,14 +1593,10 @@ int dec_sampler_create(int32_t vocab, int32_t max_seqs, void* workspace, size_t 
     dec_sampler_destroy(s);
     return sfail(DEC_ECUDA, "workspace clear failed");
   }
-  static bool attr_set[64] = {};  // the attribute is per device
-  const int dev = s->device >= 0 && s->device < 64 ? s->device : 0;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(k_pick, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(PickSmem)) != cudaSuccess) {
-      dec_sampler_destroy(s);
-      return sfail(DEC_ECUDA, "cannot reserve %zu bytes of shared memory for the pick kernel", sizeof(PickSmem));
-    }
-    attr_set[dev] = true;
+  static dec::SmemOptIn pick_optin;
+  if (pick_optin.ensure(k_pick, (int)sizeof(PickSmem)) != cudaSuccess) {
+    dec_sampler_destroy(s);
+    return sfail(DEC_ECUDA, "cannot reserve %zu bytes of shared memory for the pick kernel", sizeof(PickSmem));
   }
   *out = s;
   return DEC_OK;

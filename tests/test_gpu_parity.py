@@ -52,6 +52,26 @@ def test_tiny_full_cached_and_greedy_decode(tiny):
     m.release(t2)
 
 
+def test_tiny_context_filled_to_the_last_position(tiny):
+    """The largest context the model was made for: a 60-token prompt, then
+    greedy decode at positions 60..63, the last row of the RoPE table and the
+    last slot of the fourth (last) 16-token block."""
+    mode, m, orc, w = tiny
+    ids = inputs.make_ids(512, 60, seed=11)
+    table = m.blocks_for(64)
+    assert len(table) == 4
+    lg, am = m.prefill([(ids, 0, table)], rows=dec.DEC_ROWS_LAST)
+    cache = orc.new_cache(64)
+    ref = orc.forward(cache, ids, 0, rows="last")
+    check(np_(lg), np_(am), ref, mode, "prompt of 60")
+    fed, rows = orc.greedy(cache, int(np.argmax(ref[-1])), 60, 4)
+    for i, tok in enumerate(fed):
+        lg, am = m.decode([([tok], 60 + i, table)])
+        check(np_(lg), np_(am), rows[i:i + 1], mode, f"decode at position {60 + i}")
+    assert m.device_status() == 0
+    m.release(table)
+
+
 def test_tiny_embedding_rows_are_bit_exact(tiny):
     mode, m, orc, w = tiny
     ids = inputs.make_ids(512, 16, seed=7)

@@ -140,6 +140,20 @@ def test_parameter_grid_matches_the_oracle(V):
     s.close()
 
 
+@pytest.mark.parametrize("V", [7, 1025, 2049])
+def test_ragged_vocabularies(V):
+    """Vocabularies one past the scan kernels' chunk sizes (1,024 and 2,048
+    ids) and below the 8-id padding: the chunk and padding tails."""
+    rng = np.random.default_rng(50 + V)
+    grid = param_grid(rng, V)
+    ps = [grid[i] for i in rng.choice(len(grid), 32, replace=False)]
+    x = random_logits(rng, len(ps), V) if V > 8 else rng.normal(0, 2, (len(ps), V)).astype(np.float32)
+    hist = [(list(rng.integers(0, V, 6)), list(rng.integers(0, V, 4))) for _ in ps]
+    s = Sampler(V, 32)
+    assert run_and_compare(s, x, ps, hist, [700 + i for i in range(len(ps))], f"V={V}") <= 1
+    s.close()
+
+
 def test_full_qwen3_vocabulary():
     """151,936 ids: the bucket histogram, candidate gathering and the
     multi-chunk final walk at the model's own vocabulary."""
