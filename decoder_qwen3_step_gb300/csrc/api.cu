@@ -174,13 +174,23 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
 constexpr int kStageSlots = 4;
 constexpr size_t kMaxGraphs = 8;
 
+// The two event-record nodes a captured step holds around one launch of a
+// profiled kernel class.
+struct ProfNode {
+  cudaGraphNode_t a, b;
+  int cls;
+};
+
 struct GraphEntry {
   int S;
   int slots;
   const void* logits;
   const void* argmax;
   const void* slabs;
+  uint32_t prof_mask;  // kernel classes profiled when the step was captured
+  cudaGraph_t graph;   // kept while it has profiling nodes: their handles address the executable graph's nodes
   cudaGraphExec_t exec;
+  std::vector<ProfNode> pnodes;
   int64_t n_launch;
   uint64_t last_use;
 };
@@ -228,6 +238,8 @@ struct dec_model {
   cudaStream_t cap_stream;
   std::vector<GraphEntry> graphs;
   uint64_t graph_clock;
+  bool capturing;                   // a decode step is being captured on cap_stream
+  std::vector<ProfRec> cap_recs;    // the profiling events that capture turned into graph nodes
 };
 
 namespace {
@@ -243,6 +255,13 @@ cudaEvent_t take_event(dec_model* m) {
   return e;
 }
 
+// Record a profiling event; inside a capture it becomes an event-record node
+// of the graph, which replays re-point at fresh events.
+cudaError_t record_event(dec_model* m, cudaEvent_t e, cudaStream_t st) {
+  if (!e) return cudaErrorMemoryAllocation;
+  return m->capturing ? cudaEventRecordWithFlags(e, st, cudaEventRecordExternal) : cudaEventRecord(e, st);
+}
+
 // Launch one kernel (expr returns cudaError_t) of class cls on stream st,
 // bracketed by CUDA events when that class is being profiled.
 template <typename F>
@@ -250,14 +269,26 @@ int timed_launch(dec_model* m, int cls, cudaStream_t st, F&& fn, const char* wha
   cudaEvent_t a = nullptr;
   if (m->prof_on[cls]) {
     a = take_event(m);
-    cudaEventRecord(a, st);
+    cudaError_t e = record_event(m, a, st);
+    if (e != cudaSuccess) {
+      if (a) m->ev_free.push_back(a);
+      return fail(DEC_ECUDA, "profiling event: %s", cudaGetErrorString(e));
+    }
   }
   cudaError_t e = fn();
-  if (e != cudaSuccess) return fail(DEC_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    if (a) m->ev_free.push_back(a);
+    return fail(DEC_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+  }
   if (a) {
     cudaEvent_t b = take_event(m);
-    cudaEventRecord(b, st);
-    m->prof_pending.push_back({a, b, cls});
+    e = record_event(m, b, st);
+    if (e != cudaSuccess) {
+      m->ev_free.push_back(a);
+      if (b) m->ev_free.push_back(b);
+      return fail(DEC_ECUDA, "profiling event: %s", cudaGetErrorString(e));
+    }
+    (m->capturing ? m->cap_recs : m->prof_pending).push_back({a, b, cls});
   }
   ++m->launches;
   return DEC_OK;
@@ -508,13 +539,15 @@ void dec_destroy(dec_model* m) {
     }
     if (m->stage[i]) cudaFreeHost(m->stage[i]);
   }
+  for (auto& g : m->graphs) {  // graphs first: their nodes name profiling events
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+  }
   for (auto& r : m->prof_pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
   }
   for (auto e : m->ev_free) cudaEventDestroy(e);
-  for (auto& g : m->graphs)
-    if (g.exec) cudaGraphExecDestroy(g.exec);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   delete m;
 }
@@ -897,34 +930,93 @@ static int enqueue_mega(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   return DEC_OK;
 }
 
-static bool profiling_any(const dec_model* m) {
+static uint32_t prof_mask(const dec_model* m) {
+  uint32_t mask = 0;
   for (int i = 0; i < DEC_K_COUNT; ++i)
-    if (m->prof_on[i]) return true;
-  return false;
+    if (m->prof_on[i]) mask |= 1u << i;
+  return mask;
+}
+
+// The event-record nodes that capture made of the profiling events in recs,
+// paired per launch (the graph's node list has no capture order, so nodes are
+// matched by the event they record).
+static int find_prof_nodes(cudaGraph_t g, const std::vector<dec_model::ProfRec>& recs, std::vector<ProfNode>* out) {
+  size_t n = 0;
+  DEC_CUDA(cudaGraphGetNodes(g, nullptr, &n));
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (n) DEC_CUDA(cudaGraphGetNodes(g, nodes.data(), &n));
+  std::unordered_map<cudaEvent_t, std::pair<size_t, int>> where;  // event -> (record, 0 = a / 1 = b)
+  for (size_t i = 0; i < recs.size(); ++i) {
+    where[recs[i].a] = {i, 0};
+    where[recs[i].b] = {i, 1};
+  }
+  out->assign(recs.size(), ProfNode{nullptr, nullptr, 0});
+  for (size_t i = 0; i < recs.size(); ++i) (*out)[i].cls = recs[i].cls;
+  for (cudaGraphNode_t nd : nodes) {
+    cudaGraphNodeType t;
+    DEC_CUDA(cudaGraphNodeGetType(nd, &t));
+    if (t != cudaGraphNodeTypeEventRecord) continue;
+    cudaEvent_t ev = nullptr;
+    DEC_CUDA(cudaGraphEventRecordNodeGetEvent(nd, &ev));
+    auto it = where.find(ev);
+    if (it == where.end()) continue;
+    ProfNode& p = (*out)[it->second.first];
+    (it->second.second ? p.b : p.a) = nd;
+  }
+  for (const ProfNode& p : *out)
+    if (!p.a || !p.b) return fail(DEC_ECUDA, "a profiling event has no node in the captured step");
+  return DEC_OK;
+}
+
+// Launch a captured step.  Its profiling nodes (if any) first move to fresh
+// events, so each replay's launches are timed like eager ones; launches
+// already queued keep the events they had.
+static int replay_graph(dec_model* m, GraphEntry* g, cudaStream_t st) {
+  for (const ProfNode& p : g->pnodes) {
+    cudaEvent_t a = take_event(m), b = take_event(m);
+    cudaError_t e = (a && b) ? cudaGraphExecEventRecordNodeSetEvent(g->exec, p.a, a) : cudaErrorMemoryAllocation;
+    if (e == cudaSuccess) e = cudaGraphExecEventRecordNodeSetEvent(g->exec, p.b, b);
+    if (e != cudaSuccess) {
+      if (a) m->ev_free.push_back(a);
+      if (b) m->ev_free.push_back(b);
+      return fail(DEC_ECUDA, "profiling node: %s", cudaGetErrorString(e));
+    }
+    m->prof_pending.push_back({a, b, p.cls});
+  }
+  DEC_CUDA(cudaGraphLaunch(g->exec, st));
+  m->launches += g->n_launch;
+  return DEC_OK;
+}
+
+static void drop_graph(GraphEntry& g) {
+  if (g.exec) cudaGraphExecDestroy(g.exec);
+  if (g.graph) cudaGraphDestroy(g.graph);
+  g.exec = nullptr;
+  g.graph = nullptr;
 }
 
 // Decode steps of one shape replay a captured CUDA graph: the per-step
 // metadata lives at fixed device addresses (one host->device copy before the
-// replay), so (S, attention grid, logits, argmax, pool) key a graph.  A key's first step runs
-// eagerly; its second captures.
+// replay), so (S, attention grid, logits, argmax, pool, profiled classes) key
+// a graph.  A key's first step runs eagerly; its second captures.
 static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st) {
+  const uint32_t mask = prof_mask(m);
   GraphEntry* hit = nullptr;
   for (auto& e : m->graphs)
-    if (e.S == sp.S && e.slots == sp.slots && e.logits == sp.logits && e.argmax == sp.argmax && e.slabs == sp.slabs)
+    if (e.S == sp.S && e.slots == sp.slots && e.logits == sp.logits && e.argmax == sp.argmax &&
+        e.slabs == sp.slabs && e.prof_mask == mask)
       hit = &e;
   ++m->graph_clock;
   if (hit && hit->exec) {
     hit->last_use = m->graph_clock;
-    DEC_CUDA(cudaGraphLaunch(hit->exec, st));
-    m->launches += hit->n_launch;
-    return DEC_OK;
+    return replay_graph(m, hit, st);
   }
   if (!hit) {  // first sighting: run eagerly, remember the key
     if (m->graphs.size() >= kMaxGraphs) {
       size_t victim = 0;
       for (size_t i = 1; i < m->graphs.size(); ++i)
         if (m->graphs[i].last_use < m->graphs[victim].last_use) victim = i;
-      if (m->graphs[victim].exec) cudaGraphExecDestroy(m->graphs[victim].exec);
+      drop_graph(m->graphs[victim]);
       m->graphs.erase(m->graphs.begin() + victim);
     }
     GraphEntry e{};
@@ -933,6 +1025,7 @@ static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st
     e.logits = sp.logits;
     e.argmax = sp.argmax;
     e.slabs = sp.slabs;
+    e.prof_mask = mask;
     e.last_use = m->graph_clock;
     m->graphs.push_back(e);
     return enqueue_step(m, sp, st);
@@ -941,9 +1034,20 @@ static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st
   if (!m->cap_stream) DEC_CUDA(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
   const int64_t before = m->launches;
   DEC_CUDA(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+  m->capturing = true;
+  m->cap_recs.clear();
   int rc = enqueue_step(m, sp, m->cap_stream);
+  m->capturing = false;
+  std::vector<dec_model::ProfRec> recs;
+  recs.swap(m->cap_recs);
   cudaGraph_t graph = nullptr;
   cudaError_t ec = cudaStreamEndCapture(m->cap_stream, &graph);
+  std::vector<ProfNode> pnodes;
+  if (!rc && ec == cudaSuccess && !recs.empty()) rc = find_prof_nodes(graph, recs, &pnodes);
+  for (auto& r : recs) {  // the capture's own events never record anything
+    m->ev_free.push_back(r.a);
+    m->ev_free.push_back(r.b);
+  }
   if (rc) {
     if (graph) cudaGraphDestroy(graph);
     return rc;
@@ -951,15 +1055,21 @@ static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st
   if (ec != cudaSuccess) return fail(DEC_ECUDA, "graph capture: %s", cudaGetErrorString(ec));
   cudaGraphExec_t exec = nullptr;
   ec = cudaGraphInstantiate(&exec, graph, 0);
-  cudaGraphDestroy(graph);
-  if (ec != cudaSuccess) return fail(DEC_ECUDA, "graph instantiate: %s", cudaGetErrorString(ec));
+  if (ec != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return fail(DEC_ECUDA, "graph instantiate: %s", cudaGetErrorString(ec));
+  }
+  if (pnodes.empty()) {
+    cudaGraphDestroy(graph);
+    graph = nullptr;
+  }
   hit->exec = exec;
+  hit->graph = graph;
+  hit->pnodes = std::move(pnodes);
   hit->n_launch = m->launches - before;
   m->launches = before;
   hit->last_use = m->graph_clock;
-  DEC_CUDA(cudaGraphLaunch(exec, st));
-  m->launches += hit->n_launch;
-  return DEC_OK;
+  return replay_graph(m, hit, st);
 }
 
 static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_mode, float* logits, int32_t* argmax,
@@ -1079,7 +1189,7 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   DEC_CUDA(cudaEventRecord(m->stage_ev[slot], st));
   m->last_stream = st;
 
-  const bool graph = decode && m->graphs_on && !m->dump && !profiling_any(m);
+  const bool graph = decode && m->graphs_on && !m->dump;
   if (graph && b->ids_device)  // graphs read ids from the metadata block
     DEC_CUDA(cudaMemcpyAsync(dmeta + o_ids, b->ids_device, (size_t)N * 4, cudaMemcpyDeviceToDevice, st));
 

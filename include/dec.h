@@ -265,8 +265,11 @@ int dec_set_tensor_cores(dec_model* m, int32_t on);
 /* Decode steps replay CUDA graphs (on by default): the first step of a given
  * (batch size, logits, argmax, pool) runs eagerly, the second is captured on
  * a private stream, later ones replay it on the caller's stream.  Off: every
- * step launches its kernels one by one.  Graphs are bypassed while a dump or
- * a profiled kernel class is active. */
+ * step launches its kernels one by one.  Graphs are bypassed while a dump is
+ * active.  Profiled kernel classes (dec_profile_enable) stay timed inside
+ * graphs: their events become event-record nodes that each replay points at
+ * fresh events; a step captured with one set of profiled classes replays only
+ * while the same set is enabled. */
 int dec_set_graphs(dec_model* m, int32_t on);
 /* Serving-mode decode steps of at most 8 sequences run as one persistent
  * cooperative kernel, one CTA per SM, with grid-wide barriers between the

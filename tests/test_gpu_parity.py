@@ -255,6 +255,50 @@ def test_graph_replay_matches_eager_decode_bitwise(tiny):
     assert m.device_status() == 0
 
 
+def test_profiled_classes_stay_timed_inside_graph_replays(tiny):
+    """Attention and the LM head profiled while decode steps replay a graph:
+    the logits equal the eager ones bit for bit, and every step (eager,
+    captured or replayed) contributes one timed launch per layer (attention)
+    and one per step (LM head)."""
+    import ctypes as C
+
+    mode, m, orc, w = tiny
+    n_layers = inputs.SHAPES["tiny"]["n_layers"]
+    classes = (dec.KERNEL_CLASSES.index("attn"), dec.KERNEL_CLASSES.index("lmhead"))
+    prompts = [inputs.make_ids(512, n, seed=40 + n) for n in (6, 11)]
+    m.set_megakernel(False)
+    outs, counts = {}, {}
+    for graphs in (False, True):
+        m.set_graphs(graphs)
+        tabs = [m.blocks_for(40) for _ in prompts]
+        m.prefill([(p, 0, t) for p, t in zip(prompts, tabs)], rows=dec.DEC_ROWS_LAST)
+        lg = torch.empty((2, 512), dtype=torch.float32, device=m.device)
+        ids = [torch.empty((2,), dtype=torch.int32, device=m.device) for _ in range(2)]
+        ids[0].fill_(3)
+        for c in classes:
+            dec.check(m.L.dec_profile_enable(m.handle, c, 1), "dec_profile_enable")
+        rows = []
+        for i in range(6):
+            m.decode([([0], len(p) + i, t) for p, t in zip(prompts, tabs)], device_ids=ids[i & 1],
+                     out=(lg, ids[(i + 1) & 1]))
+            rows.append(np_(lg).copy())
+        got = []
+        for c in classes:
+            ms, n = C.c_double(), C.c_int64()
+            dec.check(m.L.dec_profile_read(m.handle, c, C.byref(ms), C.byref(n)), "dec_profile_read")
+            dec.check(m.L.dec_profile_enable(m.handle, c, 0), "dec_profile_enable")
+            assert ms.value > 0.0
+            got.append(n.value)
+        outs[graphs], counts[graphs] = np.stack(rows), got
+        for t in tabs:
+            m.release(t)
+    m.set_graphs(True)
+    m.set_megakernel(True)
+    assert np.array_equal(outs[False], outs[True])
+    assert counts[False] == counts[True] == [6 * n_layers, 6]
+    assert m.device_status() == 0
+
+
 def test_f16_kv_store_rounds_to_nearest_even_bit_exact():
     import ctypes as C
 
