@@ -469,6 +469,11 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
   DEC_CUDA(cudaMemsetAsync((char*)workspace + wl.ERR, 0, 64, s));
   DEC_CUDA(cudaMemsetAsync((char*)workspace + wl.ACNT, 0, (size_t)max_seqs * c.n_kv_heads * 4, s));
   DEC_CUDA(cudaStreamSynchronize(s));
+  int device = 0, num_sms = 0, smem_optin = 0, coop = 0;
+  DEC_CUDA(cudaGetDevice(&device));
+  DEC_CUDA(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device));
+  DEC_CUDA(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device));
+  DEC_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device));
 
   dec_model* m = new dec_model();
   m->cfg = c;
@@ -480,7 +485,7 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
   m->Smax = max_seqs;
   m->MB = max_blocks_of(c);
   m->NCH = max_chunks_of(c);
-  cudaGetDevice(&m->device);
+  m->device = device;
   m->stage_next = 0;
   m->dump = nullptr;
   m->dump_floats = 0;
@@ -491,18 +496,13 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
     m->prof_n[i] = 0;
   }
   m->launches = 0;
-  m->num_sms = 0;
-  cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
-  if (m->num_sms <= 0) m->num_sms = 148;
+  m->num_sms = num_sms;
   m->graphs_on = true;
   m->mega_on = true;
   m->trace = nullptr;
   m->trace_n = 0;
-  m->smem_optin = 0;
-  cudaDeviceGetAttribute(&m->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device);
+  m->smem_optin = smem_optin;
   {
-    int coop = 0;
-    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device);
     const int P = m->num_sms;
     m->mega_shape = c.mode == DEC_BF16_F16KV && coop && P <= kMegaMaxGrid && c.n_heads == 2 * c.n_kv_heads &&
                     (D == 32 || D == 64 || D == 128) && c.block_tokens == 16 && d <= kMegaKSlice && d % 16 == 0 &&
