@@ -398,55 +398,83 @@ def blas_threads():
     return os.cpu_count()
 
 
-def oracle_decode_sample(budget_s=12.0, n_sample=4):
-    """Oracle decode steps on a sample of the headline workload's sequences.
+def _oracle_sample(n_sample, horizon):
+    """The oracle at the headline shape and caches for n_sample of the 32
+    sequences, at their context lengths, with room for `horizon` new tokens.
 
-    The sampled sequences keep their context lengths; their float64 caches are
-    filled with seeded random K/V (the cost of a decode step does not depend
-    on the cached values), so no prefill is timed.  Steps run until the
-    budget is spent; returns tokens/s and a description."""
+    The caches hold seeded random K/V (the cost of a decode step does not
+    depend on the cached values), so no prefill is timed."""
     from decoder_qwen3_step_gb300 import inputs
     from oracle.model import DecoderConfig, Oracle
 
     shape = inputs.SHAPES["qwen3_0p6b"]
     lens = inputs.serving_context_lengths(32)
     pick = [lens[i] for i in np.linspace(0, 31, n_sample).astype(int)]
-    cfg = DecoderConfig(**shape, max_positions=max(pick) + 64)
+    cfg = DecoderConfig(**shape, max_positions=max(pick) + horizon + 1)
     orc = Oracle(cfg, inputs.make_weights(shape), mode="bf16")
     rng = np.random.default_rng(5)
     caches = []
     for L in pick:
-        c = orc.new_cache(L + 64)
+        c = orc.new_cache(L + horizon + 1)
         for l in range(cfg.n_layers):
             c.k[l][:L] = rng.standard_normal((L, cfg.n_kv_heads, cfg.head_dim))
             c.v[l][:L] = rng.standard_normal((L, cfg.n_kv_heads, cfg.head_dim))
             c.written[l][:L] = True
         caches.append(c)
-    tokens, t0 = 0, time.perf_counter()
-    step = 0
-    while True:
-        for c, L in zip(caches, pick):
-            orc.forward(c, [step % cfg.vocab], L + step)
-            tokens += 1
+    return orc, cfg, caches, pick
+
+
+def _oracle_step(orc, cfg, caches, pick, step):
+    """One float64 decode step: one new token for each sampled sequence."""
+    for c, L in zip(caches, pick):
+        orc.forward(c, [step % cfg.vocab], L + step)
+
+
+def oracle_decode_sample(budget_s=12.0, n_sample=4):
+    """Oracle decode steps on a sample of the headline workload's sequences,
+    until the time budget is spent; returns tokens/s and a description."""
+    orc, cfg, caches, pick = _oracle_sample(n_sample, 256)
+    step, t0 = 0, time.perf_counter()
+    while step < 256:
+        _oracle_step(orc, cfg, caches, pick, step)
         step += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return tokens / dt, {"kind": "oracle", "cores": blas_threads(),
-                         "sample": f"{step} float64 decode step(s) of {n_sample} of the 32 sequences "
-                                   f"(contexts {pick}), caches filled with seeded random K/V; {dt:.1f} s"}
+    return n_sample * step / dt, {"kind": "oracle", "cores": blas_threads(),
+                                  "sample": f"{step} float64 decode step(s) of {n_sample} of the 32 sequences "
+                                            f"(contexts {pick}), caches filled with seeded random K/V; {dt:.1f} s"}
+
+
+# One float64 decode token of the 0.6B shape costs about 0.09 s on a 16-core host.
+ORACLE_TOKEN_S = 0.09
 
 
 def reference_arm(args, rank, world):
+    """The oracle as the reference arm: W untimed and K timed steps, a step
+    being one float64 decode token for each of a sample of the 32 sequences
+    (4, fewer when K + W is large, so the run stays near a minute)."""
     if rank != 0:
         return None
-    budget = min(25.0, max(8.0, 2.0 * args.steps))
-    v, info = oracle_decode_sample(budget_s=budget)
-    info["value"] = round(v, 3)
+    n_sample = int(min(4, max(1, 60.0 / ((args.steps + args.warmup) * ORACLE_TOKEN_S))))
+    orc, cfg, caches, pick = _oracle_sample(n_sample, args.warmup + args.steps)
+    for i in range(args.warmup):
+        _oracle_step(orc, cfg, caches, pick, i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_step(orc, cfg, caches, pick, args.warmup + i)
+    dt = time.perf_counter() - t0
+    v = n_sample * args.steps / dt
+    info = {"kind": "oracle", "cores": blas_threads(), "value": round(v, 3),
+            "sample": f"{args.steps} timed float64 decode step(s) after {args.warmup} untimed, each one token "
+                      f"for {n_sample} of the 32 sequences (contexts {pick}), caches filled with seeded random "
+                      f"K/V; {dt:.1f} s"}
     return {"metric": METRIC, "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD, "batch": 32, "parallelism": "host cores"},
+            "config": {"workload": WORKLOAD, "batch": 32, "sampled_sequences": n_sample,
+                       "parallelism": "host cores"},
             "cpu_baseline": info,
             "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
