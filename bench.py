@@ -464,7 +464,7 @@ def reference_arm(args, rank, world):
     for i in range(args.steps):
         _oracle_step(orc, cfg, caches, pick, args.warmup + i)
     dt = time.perf_counter() - t0
-    v = n_sample * args.steps / dt
+    v = n_sample * args.steps / max(dt, 1e-9)
     info = {"kind": "oracle", "cores": blas_threads(), "value": round(v, 3),
             "sample": f"{args.steps} timed float64 decode step(s) after {args.warmup} untimed, each one token "
                       f"for {n_sample} of the 32 sequences (contexts {pick}), caches filled with seeded random "
