@@ -130,9 +130,11 @@ PackedLayout packed_layout(const dec_config& c) {
 }
 
 struct WsLayout {
-  size_t X, XN, SSQ, RAW, Q, ATT, ACT, PART, ACNT, META, KEYS, ERR, SSQP, MSYNC, total;
+  size_t X, XN, SSQ, RAW, Q, ATT, ACT, PART, ACNT, META, KEYS, ERR, MSYNC, FLOW, total;
   size_t meta_ints;
   size_t msync_bytes;
+  // the one-kernel decode step's hand-over buffers (offsets within FLOW)
+  size_t f_xa, f_xb, f_sa, f_sb, f_raw, f_att, f_act, f_rec, flow_bytes;
 };
 
 // 64-key chunks of the longest context (the one-kernel decode step's split).
@@ -150,9 +152,7 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
   L.Q = take((size_t)T * HD * 4);
   L.ATT = take((size_t)T * HD * a);
   L.ACT = take((size_t)T * c.ff_hidden * a);
-  const size_t part_recs = std::max((size_t)S * max_chunks_of(c),
-                                     (size_t)std::min(S, kMegaMaxTokens) * max_chunks64_of(c));
-  L.PART = take(part_recs * c.n_heads * (c.head_dim + 2) * 4);
+  L.PART = take((size_t)S * max_chunks_of(c) * c.n_heads * (c.head_dim + 2) * 4);
   L.ACNT = take((size_t)S * c.n_kv_heads * 4);
   // ids, tok_pos, tok_seq, row_tok [T]; seq_start [S+1]; seq_ctx [S]; tables [S*MB]; then either the
   // prefill tiles [3*(T+S)] or the decode work list [1 + 2*S*chunks]
@@ -161,12 +161,25 @@ WsLayout ws_layout(const dec_config& c, int T, int S) {
   L.META = take(L.meta_ints * 4);
   L.KEYS = take((size_t)T * 8);
   L.ERR = take(64);
-  // one-kernel decode step: per-CTA partial sums of x^2, then one block that
-  // is cleared before every launch (barrier counter | chunk counters | argmax keys)
+  // one-kernel decode step: one block cleared before every launch (sync
+  // counter | finished CTAs | abort word | argmax keys | chunk counters),
+  // then the buffers its CTAs hand over to each other
   const size_t Tm = (size_t)std::min(T, kMegaMaxTokens);
-  L.SSQP = take(Tm * kMegaMaxGrid * 4);
-  L.msync_bytes = 256 + align256(Tm * c.n_kv_heads * 4) + align256(Tm * 8);
+  L.msync_bytes = 256 + align256(Tm * 8) + align256(Tm * c.n_kv_heads * 4);
   L.MSYNC = take(L.msync_bytes);
+  size_t fo = 0;
+  auto ftake = [&](size_t bytes) { size_t o = fo; fo = align256(fo + bytes); return o; };
+  const size_t D = c.head_dim;
+  L.f_xa = ftake(Tm * d * 2);
+  L.f_xb = ftake(Tm * d * 2);
+  L.f_sa = ftake(Tm * kMegaMaxGrid * 4);
+  L.f_sb = ftake(Tm * kMegaMaxGrid * 4);
+  L.f_raw = ftake(Tm * qkv_rows(c) * 4);
+  L.f_att = ftake(Tm * HD * 2);
+  L.f_act = ftake(Tm * c.ff_hidden * 2);
+  L.f_rec = ftake(Tm * c.n_kv_heads * max_chunks64_of(c) * 2 * (D + 2) * 4);
+  L.flow_bytes = fo;
+  L.FLOW = take(L.flow_bytes);
   L.total = off;
   return L;
 }
@@ -230,6 +243,9 @@ struct dec_model {
   // the one-kernel decode step
   bool mega_on;
   bool mega_shape;  // the shape and device allow it
+  const void* kvmap_slabs;  // the pool the one-kernel step's KV tensor map was made for
+  int kvmap_blocks;
+  CUtensorMap kvmap;
   unsigned long long* trace;  // per-stage timer stamps of the one-kernel step (or null)
   size_t trace_n;
   int smem_optin;
@@ -333,6 +349,22 @@ bool bf16_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, u
   return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D f16 tensor map of the KV pool as [rows, D] (a row: one slot of one KV
+// head of one block of one layer, K or V), box 16 rows x min(D, 64) columns;
+// 128-byte swizzle when a box row is 128 bytes.
+bool kv_map(CUtensorMap* out, const void* slabs, uint64_t rows, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint32_t bd = D >= 64 ? 64u : (uint32_t)D;
+  cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {bd, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(slabs), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, bd == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Tensor maps for the tcgen05 products (serving mode only); false leaves the
@@ -499,16 +531,23 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
   m->num_sms = num_sms;
   m->graphs_on = true;
   m->mega_on = true;
+  m->kvmap_slabs = nullptr;
+  m->kvmap_blocks = 0;
   m->trace = nullptr;
   m->trace_n = 0;
   m->smem_optin = smem_optin;
   {
     const int P = m->num_sms;
+    const int kmax = std::max(d, std::max(H * D, F));
+    const MegaSmem ms = mega_smem(kMegaMaxTokens, kmax, D, m->smem_optin);
+    // every product's tiles of one group must fit in the ring together: two
+    // 16-row tiles, or one tile of each 1024-wide slice of the widest input
+    const int slice_foot = 16 * (kMegaKSlice * 2 + 16);
+    const int nks_max = (std::max(H * D, F) + kMegaKSlice - 1) / kMegaKSlice;
     m->mega_shape = c.mode == DEC_BF16_F16KV && coop && P <= kMegaMaxGrid && c.n_heads == 2 * c.n_kv_heads &&
-                    (D == 32 || D == 64 || D == 128) && c.block_tokens == 16 && d <= kMegaKSlice && d % 16 == 0 &&
-                    (H * D) % 16 == 0 && F % 16 == 0 && (d + P - 1) / P <= 16 &&
-                    mega_slots(kMegaMaxTokens, D, (size_t)m->smem_optin) >= 2 &&
-                    mega_fits(kMegaMaxTokens, D, mega_slots(kMegaMaxTokens, D, (size_t)m->smem_optin));
+                    (D == 32 || D == 64 || D == 128) && c.block_tokens == 16 && d <= kMegaKSlice && d % 64 == 0 &&
+                    (H * D) % 64 == 0 && F % 64 == 0 && d <= 16 * P && 5 * c.n_layers <= 255 && ms.total > 0 &&
+                    ms.ring >= std::max(2, nks_max) * slice_foot + 1024 && mega_fits(D, ms.total);
   }
   m->tc_on = true;
   m->tc_ready = build_tensor_maps(m);
@@ -877,7 +916,6 @@ static int enqueue_mega(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   const WsLayout& wl = m->wl;
   const PackedLayout& pl = m->pl;
   DEC_CUDA(cudaMemsetAsync(ws + wl.MSYNC, 0, wl.msync_bytes, st));
-  const size_t Tm = (size_t)std::min(m->Tmax, kMegaMaxTokens);
   MegaArgs a{};
   a.layers = m->packed + pl.layer0;
   a.layer_stride = pl.layer_stride;
@@ -911,22 +949,43 @@ static int enqueue_mega(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   a.tables = sp.meta.tables;
   a.item_start = sp.meta.work;
   a.X = (float*)(ws + wl.X);
-  a.XN = (bf16*)(ws + wl.XN);
-  a.RAW = (float*)(ws + wl.RAW);
-  a.ATT = (bf16*)(ws + wl.ATT);
-  a.ACT = (bf16*)(ws + wl.ACT);
-  a.SSQP = (float*)(ws + wl.SSQP);
-  a.PART = (float*)(ws + wl.PART);
+  char* fl = ws + wl.FLOW;
+  a.xa = (bf16*)(fl + wl.f_xa);
+  a.xb = (bf16*)(fl + wl.f_xb);
+  a.sa = (float*)(fl + wl.f_sa);
+  a.sb = (float*)(fl + wl.f_sb);
+  a.raw = (float*)(fl + wl.f_raw);
+  a.att = (bf16*)(fl + wl.f_att);
+  a.act = (bf16*)(fl + wl.f_act);
+  a.rec = (float*)(fl + wl.f_rec);
   a.nch_cap = max_chunks64_of(c);
-  a.bar = (unsigned int*)(ws + wl.MSYNC);
-  a.acnt = (int*)(ws + wl.MSYNC + 256);
-  a.keys = (unsigned long long*)(ws + wl.MSYNC + 256 + align256(Tm * c.n_kv_heads * 4));
+  const size_t Tm = (size_t)std::min(m->Tmax, kMegaMaxTokens);
+  char* ms0 = ws + wl.MSYNC;
+  a.sync = (unsigned int*)ms0;
+  a.done = (unsigned int*)(ms0 + 64);
+  a.abort = (unsigned int*)(ms0 + 128);
+  a.keys = (unsigned long long*)(ms0 + 256);
+  a.acnt = (unsigned int*)(ms0 + 256 + align256(Tm * 8));
   a.logits = sp.logits;
   a.argmax = sp.argmax;
   a.err = (uint32_t*)(ws + wl.ERR);
-  a.nslots = mega_slots(sp.N, c.head_dim, (size_t)m->smem_optin);
+  const int kmax = std::max(c.d_model, std::max(c.n_heads * c.head_dim, c.ff_hidden));
+  const MegaSmem ms = mega_smem(sp.N, kmax, c.head_dim, m->smem_optin);
+  if (!ms.total) return fail(DEC_ECUDA, "the one-kernel step does not fit in shared memory");
+  a.ring = ms.ring;
+  a.o_stage = ms.o_stage;
+  a.o_scr = ms.o_scr;
+  a.o_small = ms.o_small;
+  a.o_bars = ms.o_bars;
   a.trace = m->trace && m->trace_n >= (size_t)m->num_sms * kMegaTraceStride ? m->trace : nullptr;
-  DEC_LAUNCH(DEC_K_STEP, launch_decode_mega(a, m->num_sms, st));
+  if (m->kvmap_slabs != sp.slabs || m->kvmap_blocks != sp.dm.n_blocks) {
+    const uint64_t rows = (uint64_t)c.n_layers * sp.dm.n_blocks * 2 * c.n_kv_heads * c.block_tokens;
+    if (!kv_map(&m->kvmap, sp.slabs, rows, c.head_dim)) return fail(DEC_ECUDA, "tensor map of the KV pool failed");
+    m->kvmap_slabs = sp.slabs;
+    m->kvmap_blocks = sp.dm.n_blocks;
+  }
+  a.tm_kv = m->kvmap;
+  DEC_LAUNCH(DEC_K_STEP, launch_decode_mega(a, m->num_sms, ms.total, st));
   return DEC_OK;
 }
 

@@ -1,6 +1,7 @@
 // launch.h - host-side launchers of the decoder kernels (internal to libdec).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -135,21 +136,21 @@ bool attn_prefill_tc_eligible(const AttnArgs& a);
 cudaError_t launch_attn_prefill_tc(const AttnArgs& a, int n_work, cudaStream_t s);
 
 // ---- the whole decode step in one persistent kernel (serving mode) -----------
-constexpr int kMegaComputeWarps = 16;                 // + one loader warp
+constexpr int kMegaComputeWarps = 8;                  // + one loader warp
 constexpr int kMegaKSlice = 1024;                     // k elements per weight tile
-constexpr int kMegaRowStride = kMegaKSlice * 2 + 16;  // bytes between staged rows (padded)
-constexpr int kMegaSlotBytes = 16 * kMegaRowStride;   // one ring slot: 16 weight rows
 constexpr int kMegaKeys = 64;                         // cached keys per attention tile
-constexpr int kMegaMaxSlots = 8;
-constexpr int kMegaMaxTokens = 32;                    // sequences per step the kernel supports
-// Steps of at most this many sequences take the one-kernel path by default:
-// measured on GB300 at context 2048 it is ahead up to 8 sequences (8% at 1,
-// 3% at 8) and behind the per-operation kernels from 16.
+constexpr int kMegaTiles = 32;                        // ring tiles in flight at most (mbarrier pairs)
+constexpr int kMegaMaxTokens = 8;                     // sequences per step the kernel supports
+// Steps of at most this many sequences take the one-kernel path by default.
 constexpr int kMegaAutoTokens = 8;
 constexpr int kMegaMaxGrid = 256;                     // CTAs (one per SM) the partial sums are sized for
 constexpr int kMegaTraceStride = 320;                 // trace stamps per CTA (the last: the loader's end)
+constexpr int kMegaMinRing = 128 * 1024;              // smallest weight/KV ring worth running with
 
 struct MegaArgs {
+  // the KV pool as a 2-D f16 tensor [layers * blocks * 2 * Hkv * 16 rows, D]:
+  // boxes of 16 rows x min(D, 64) columns, 128-byte swizzle when D >= 64
+  CUtensorMap tm_kv;
   // packed weights: layer 0 at `layers`, then every layer_stride bytes
   const char* layers;
   size_t layer_stride;
@@ -168,30 +169,40 @@ struct MegaArgs {
   const int32_t* seq_ctx;     // [T] context length after this token
   const int32_t* tables;      // [T, max_blocks]
   const int32_t* item_start;  // [T+1] first attention item of each sequence (Hkv * 64-key chunks each)
-  // workspace
-  float* X;                   // [T, d] residual
-  bf16* XN;                   // [T, d] next product input
-  float* RAW;                 // [T, (H+2Hkv)*D] q|k|v before QK-norm/RoPE
-  bf16* ATT;                  // [T, H*D]
-  bf16* ACT;                  // [T, F]
-  float* SSQP;                // [T, grid] per-CTA partial sums of x^2
-  float* PART;                // [T, H, nch_cap, D+2] chunk records
+  float* X;                   // [T, d] residual; each CTA reads and writes only the rows it owns
+  // buffers other CTAs read (each written once per stage, read after a sync)
+  bf16* xa;                   // [T, d]  x * next gain after the down projection (QKV and LM-head input)
+  bf16* xb;                   // [T, d]  the same after the O projection (gate/up input)
+  float* sa;                  // [T, kMegaMaxGrid] per-CTA sums of x^2 paired with xa
+  float* sb;                  // [T, kMegaMaxGrid] paired with xb
+  float* raw;                 // [T, (H+2Hkv)*D] q|k|v before QK-norm/RoPE
+  bf16* att;                  // [T, H*D] attention output
+  bf16* act;                  // [T, F] silu(gate)*up
+  float* rec;                 // [T, Hkv, nch_cap, 2*(D+2)] per-chunk records: per head max, sum, values
   int nch_cap;
-  unsigned int* bar;          // grid barrier counter, zero at launch
-  int* acnt;                  // [T, Hkv] finished chunks, zero at launch
+  unsigned int* sync;         // CTAs arrived, summed over the step's sync points; zero at launch
+  unsigned int* acnt;         // [T, Hkv] chunks recorded, summed over layers; zero at launch
+  unsigned int* done;         // CTAs finished; zero at launch
+  unsigned int* abort;        // set by a CTA that gave up; zero at launch
   unsigned long long* keys;   // [T] argmax keys, zero at launch
   float* logits;              // [T, vocab] or null
   int32_t* argmax;            // [T]
   uint32_t* err;
-  int nslots;
+  // dynamic shared memory: ring of `ring` bytes at 0, then the other regions
+  int ring, o_stage, o_scr, o_small, o_bars;
   unsigned long long* trace;  // null, or [grid, kMegaTraceStride] global-timer stamps
 };
 
-size_t mega_smem_bytes(int T, int nslots, int D);
-int mega_slots(int T, int D, size_t smem_limit);
+// Shared-memory plan of the kernel for T tokens, product inputs up to kmax
+// wide and head size D: the largest ring (a multiple of 1 KB) that fits in
+// `smem_limit` bytes.  total == 0 if not even kMegaMinRing fits.
+struct MegaSmem {
+  int ring, o_stage, o_scr, o_small, o_bars, total;
+};
+MegaSmem mega_smem(int T, int kmax, int D, int smem_limit);
 int mega_threads();
-// Whether one CTA of the kernel for head size D fits on an SM at T tokens.
-bool mega_fits(int T, int D, int nslots);
-cudaError_t launch_decode_mega(const MegaArgs& a, int grid, cudaStream_t s);
+// Whether one CTA of the kernel for head size D fits on an SM with `smem` bytes.
+bool mega_fits(int D, int smem);
+cudaError_t launch_decode_mega(const MegaArgs& a, int grid, int smem, cudaStream_t s);
 
 }  // namespace dec

@@ -272,18 +272,24 @@ int dec_set_tensor_cores(dec_model* m, int32_t on);
  * while the same set is enabled. */
 int dec_set_graphs(dec_model* m, int32_t on);
 /* Serving-mode decode steps of at most 8 sequences run as one persistent
- * cooperative kernel, one CTA per SM, with grid-wide barriers between the
- * dependent stages of every layer (on by default).  Off: the per-operation
- * kernels above, one launch each.  The per-layer dump and CUDA graphs do
- * not apply to the one-kernel step.  Same tolerances as the other paths. */
+ * cooperative kernel, one CTA per SM (on by default): a loader warp streams
+ * the CTA's weight rows and cached keys into a shared-memory ring while the
+ * compute warps run the stages; between dependent stages each CTA counts its
+ * outputs in on a step-wide counter and waits for every CTA's (attention
+ * records: per sequence and KV head).  Off: the per-operation kernels above,
+ * one launch each.  The per-layer dump and CUDA graphs do not apply to the
+ * one-kernel step.  Same tolerances as the other paths. */
 int dec_set_megakernel(dec_model* m, int32_t on);
 /* Profiling aid for the one-kernel step: while `stamps` is set (DEVICE
  * memory, uint64 [n], n >= number of SMs x 320), every such step writes, per
- * CTA b, the global timer (ns) at stamps[b*320 + k]: k = 0 at the start, then
- * for each of its grid barriers in order (embedding, 5 per layer, LM head)
- * one stamp when the CTA's share of the stage is done and one when the
- * barrier releases; stamps[b*320 + 319] is when the CTA's loader warp issued
- * its last tile.  NULL turns it off.  DEC_EINVAL if n is too small. */
+ * CTA b, the global timer (ns) at stamps[b*320 + k]: k = 0 at the start; for
+ * stage s (5 per layer: QKV, attention, O projection, gate/up, down; then the
+ * LM head at s = 5 * n_layers) k = 1 + 2s once the stage's inputs are in
+ * shared memory and k = 2 + 2s once its outputs are counted in; k = 284..308
+ * points inside layer 1's stages (5 per stage); k = 310..315 when the loader
+ * issued the first tile of layer 1's stages and of layer 2's QKV; k = 319
+ * when the loader issued its last tile.  NULL turns it off.  DEC_EINVAL if n
+ * is too small. */
 int dec_set_step_trace(dec_model* m, uint64_t* stamps, size_t n);
 /* *available = 1 when this model's shape and device can run the one-kernel
  * decode step (serving mode, two query heads per KV head, head_dim 32, 64 or
