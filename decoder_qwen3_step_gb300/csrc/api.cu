@@ -243,6 +243,8 @@ struct dec_model {
   // the one-kernel decode step
   bool mega_on;
   bool mega_shape;  // the shape and device allow it
+  uint32_t wait_extra;         // test hook of the one-kernel step's hand-off waits
+  uint64_t wait_limit;
   const void* kvmap_slabs;  // the pool the one-kernel step's KV tensor map was made for
   int kvmap_blocks;
   CUtensorMap kvmap;
@@ -532,6 +534,8 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
   m->graphs_on = true;
   m->mega_on = true;
   m->kvmap_slabs = nullptr;
+  m->wait_extra = 0;
+  m->wait_limit = 1000000000ull;
   m->kvmap_blocks = 0;
   m->trace = nullptr;
   m->trace_n = 0;
@@ -551,6 +555,13 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
   }
   m->tc_on = true;
   m->tc_ready = build_tensor_maps(m);
+  // dec_attend_noalloc's array on this device: resolved here, so that its
+  // later calls on the device do no set-up (the first resolution loads the
+  // module that holds the array, which allocates it under lazy loading)
+  if (noalloc_prepare() != DEC_OK) {
+    dec_destroy(m);
+    return fail(DEC_ECUDA, "the no-allocation attention array could not be resolved");
+  }
   m->cap_stream = nullptr;
   m->graph_clock = 0;
   for (int i = 0; i < kStageSlots; ++i) {
@@ -645,6 +656,15 @@ int dec_set_step_trace(dec_model* m, uint64_t* stamps, size_t n) {
     return fail(DEC_EINVAL, "the trace needs %zu stamps", (size_t)m->num_sms * kMegaTraceStride);
   m->trace = (unsigned long long*)stamps;
   m->trace_n = stamps ? n : 0;
+  return DEC_OK;
+}
+
+int dec_debug_wait_timeout(dec_model* m, uint32_t extra, uint64_t limit_ns) {
+  if (!m) return fail(DEC_EINVAL, "NULL model");
+  if (extra && (limit_ns < 1000 || limit_ns > 1000000000ull))
+    return fail(DEC_EINVAL, "the test limit must lie between 1 us and 1 s");
+  m->wait_extra = extra;
+  m->wait_limit = extra ? limit_ns : 1000000000ull;
   return DEC_OK;
 }
 
@@ -985,6 +1005,8 @@ static int enqueue_mega(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     m->kvmap_blocks = sp.dm.n_blocks;
   }
   a.tm_kv = m->kvmap;
+  a.wait_extra = m->wait_extra;
+  a.wait_limit = m->wait_limit;
   DEC_LAUNCH(DEC_K_STEP, launch_decode_mega(a, m->num_sms, ms.total, st));
   return DEC_OK;
 }
@@ -1131,21 +1153,22 @@ static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st
   return replay_graph(m, hit, st);
 }
 
-static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_mode, float* logits, int32_t* argmax,
-                    cudaStream_t st, bool decode) {
-  if (!m || !pool || !b || !argmax) return fail(DEC_EINVAL, "NULL argument");
-  const dec_config& c = m->cfg;
-  if (!same_shape(c, pool->cfg)) return fail(DEC_EINVAL, "pool was made for another decoder shape or mode");
-  if (rows_mode != DEC_ROWS_ALL && rows_mode != DEC_ROWS_LAST) return fail(DEC_EINVAL, "bad rows mode");
+// Every check a step makes before it launches anything, host data only
+// (tinyllm L10.1 section 4, forward_refuses_bad_batches: a scheduler's
+// mistake surfaces as an error instead of corrupting the cache).  The blocks
+// a sequence writes (positions p0 .. its last new position) must belong to it
+// alone: refcount 1, not indexed in the prefix cache, and named by no other
+// written position of the batch.
+static int check_batch(const dec_config& c, const dec_pool* pool, const dec_batch* b, bool decode) {
+  if (!b) return fail(DEC_EINVAL, "NULL argument");
   const int S = b->n_seqs, N = b->n_tokens;
   if (S < 1 || N < 1) return fail(DEC_EINVAL, "empty step: %d sequences, %d tokens", S, N);
-  if (S > m->Smax || N > m->Tmax)
-    return fail(DEC_ERANGE, "step of %d tokens / %d sequences exceeds the workspace (%d / %d)", N, S, m->Tmax, m->Smax);
   if (decode && N != S) return fail(DEC_EINVAL, "decode takes exactly one token per sequence");
   if (!b->seq_start || !b->positions || !b->block_table || (!b->ids && !b->ids_device))
     return fail(DEC_EINVAL, "NULL batch array");
   if (b->seq_start[0] != 0 || b->seq_start[S] != N) return fail(DEC_EINVAL, "seq_start must run from 0 to n_tokens");
   const int B = c.block_tokens;
+  std::vector<int32_t> written;
   for (int s = 0; s < S; ++s) {
     const int a0 = b->seq_start[s], a1 = b->seq_start[s + 1];
     if (a1 <= a0) return fail(DEC_EINVAL, "sequence %d has no new tokens", s);
@@ -1165,8 +1188,32 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
       const int id = b->block_table[(size_t)s * b->max_blocks + i];
       if (id < 0 || id >= pool->n_blocks || pool->refs[id] <= 0)
         return fail(DEC_EBLOCK, "sequence %d names block %d which is not allocated", s, id);
+      if (i >= p0 / B) {  // this step writes K/V into block i
+        if (pool->refs[id] != 1 || pool->registered[id])
+          return fail(DEC_EBLOCK, "sequence %d would write block %d, which is shared (refcount %d) or in the prefix cache",
+                      s, id, pool->refs[id]);
+        written.push_back(id);
+      }
     }
   }
+  std::sort(written.begin(), written.end());
+  const auto dup = std::adjacent_find(written.begin(), written.end());
+  if (dup != written.end()) return fail(DEC_EBLOCK, "block %d would be written for two positions of the step", *dup);
+  return DEC_OK;
+}
+
+static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_mode, float* logits, int32_t* argmax,
+                    cudaStream_t st, bool decode) {
+  if (!m || !pool || !b || !argmax) return fail(DEC_EINVAL, "NULL argument");
+  const dec_config& c = m->cfg;
+  if (!same_shape(c, pool->cfg)) return fail(DEC_EINVAL, "pool was made for another decoder shape or mode");
+  if (rows_mode != DEC_ROWS_ALL && rows_mode != DEC_ROWS_LAST) return fail(DEC_EINVAL, "bad rows mode");
+  const int S = b->n_seqs, N = b->n_tokens;
+  if (S > m->Smax || N > m->Tmax)
+    return fail(DEC_ERANGE, "step of %d tokens / %d sequences exceeds the workspace (%d / %d)", N, S, m->Tmax, m->Smax);
+  int rc = check_batch(c, pool, b, decode);
+  if (rc) return rc;
+  const int B = c.block_tokens;
   const int R = rows_mode == DEC_ROWS_ALL ? N : S;
   int max_ctx = 0;
   for (int s = 0; s < S; ++s) max_ctx = std::max(max_ctx, b->positions[b->seq_start[s + 1] - 1] + 1);
@@ -1279,6 +1326,11 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   if (mega) return enqueue_mega(m, sp, st);
   if (graph) return launch_decode_graph(m, sp, st);
   return enqueue_step(m, sp, st);
+}
+
+int dec_batch_check(const dec_pool* pool, const dec_batch* b, int32_t decode) {
+  if (!pool) return fail(DEC_EINVAL, "NULL argument");
+  return check_batch(pool->cfg, pool, b, decode != 0);
 }
 
 int dec_prefill(dec_model* m, dec_pool* pool, const dec_batch* b, int32_t rows, float* logits, int32_t* argmax,

@@ -146,6 +146,13 @@ int noalloc_scratch(char** out) {
 
 }  // namespace
 
+// Resolve the no-allocation array's address on the current device now (the
+// first resolution on a device loads the module that holds the array).
+int dec::noalloc_prepare() {
+  char* p = nullptr;
+  return noalloc_scratch(&p);
+}
+
 extern "C" {
 
 int dec_attend_scratch_bytes(const dec_config* cfg, int32_t n_seqs, int32_t max_ctx, int32_t max_blocks,
@@ -168,6 +175,23 @@ int dec_attend(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float*
   for (int s = 0; s <= n_seqs; ++s) seq_start[s] = s;
   return attend_launch(pool, layer, n_seqs, q, ctx, block_table, max_blocks, out, (char*)scratch, L,
                        seq_start.data(), (cudaStream_t)stream);
+}
+
+int dec_attend_noalloc_status(void* stream, uint32_t* flags) {
+  if (!flags) return fail_msg(DEC_EINVAL, "NULL argument");
+  char* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t v = 0;
+  // the error word is the array's first word (the layout dec_attend uses)
+  cudaError_t e = cudaMemcpyAsync(&v, scratch, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, 4, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail_msg(DEC_ECUDA, cudaGetErrorString(e));
+  *flags = v;
+  return DEC_OK;
 }
 
 int dec_attend_noalloc(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float* q, const int32_t* ctx,

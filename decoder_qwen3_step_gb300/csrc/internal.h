@@ -30,4 +30,7 @@ struct dec_pool {
 namespace dec {
 // Record `msg` as the thread's last error and return `code`.
 int set_error(int code, const char* msg);
+// Look up the device address of dec_attend_noalloc's array on the current
+// device (attend.cu); DEC_OK or an error code.
+int noalloc_prepare();
 }  // namespace dec

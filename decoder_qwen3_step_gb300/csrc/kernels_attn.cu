@@ -7,8 +7,10 @@
 // position j of a sequence is slot j % B of block table[j / B].
 //
 // Decode (one query per sequence): split-K over fixed 64-key chunks (the split
-// never depends on the batch), one warp per 16-key block, warp-shuffle softmax,
-// then a second kernel merges the chunk partials in chunk order.
+// never depends on the batch), one warp per 16-key block, warp-shuffle softmax;
+// each chunk's CTA writes its record, and the CTA that finishes a (sequence,
+// KV head)'s count merges all of its chunk records in chunk order, in the
+// same launch.
 // Prefill: one CTA per (tile of queries, KV head) with the G query heads of
 // the group stacked as rows; key tiles of 32 are staged in shared memory and
 // folded in with an online softmax.

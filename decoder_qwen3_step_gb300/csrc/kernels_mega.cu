@@ -127,7 +127,7 @@ __device__ __forceinline__ void red_release(unsigned int* p, unsigned int v) {
 // CTA's abort flag, when any CTA of the launch gave up or after the wait
 // limit (then also the launch's abort word and the device error word).
 __device__ __forceinline__ bool wait_count(const unsigned int* p, unsigned int target, volatile int* abort_s,
-                                        unsigned int* abort_g, uint32_t* err) {
+                                        unsigned int* abort_g, uint32_t* err, uint64_t limit = kWaitLimitNs) {
   if (ld_acquire(p) >= target) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
@@ -137,7 +137,7 @@ __device__ __forceinline__ bool wait_count(const unsigned int* p, unsigned int t
         *abort_s = 1;
         return false;
       }
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit) {
         *abort_s = 1;
         atomicOr(abort_g, 1u);
         atomicOr(err, kErrTimeout);
@@ -441,7 +441,7 @@ struct Flow {
   // compute thread returns the same answer (false: gave up).
   __device__ bool wait_all() const {
     bool ok = true;
-    if (ctid == 0) ok = wait_count(a.sync, nsync * (uint32_t)P, sm.flags, a.abort, a.err);
+    if (ctid == 0) ok = wait_count(a.sync, nsync * (uint32_t)P + a.wait_extra, sm.flags, a.abort, a.err, a.wait_limit);
     return cbar_and(ok);
   }
 

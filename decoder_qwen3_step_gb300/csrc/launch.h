@@ -188,6 +188,10 @@ struct MegaArgs {
   float* logits;              // [T, vocab] or null
   int32_t* argmax;            // [T]
   uint32_t* err;
+  // test hook: every CTA hand-off wait expects wait_extra more arrivals than
+  // will come and gives up after wait_limit ns (normally 0 and 1 s)
+  unsigned int wait_extra;
+  unsigned long long wait_limit;
   // dynamic shared memory: ring of `ring` bytes at 0, then the other regions
   int ring, o_stage, o_scr, o_small, o_bars;
   unsigned long long* trace;  // null, or [grid, kMegaTraceStride] global-timer stamps

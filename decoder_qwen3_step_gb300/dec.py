@@ -33,7 +33,7 @@ EXPORTS = (
     "dec_prefix_key", "dec_pool_set_fill", "dec_pool_register", "dec_pool_lookup", "dec_pool_cached_blocks",
     "dec_child_seed", "dec_rng_stream", "dec_rng_next_u32", "dec_rng_uniform", "dec_sampler_workspace_bytes",
     "dec_sampler_create", "dec_sampler_destroy", "dec_sampler_status", "dec_sample", "dec_debug_df_exp",
-    "dec_quantize_int4",
+    "dec_quantize_int4", "dec_batch_check", "dec_attend_noalloc_status", "dec_debug_wait_timeout",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax",
                   "step")
@@ -135,6 +135,9 @@ def lib() -> C.CDLL:
             "dec_sample": (I, [V, V, I64, C.c_int32, C.POINTER(dec_sampling), V, _I32P, _I32P, V, V, V, V]),
             "dec_debug_df_exp": (I, [V, V, I64, V]),
             "dec_quantize_int4": (I, [V, C.c_int32, C.c_int32, V, V, V]),
+            "dec_batch_check": (I, [V, C.POINTER(dec_batch), C.c_int32]),
+            "dec_attend_noalloc_status": (I, [V, C.POINTER(C.c_uint32)]),
+            "dec_debug_wait_timeout": (I, [V, C.c_uint32, C.c_uint64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

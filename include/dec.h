@@ -224,6 +224,18 @@ int dec_kv_offset(const dec_pool* p, const int32_t* table, int32_t n_table, int3
                   int32_t kv_head, int32_t is_v, int64_t* offset);
 
 /* ---- the step ------------------------------------------------------------- */
+/* The checks dec_prefill / dec_decode make before launching anything, on
+ * host data only (no GPU needed): sequence layout, consecutive positions
+ * below max_positions, ids in the vocabulary (host ids), block tables long
+ * enough and naming allocated blocks, and every block the step writes (those
+ * holding positions p_s .. the last new position of each sequence) owned by
+ * that sequence alone: refcount 1, not registered in the prefix cache, and
+ * written for no other position of the batch (tinyllm L10.1 section 4,
+ * forward_refuses_bad_batches).  decode != 0 also requires one token per
+ * sequence.  DEC_OK, or the code and dec_last_error text the step would
+ * return (DEC_EINVAL, DEC_ERANGE, DEC_EVOCAB, DEC_EBLOCK). */
+int dec_batch_check(const dec_pool* pool, const dec_batch* b, int32_t decode);
+
 /* Prefill (or any mixed step): run the batch's new tokens, write their K/V into
  * the blocks their tables name, and produce fp32 logits [R, vocab] and greedy ids
  * [R] (int32, device), R = N for DEC_ROWS_ALL or S for DEC_ROWS_LAST; rows are in
@@ -291,6 +303,14 @@ int dec_set_megakernel(dec_model* m, int32_t on);
  * when the loader issued its last tile.  NULL turns it off.  DEC_EINVAL if n
  * is too small. */
 int dec_set_step_trace(dec_model* m, uint64_t* stamps, size_t n);
+/* Test hook for the bounded waits of the one-kernel step (no counterpart on
+ * the pages): with extra > 0, every later one-kernel step's CTA hand-off
+ * waits for `extra` more arrivals than will ever come and gives up after
+ * limit_ns (1 us .. 1 s): the step then ends early with DEC_DEV_TIMEOUT in
+ * the device error word (dec_device_status) and its logits and ids are not
+ * valid; the GPU stays usable.  extra = 0 restores the normal waits (limit
+ * 1 s).  DEC_EINVAL for a limit outside the range. */
+int dec_debug_wait_timeout(dec_model* m, uint32_t extra, uint64_t limit_ns);
 /* *available = 1 when this model's shape and device can run the one-kernel
  * decode step (serving mode, two query heads per KV head, head_dim 32, 64 or
  * 128, d_model <= 1024, cooperative launch), else 0. */
@@ -333,13 +353,25 @@ int dec_attend(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float*
  * nothing.  Limits: at most 256 sequences, and the dec_attend_scratch_bytes
  * of the request must not exceed 4 MiB (e.g. 8 sequences of 2,048 keys at the
  * Qwen3-0.6B shape); larger requests return DEC_ERANGE with a message.
- * The first call on a device looks up the array's device address for that
- * device (make it before any stream capture).  Every call on a device shares
- * the one array and each call overwrites it (its counters are cleared at the
- * start of every call), so calls that may overlap on the GPU - on different
- * streams, or from different threads - race: order them on one stream. */
+ * The array's device address on a device is looked up once: by dec_create
+ * on that device, else by the first call there.  That first lookup loads the
+ * library's module holding the array (with CUDA's lazy module loading, this
+ * is when the array is allocated, and it may synchronise), so a caller that
+ * never creates a model should make one call, or dec_attend_noalloc_status,
+ * before any stream capture and before the loop that must not allocate.  The
+ * looked-up address does not survive cudaDeviceReset.  Every call on a device
+ * shares the one array and each call overwrites it (its counters and error
+ * word are cleared at the start of every call), so calls that may overlap on
+ * the GPU - on different streams, or from different threads - race: order
+ * them on one stream.  The kernel's error word (DEC_DEV_TIMEOUT if a bounded
+ * wait gave up) is read with dec_attend_noalloc_status after the call and
+ * before the next one. */
 int dec_attend_noalloc(const dec_pool* pool, int32_t layer, int32_t n_seqs, const float* q, const int32_t* ctx,
                        const int32_t* block_table, int32_t max_blocks, void* out, void* stream);
+/* Synchronise `stream`, then read and clear the device error word that the
+ * last dec_attend_noalloc call on the current device left in the library's
+ * array (0: no bounded wait gave up).  Allocates nothing. */
+int dec_attend_noalloc_status(void* stream, uint32_t* flags);
 
 /* Quantize one f32 matrix to int4 as DEC_INT4_F16KV does at load (tinyllm L10.1
  * section 2.5): W device [rows, K] f32, K a multiple of 32; codes device

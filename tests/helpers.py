@@ -3,6 +3,9 @@ the same seeded weights, and run the pages' paths (full, cached, decode)."""
 
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 from decoder_qwen3_step_gb300 import dec, inputs
@@ -27,8 +30,20 @@ def make_pair(shape_name, mode, max_positions, max_tokens=4096, max_seqs=64, n_b
     return m, orc, w
 
 
-def check(dev_logits, dev_ids, ref_logits, mode, what=""):
+def check(dev_logits, dev_ids, ref_logits, mode, what="", case=None, path=None):
+    """Compare device logits and ids with the oracle's under the mode's
+    tolerance and the near-tie argmax rule.  With DEC_PARITY_ROWS set to a
+    file path, the comparison is appended there as one JSON row per call that
+    names its case and path (octlm "Proving it's the same model": one row per
+    case and path, max and mean absolute error, argmax agreement as integer
+    counts), extended with the mode, the near-tie count and the tolerance."""
     r = compare(dev_logits, ref_logits, TOLS[mode], dev_ids)
+    out = os.environ.get("DEC_PARITY_ROWS")
+    if out and case:
+        row = {"case": case, "path": path or what, "mode": mode, **{k: (float(v) if isinstance(v, np.floating) else v)
+                                                                    for k, v in r.items()}}
+        with open(out, "a") as f:
+            f.write(json.dumps(row, default=float) + "\n")
     assert r["passed"], f"{what}: {r}"
     assert r["argmax_agree"] == r["rows"], f"{what}: {r}"
     return r

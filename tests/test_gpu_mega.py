@@ -137,3 +137,59 @@ def test_one_kernel_step_at_the_qwen3_shape():
         check(got[i], ids[i], want[i], "bf16", f"0.6B one-kernel decode step {i}")
     assert m.device_status() == 0
     m.close()
+
+
+def test_one_kernel_step_at_the_bench_batch1_case():
+    """The bench's batch-1 decode case exactly: the Qwen3-0.6B shape in the
+    serving mode, one sequence whose 2,048-token context is the bench's
+    longest (ids seed 131), decode steps on the one-kernel path, each checked
+    against the oracle on the same bf16-rounded weights."""
+    shape = inputs.SHAPES["qwen3_0p6b"]
+    V = shape["vocab"]
+    m, orc, w = make_pair("qwen3_0p6b", "bf16", max_positions=2048 + 64, max_tokens=2048, max_seqs=1, n_blocks=140)
+    if not m.megakernel_available():
+        pytest.skip("the one-kernel step is not available on this device")
+    ctx = inputs.make_ids(V, 2048, seed=100 + 31)
+    table = m.blocks_for(2048 + 8)
+    m.prefill([(ctx, 0, table)], rows=dec.DEC_ROWS_LAST)
+    cache = orc.new_cache(2048 + 8)
+    tok = int(np.argmax(orc.forward(cache, ctx, 0, rows="last")[-1]))
+    m.L.dec_profile_enable(m.handle, STEP, 1)
+    step_launches(m)
+    for i in range(4):
+        ref = orc.forward(cache, [tok], 2048 + i)
+        lg, am = m.decode([([tok], 2048 + i, table)])
+        check(np_(lg), np_(am), ref, "bf16", f"batch-1 decode step {i}", case="decode_b1 bench case",
+              path=f"one-kernel decode step {i} (context {2049 + i})")
+        tok = int(np.argmax(ref[0]))
+    assert step_launches(m) == 4
+    m.L.dec_profile_enable(m.handle, STEP, 0)
+    assert m.device_status() == 0
+    m.close()
+
+
+def test_one_kernel_step_wait_gives_up_and_the_gpu_stays_usable():
+    """A bounded wait of the one-kernel step runs out on purpose (the test
+    hook makes every hand-off expect one arrival too many, with a 2 ms
+    limit): the step ends with DEC_DEV_TIMEOUT in the device error word, no
+    fault; then the same step with the normal waits matches the oracle."""
+    m, orc, w = make_pair("tiny", "bf16", max_positions=128, max_tokens=128, max_seqs=2)
+    if not m.megakernel_available():
+        pytest.skip("the one-kernel step is not available on this device")
+    prompt = inputs.make_ids(512, 37, seed=140)
+    table = m.blocks_for(48)
+    m.prefill([(prompt, 0, table)], rows=dec.DEC_ROWS_LAST)
+    cache = orc.new_cache(48)
+    tok = int(np.argmax(orc.forward(cache, prompt, 0, rows="last")[-1]))
+    assert m.device_status() == 0
+    with pytest.raises(dec.DecError):  # the limit is bounded on both sides
+        dec.check(m.L.dec_debug_wait_timeout(m.handle, 1, 10), "dec_debug_wait_timeout")
+    dec.check(m.L.dec_debug_wait_timeout(m.handle, 1, 2_000_000), "dec_debug_wait_timeout")
+    m.decode([([tok], 37, table)])
+    assert m.device_status() & dec.DEC_DEV_TIMEOUT
+    dec.check(m.L.dec_debug_wait_timeout(m.handle, 0, 0), "dec_debug_wait_timeout")
+    ref = orc.forward(cache, [tok], 37)
+    lg, am = m.decode([([tok], 37, table)])
+    check(np_(lg), np_(am), ref, "bf16", "decode after a timed-out step")
+    assert m.device_status() == 0
+    m.close()

@@ -34,19 +34,20 @@ def test_tiny_full_cached_and_greedy_decode(tiny):
     ref_full = orc.full(ids)
     table = m.blocks_for(25)
     lg, am = m.prefill([(ids, 0, table)])
-    check(np_(lg), np_(am), ref_full, mode, "full")
+    check(np_(lg), np_(am), ref_full, mode, "full", case="C1 tiny", path="full prefill (16 tokens)")
     # cached: 8 + 8 on top of the first half's cache
     t2 = m.blocks_for(25)
     a1, i1 = m.prefill([(ids[:8], 0, t2)])
     a2, i2 = m.prefill([(ids[8:], 8, t2)])
-    check(np.concatenate([np_(a1), np_(a2)]), np.concatenate([np_(i1), np_(i2)]), orc.cached(ids), mode, "cached")
+    check(np.concatenate([np_(a1), np_(a2)]), np.concatenate([np_(i1), np_(i2)]), orc.cached(ids), mode, "cached",
+          case="C1 tiny", path="8+8 cached prefill")
     # 8 greedy decode steps on the cached sequence
     cache = orc.new_cache(64)
     orc.forward(cache, ids, 0)
     fed, rows = orc.greedy(cache, int(np.argmax(ref_full[-1])), 16, 8)
     for i, tok in enumerate(fed):
         lg, am = m.decode([([tok], 16 + i, t2)])
-        check(np_(lg), np_(am), rows[i:i + 1], mode, f"decode {i}")
+        check(np_(lg), np_(am), rows[i:i + 1], mode, f"decode {i}", case="C1 tiny", path=f"greedy decode step {i}")
     assert m.device_status() == 0
     m.release(table)
     m.release(t2)
@@ -105,7 +106,8 @@ def test_small_batched_full_cached_and_decode():
             cache = orc.new_cache(256)
             ref = orc.forward(cache, p, 0)
             caches.append(cache)
-            check(lg[128 * s:128 * (s + 1)], am[128 * s:128 * (s + 1)], ref, mode, f"{mode} full seq {s}")
+            check(lg[128 * s:128 * (s + 1)], am[128 * s:128 * (s + 1)], ref, mode, f"{mode} full seq {s}",
+                  case="C2 small", path=f"full prefill, batch 4, sequence {s}")
         # cached: 64 + 64, both halves batched over the 4 sequences
         t2 = [m.blocks_for(128 + 64) for _ in range(4)]
         a1, i1 = m.prefill([(p[:64], 0, t) for p, t in zip(prompts, t2)])
@@ -114,14 +116,16 @@ def test_small_batched_full_cached_and_decode():
         for s, p in enumerate(prompts):
             got = np.concatenate([a1[64 * s:64 * (s + 1)], a2[64 * s:64 * (s + 1)]])
             gid = np.concatenate([i1[64 * s:64 * (s + 1)], i2[64 * s:64 * (s + 1)]])
-            check(got, gid, orc.cached(p), mode, f"{mode} cached seq {s}")
+            check(got, gid, orc.cached(p), mode, f"{mode} cached seq {s}", case="C2 small",
+                  path=f"64+64 cached prefill, sequence {s}")
         # 64 greedy decode steps at batch 4, teacher-forced on the oracle's ids
         steps = 64
         toks = [int(np.argmax(orc.forward(orc.new_cache(256), p, 0)[-1])) for p in prompts]
         for i in range(steps):
             refs = [orc.forward(caches[s], [toks[s]], 128 + i)[0] for s in range(4)]
             lg, am = m.decode([([toks[s]], 128 + i, t2[s]) for s in range(4)])
-            check(np_(lg), np_(am), np.stack(refs), mode, f"{mode} decode step {i}")
+            check(np_(lg), np_(am), np.stack(refs), mode, f"{mode} decode step {i}",
+                  case="C2 small" if i in (0, steps - 1) else None, path=f"batch-4 decode step {i}")
             toks = [int(np.argmax(r)) for r in refs]
         assert m.device_status() == 0
         m.close()

@@ -200,3 +200,57 @@ def test_random_lifecycles_keep_the_pool_invariants(L, seed):  # noqa: F811
         assert counts(L, p) == (len(free), len(lru))
         assert sorted(free + lru + [b for b in range(N) if ref[b] > 0]) == list(range(N))
     L.dec_pool_destroy(p)
+
+
+def batch(seqs, vocab_ok=True):  # noqa: F811
+    """A dec_batch (and the host arrays it points at) from [(ids, first position, table)]."""
+    ids, pos, start, tab = [], [], [0], []
+    mb = max(len(t) for _, _, t in seqs)
+    for toks, p0, table in seqs:
+        ids += list(toks)
+        pos += list(range(p0, p0 + len(toks)))
+        start.append(len(ids))
+        tab += list(table) + [0] * (mb - len(table))
+    arr = lambda v: (C.c_int32 * len(v))(*v)  # noqa: E731
+    keep = (arr(ids), arr(pos), arr(start), arr(tab))
+    b = dec.dec_batch(len(seqs), len(ids), keep[0], None, keep[1], keep[2], keep[3], mb)
+    return b, keep
+
+
+def check(L, p, seqs, decode=0):  # noqa: F811
+    b, _keep = batch(seqs)
+    return L.dec_batch_check(p, C.byref(b), decode)
+
+
+def test_step_check_refuses_writes_into_shared_or_cached_blocks(L):  # noqa: F811
+    """A step writes K/V only into blocks its sequence owns alone: a block
+    shared after retain or lookup, or indexed in the prefix cache, is refused
+    (DEC_EBLOCK) before anything runs, so a scheduler's mistake cannot
+    overwrite another sequence's cache or a cached prefix."""
+    _c, p, _ = _pool(L, 16)
+    rc, blk = alloc(L, p, 3)
+    assert rc == 0
+    toks = list(range(1, 17))
+    # a clean prefill of 20 tokens into blocks 0 and 1 of the table passes
+    assert check(L, p, [(list(range(20)), 0, blk[:2])]) == 0
+    # sharing the block the step writes (refcount 2) is refused ...
+    assert L.dec_pool_retain(p, blk[1]) == 0
+    assert check(L, p, [([7], 20, blk[:2])]) == dec.DEC_EBLOCK
+    assert "shared" in L.dec_last_error().decode()
+    # ... while reading a shared block is fine: the step writes only block 2
+    assert check(L, p, [([7], 32, [blk[0], blk[1], blk[2]])]) == 0
+    assert L.dec_pool_release(p, blk[1]) == 0
+    # a full block registered in the prefix index may be read, never written
+    assert L.dec_pool_set_fill(p, blk[0], B) == 0
+    assert register(L, p, blk[0], key_of(L, 0, toks)) == (0, 1)
+    assert check(L, p, [(toks, 0, blk[:1])]) == dec.DEC_EBLOCK
+    assert check(L, p, [([3], 16, blk[:2])]) == 0
+    # two sequences (or two positions) that would write the same block are refused
+    assert check(L, p, [([3], 17, blk[:2]), ([4], 20, [blk[2], blk[1]])]) == dec.DEC_EBLOCK
+    assert "two positions" in L.dec_last_error().decode()
+    assert check(L, p, [(list(range(20)), 16, [blk[0], blk[1], blk[1]])]) == dec.DEC_EBLOCK
+    # the remaining checks still hold: unallocated block, short table, decode shape
+    assert check(L, p, [([3], 16, [blk[0], 15])]) == dec.DEC_EBLOCK
+    assert check(L, p, [([3], 40, blk[:2])]) == dec.DEC_ERANGE
+    assert check(L, p, [([3, 4], 16, blk[:2])], decode=1) == dec.DEC_EINVAL
+    L.dec_pool_destroy(p)

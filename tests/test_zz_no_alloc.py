@@ -7,7 +7,10 @@ the library, so the only buffers a caller passes are inputs and outputs.
 Checked through the C ABI against dec_attend (the same kernel with caller
 scratch) on two calls in a row, within the tolerance of test_gpu_attend;
 the second call also shows that what the first left in the shared array does
-not leak into the result.  This file is named to be collected last."""
+not leak into the result.  A repeated call leaves the device's free memory
+and torch's allocation count unchanged (it allocates nothing), and the
+array's error word reads 0 after good calls.  This file is named to be
+collected last."""
 
 import ctypes as C
 
@@ -22,6 +25,13 @@ from .helpers import make_pair  # noqa: E402
 from .test_gpu_attend import fill_cache, run_attend  # noqa: E402
 
 pytestmark = pytest.mark.gpu
+
+
+def noalloc_status(m):
+    v = C.c_uint32(0xFFFFFFFF)
+    s = torch.cuda.current_stream()
+    dec.check(m.L.dec_attend_noalloc_status(C.c_void_p(s.cuda_stream), C.byref(v)), "dec_attend_noalloc_status")
+    return v.value
 
 
 def run_noalloc(m, layer, q, ctxs, tables, out):
@@ -60,6 +70,14 @@ def test_noalloc_attention_matches_dec_attend_twice(mode):
         w, g = want.float().cpu().numpy(), got.float().cpu().numpy()
         assert np.isfinite(g).all()
         assert np.abs(g - w).max() <= tol * max(1.0, np.abs(w).max())
+        assert noalloc_status(m) == 0
+        # the same call again: no device memory taken, by the driver's count or torch's
+        torch.cuda.synchronize()
+        free0, allocated0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        run_noalloc(m, lay, q, ctxs, tables, got)
+        free1, allocated1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        assert (free1, allocated1) == (free0, allocated0)
+        assert np.array_equal(got.float().cpu().numpy(), g)
         for t in tables:
             m.release(t)
     # beyond the fixed scratch (256 sequences x 1,024 keys: 8.7 MB): refused with a message,
