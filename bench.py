@@ -38,6 +38,13 @@ WORKLOAD = ("qwen3-0.6B-shape decoder (596,049,920 params), bf16 weights / f16 p
             "greedy decode at batch 32, contexts 1024..2048 (distinct) preloaded by prefill")
 KV_BYTES_PER_CTX_TOKEN_LAYER = 8 * 128 * 2 * 2  # K and V, 8 KV heads x 128, f16
 WEIGHT_BYTES_BF16 = 1_192_099_840  # 596,049,920 params x 2 bytes (tied head read once per step)
+WEIGHT_BYTES_F32 = 2_384_199_680   # the same in fp32
+KV_BYTES_PER_CTX_TOKEN_F32 = 28 * 8 * 128 * 2 * 4  # K and V of every layer, fp32 (229,376 B)
+NOMINAL_HBM_GBS = 8000.0           # the ~8 TB/s HBM3e figure the fractions are also given against
+# fp32 FFMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz
+FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+PROF_STEPS = 4   # untimed steps whose dominant-class launches are timed with CUDA events
+REPEATS = 5      # timed loops of K steps; the median loop is reported
 
 
 def peaks():
@@ -152,8 +159,9 @@ def our_arm(args, rank, world):
     lens = inputs.serving_context_lengths(S)
     e2e_steps = max(8, args.steps // 4)
     b1_steps = max(32, args.steps)
-    # positions every sequence may reach: warmup, 2 + 2 profiled steps, timed, e2e, batch-1 (last sequence only)
-    extra = args.warmup + 4 + args.steps + e2e_steps + 3 + b1_steps + 2 + 16
+    # positions every sequence may reach: warmup, 2 class-share steps, PROF_STEPS dominant-class steps,
+    # 2 unprofiled steps (graph capture), REPEATS timed loops, e2e, batch-1 (last sequence only)
+    extra = args.warmup + 2 + PROF_STEPS + 2 + REPEATS * args.steps + e2e_steps + 3 + b1_steps + 2 + 16
     max_positions = max(((max(lens) + extra + 15) // 16) * 16, 4096 + 64)
     weights = inputs.make_weights(shape)
     blocks_needed = sum((L + extra) // 16 + 1 for L in lens) + 4 * (4096 // 16 + 2) + 200
@@ -200,53 +208,70 @@ def our_arm(args, rank, world):
     dom = dec.KERNEL_CLASSES.index(dom_name)
     launches(m)
 
-    # ---- timed region: K decode steps at batch 32 ----
-    # The dominant class keeps CUDA events around its launches inside the replayed
-    # step graph; two untimed steps first run it eagerly and capture it.
-    ctx_sum = 0
+    # the dominant class's time per launch: CUDA events around its launches in
+    # PROF_STEPS untimed steps (their events are record nodes in a graph of their own)
+    step_no = args.warmup + 2
+    prof_ctx = 0
     profile_classes(m, [dom], True)
-    for i in range(2):
-        decode_step(i, pos, range(S), ids_buf[(args.warmup + 2 + i) & 1], ids_buf[(args.warmup + 3 + i) & 1])
+    for i in range(PROF_STEPS):
+        prof_ctx += sum(p + 1 for p in pos)
+        decode_step(i, pos, range(S), ids_buf[(step_no + i) & 1], ids_buf[(step_no + i + 1) & 1])
         pos = [p + 1 for p in pos]
-    read_profile(m, dom)  # discard the untimed steps' records
-    launches(m)  # and their launch count
+    torch.cuda.synchronize()
+    step_no += PROF_STEPS
+    # (a new set of profiled classes runs eagerly once, is captured the next step, then replays)
+    dom_ms, dom_n = read_profile(m, dom)
+    profile_classes(m, [dom], False)
+    # two unprofiled steps: the headline graph is captured (first eager, second captured)
+    for i in range(2):
+        decode_step(i, pos, range(S), ids_buf[(step_no + i) & 1], ids_buf[(step_no + i + 1) & 1])
+        pos = [p + 1 for p in pos]
+    step_no += 2
+    launches(m)
+
+    # ---- timed region: REPEATS loops of K decode steps at batch 32, no profiling nodes ----
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    base = args.warmup + 4
+    loop_ms = []
     with Clocks(dev.index) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            ctx_sum += sum(p + 1 for p in pos)
-            decode_step(i, pos, range(S), ids_buf[(base + i) & 1], ids_buf[(base + i + 1) & 1])
-            pos = [p + 1 for p in pos]
-        t_end.record(stream)
-        torch.cuda.synchronize()
+        for r in range(REPEATS):
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t_start.record(stream)
+            for i in range(args.steps):
+                decode_step(i, pos, range(S), ids_buf[(step_no + i) & 1], ids_buf[(step_no + i + 1) & 1])
+                pos = [p + 1 for p in pos]
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            step_no += args.steps
+            t = t_start.elapsed_time(t_end)
+            if world > 1:
+                t = max_over_ranks(t, dev)
+            loop_ms.append(t)
     if world > 1:
         dist.barrier()
-    ms = t_start.elapsed_time(t_end)
+    ms = statistics.median(loop_ms)
     n_launch = launches(m)
-    dom_ms, dom_n = read_profile(m, dom)
-    profile_classes(m, [dom], False)
-    if world > 1:
-        ms = max_over_ranks(ms, dev)
     value = whole_job_rate(S * args.steps, ms, world)
-
+    ctx_sum = prof_ctx
     # roofline of the dominant kernel class: algorithmic bytes per launch / event time per launch
     L = shape["n_layers"]
     per_launch_s = (dom_ms / max(dom_n, 1)) / 1e3
+    launches_per_step = max(dom_n, 1) / PROF_STEPS
     if dom_name == "step":
         # the whole step in one kernel: every weight byte once, every cached K/V byte once,
         # the new K/V rows and the logits written
-        alg_bytes = (WEIGHT_BYTES_BF16 + ctx_sum * KV_BYTES_PER_CTX_TOKEN_LAYER * L / args.steps
+        alg_bytes = (WEIGHT_BYTES_BF16 + ctx_sum * KV_BYTES_PER_CTX_TOKEN_LAYER * L / PROF_STEPS
                      + S * KV_BYTES_PER_CTX_TOKEN_LAYER * L + S * shape["vocab"] * 4)
         unit_note = ("per step: 1,192,099,840 B of bf16 weights + 4,096 B of K+V per context token per layer "
                      "(28 layers) + the new K/V rows + fp32 logits [32, 151936]")
     elif dom_name == "attn":
-        alg_bytes = ctx_sum * KV_BYTES_PER_CTX_TOKEN_LAYER / args.steps  # per launch (one layer)
+        alg_bytes = ctx_sum * KV_BYTES_PER_CTX_TOKEN_LAYER / PROF_STEPS * L / launches_per_step  # per launch (one layer)
         unit_note = "4,096 B of K+V per context token per layer; units = sum of the 32 context lengths"
     else:
         alg_bytes = _class_weight_bytes(dom_name, shape) + 0.0
@@ -258,11 +283,14 @@ def our_arm(args, rank, world):
     traffic_ratio = {"attn": 277.6 / 268.7, "step": 1.441 / 1.427}.get(dom_name)
     traffic = int(alg_bytes * traffic_ratio) if traffic_ratio else None
     roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "peak_nominal": NOMINAL_HBM_GBS,
+                "traffic": traffic,
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of a smaller case, "
                                   "scaled by algorithmic bytes" if traffic else None,
                 "peak_source": pk["source"], "bytes_per_launch": int(alg_bytes), "per_unit": unit_note,
                 "launch_us": round(per_launch_s * 1e6, 2), "launches": dom_n,
+                "timing": f"CUDA events around the class's {dom_n} launches in {PROF_STEPS} untimed steps",
                 "step_share": {k: round(v / max(sum(shares.values()), 1e-9), 4) for k, v in shares.items()}}
 
     # ---- e2e: host ids in, host ids out, every step ----
@@ -317,6 +345,7 @@ def our_arm(args, rank, world):
     b1_bytes = WEIGHT_BYTES_BF16 + (b1_ctx / b1_steps) * KV_BYTES_PER_CTX_TOKEN_LAYER * L
     decode_b1 = {"tokens_per_s": round(1e3 / b1_ms, 1), "ms_per_token": round(b1_ms, 4),
                  "hbm_frac": round(b1_bytes / (b1_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                 "hbm_frac_nominal": round(b1_bytes / (b1_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
                  "bytes_per_token": int(b1_bytes), "context": p1,
                  "kernel_us_per_step": {k: round(v[0] * 1e3 / 2, 1) for k, v in b1_cls.items() if v[1]},
                  "kernel_share": {k: round(v[0] / b1_tot, 4) for k, v in b1_cls.items() if v[1]}}
@@ -359,6 +388,7 @@ def our_arm(args, rank, world):
 
     status = m.device_status()
     m.close()
+    fp32 = fp32_parity_runs(dev, pk)
     return {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -366,10 +396,11 @@ def our_arm(args, rank, world):
         "config": {"workload": WORKLOAD, "batch": S, "context_lengths": [min(lens), max(lens)],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1.19 GB weights + >5.6 GB KV read per step); no flush",
-                   "launch": "each step replays a captured CUDA graph; the events around the dominant kernel "
-                             "class are event-record nodes inside it"},
+                   "launch": "each step replays a captured CUDA graph (no profiling nodes in the timed loops)",
+                   "timing": f"median of {REPEATS} timed loops of {args.steps} steps each",
+                   "loop_ms": [round(t, 3) for t in loop_ms]},
         "roofline": roofline, "e2e": e2e, "gpu_launches": n_launch, "clocks": clk.summary(),
-        "decode_b1": decode_b1, "prefill_4x4096": prefill, "device_status": status,
+        "decode_b1": decode_b1, "prefill_4x4096": prefill, "fp32_parity_mode": fp32, "device_status": status,
     }
 
 
@@ -377,6 +408,70 @@ def _class_weight_bytes(name, shape):
     d, H, Hkv, D, F, V = (shape[k] for k in ("d_model", "n_heads", "n_kv_heads", "head_dim", "ff_hidden", "vocab"))
     return 2 * {"qkv": (H + 2 * Hkv) * D * d, "oproj": d * H * D, "gateup": 2 * F * d, "down": d * F,
                 "lmhead": V * d}.get(name, 0)
+
+
+def fp32_parity_runs(dev, pk):
+    """The parity mode at the Qwen3-0.6B shape (fp32 weights, KV and
+    arithmetic): the 188-token prompt prefilled with logits at every position
+    (P-C3: 228.2 GFLOP, FFMA), then 256 greedy decode tokens at batch 1,
+    context 189 -> 444 (D-b1-fp32: 2,384,199,680 B of weights + 229,376 B of
+    K/V per context token)."""
+    import torch
+
+    from decoder_qwen3_step_gb300 import dec, inputs
+    from decoder_qwen3_step_gb300.runtime import Decoder
+
+    shape = inputs.SHAPES["qwen3_0p6b"]
+    V = shape["vocab"]
+    m = Decoder(shape, inputs.make_weights(shape), mode=dec.DEC_FP32, max_positions=512, max_tokens=512, max_seqs=1,
+                n_blocks=40)
+    ids = inputs.make_ids(V, 188)
+    table = m.blocks_for(188 + 257)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    logits = torch.empty((188, V), dtype=torch.float32, device=dev)
+    am = torch.empty((188,), dtype=torch.int32, device=dev)
+    warm = m.blocks_for(188)
+    for _ in range(2):
+        m.prefill([(ids, 0, warm)], out=(logits, am))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    m.prefill([(ids, 0, table)], out=(logits, am))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pf_ms = e0.elapsed_time(e1)
+    d, H, Hkv, D, F, L = (shape[k] for k in ("d_model", "n_heads", "n_kv_heads", "head_dim", "ff_hidden", "n_layers"))
+    proj = 2 * ((H + 2 * Hkv) * D * d + d * H * D + 2 * F * d + d * F) * L
+    attn = 4 * H * D * L * sum(p + 1 for p in range(188))
+    flops = 188 * proj + 188 * 2 * V * d + attn
+    tok = torch.empty((1,), dtype=torch.int32, device=dev)
+    nxt = torch.empty((1,), dtype=torch.int32, device=dev)
+    tok.copy_(am[187:188])
+    lg1 = torch.empty((1, V), dtype=torch.float32, device=dev)
+    steps, ctx_sum = 256, 0
+    for i in range(3):  # warm-up and graph capture; the timed loop rewrites these positions
+        m.decode([([0], 188 + i, table)], device_ids=tok, out=(lg1, nxt))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        ctx_sum += 188 + i + 1
+        m.decode([([0], 188 + i, table)], device_ids=tok if i % 2 == 0 else nxt, out=(lg1, nxt if i % 2 == 0 else tok))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    d_ms = e0.elapsed_time(e1) / steps
+    bytes_tok = WEIGHT_BYTES_F32 + ctx_sum / steps * KV_BYTES_PER_CTX_TOKEN_F32
+    status = m.device_status()
+    m.close()
+    return {"prefill_188": {"ms": round(pf_ms, 3), "tokens_per_s": round(188 / (pf_ms / 1e3), 1),
+                            "gflop": round(flops / 1e9, 1), "tflops": round(flops / (pf_ms / 1e3) / 1e12, 2),
+                            "ffma_frac": round(flops / (pf_ms / 1e3) / 1e12 / FP32_FFMA_TFLOPS, 4),
+                            "ffma_peak_tflops": round(FP32_FFMA_TFLOPS, 1),
+                            "ffma_peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz"},
+            "decode_b1": {"tokens_per_s": round(1e3 / d_ms, 1), "ms_per_token": round(d_ms, 4),
+                          "context": [189, 188 + steps], "bytes_per_token": int(bytes_tok),
+                          "hbm_frac": round(bytes_tok / (d_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                          "hbm_frac_nominal": round(bytes_tok / (d_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4)},
+            "device_status": status}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -430,20 +525,84 @@ def _oracle_step(orc, cfg, caches, pick, step):
         orc.forward(c, [step % cfg.vocab], L + step)
 
 
-def oracle_decode_sample(budget_s=12.0, n_sample=4):
-    """Oracle decode steps on a sample of the headline workload's sequences,
-    until the time budget is spent; returns tokens/s and a description."""
-    orc, cfg, caches, pick = _oracle_sample(n_sample, 256)
-    step, t0 = 0, time.perf_counter()
-    while step < 256:
-        _oracle_step(orc, cfg, caches, pick, step)
-        step += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return n_sample * step / dt, {"kind": "oracle", "cores": blas_threads(),
-                                  "sample": f"{step} float64 decode step(s) of {n_sample} of the 32 sequences "
-                                            f"(contexts {pick}), caches filled with seeded random K/V; {dt:.1f} s"}
+def _filled_cache(orc, cfg, n_ctx, room):
+    """A cache holding n_ctx positions of constant K/V (the cost of the next
+    tokens does not depend on the cached values)."""
+    c = orc.new_cache(n_ctx + room)
+    for l in range(cfg.n_layers):
+        c.k[l][:n_ctx] = 0.01
+        c.v[l][:n_ctx] = 0.01
+        c.written[l][:n_ctx] = True
+    return c
+
+
+def cpu_baselines(budget_s=2.5):
+    """The oracle on the host cores: the headline decode rate (one float64
+    token for each of the shortest and longest of the 32 serving sequences)
+    and, per configuration, prefill and decode tokens/s on bounded samples
+    (each timed piece stops after about budget_s): the tiny and small
+    decoders, the Qwen3-0.6B shape in the parity mode (fp32 weights) and in
+    the serving mode (bf16-rounded weights)."""
+    from decoder_qwen3_step_gb300 import inputs
+    from oracle.model import DecoderConfig, Oracle
+
+    def timed(fn, units_per_call, limit):
+        n, t0 = 0, time.perf_counter()
+        while n < limit:
+            fn(n)
+            n += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return n * units_per_call / dt, n, dt
+
+    def run(orc, vocab, n_prompt, start, pre, dctx, caches):
+        ids = inputs.make_ids(vocab, n_prompt, seed=3)
+
+        def prefill(i):
+            c = pre if pre is not None else orc.new_cache(n_prompt + 1)
+            orc.forward(c, ids, start, rows="all" if start == 0 else "last")
+
+        pf, n_pf, t_pf = timed(prefill, n_prompt, 3)
+
+        def decode(i):
+            for c, L in zip(caches, dctx):
+                orc.forward(c, [i % vocab], L + i)
+
+        dc, n_dc, t_dc = timed(decode, len(dctx), 64)
+        sample = (f"prefill: {n_pf} x {n_prompt} tokens" + (f" after {start} cached" if start else "")
+                  + f" ({t_pf:.1f} s); decode: {n_dc} step(s) at batch {len(dctx)}, contexts {dctx} ({t_dc:.1f} s)")
+        return {"prefill_tokens_per_s": round(pf, 2), "decode_tokens_per_s": round(dc, 2), "sample": sample}
+
+    out = {}
+    for name, shp, n_prompt, dctx in (("C1 tiny fp32", "tiny", 16, [16]), ("C2 small fp32", "small", 128, [128] * 4)):
+        shape = inputs.SHAPES[shp]
+        orc = Oracle(DecoderConfig(**shape, max_positions=256), inputs.make_weights(shape), mode="fp32")
+        out[name] = run(orc, shape["vocab"], n_prompt, 0, None, dctx,
+                        [_filled_cache(orc, orc.cfg, L, 64) for L in dctx])
+    shape = inputs.SHAPES["qwen3_0p6b"]
+    V = shape["vocab"]
+    w = inputs.make_weights(shape)
+    orc = Oracle(DecoderConfig(**shape, max_positions=512), w, mode="fp32")
+    out["C3 qwen3-0.6B fp32"] = run(orc, V, 188, 0, None, [188], [_filled_cache(orc, orc.cfg, 188, 64)])
+    del orc
+    orc = Oracle(DecoderConfig(**shape, max_positions=4096 + 128), w, mode="bf16")
+    del w
+    lens = inputs.serving_context_lengths(32)
+    pick = [lens[0], lens[-1]]
+    caches = [_filled_cache(orc, orc.cfg, L, 64) for L in pick]
+    c4 = run(orc, V, 64, 0, None, pick, caches)
+    c4["sample"] += "; the serving contexts' shortest and longest"
+    out["C4 qwen3-0.6B serving"] = c4
+    del caches
+    pre = _filled_cache(orc, orc.cfg, 3968, 160)
+    out["C5 qwen3-0.6B chunked prefill"] = run(orc, V, 64, 3968, pre, [4032], [pre])
+    for v in out.values():
+        v["sample"] += "; caches of constant K/V where a context precedes"
+    head = {"kind": "oracle", "cores": blas_threads(), "value": c4["decode_tokens_per_s"], "unit": "tokens/s",
+            "sample": "float64 decode tokens of 2 of the 32 serving sequences, " + c4["sample"].split("decode: ")[1],
+            "configs": out}
+    return head
 
 
 # One float64 decode token of the 0.6B shape costs about 0.09 s on a 16-core host.
@@ -502,10 +661,7 @@ def main():
     else:
         line = our_arm(args, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
-            v, info = oracle_decode_sample()
-            info["value"] = round(v, 3)
-            info["unit"] = "tokens/s"
-            line["cpu_baseline"] = info
+            line["cpu_baseline"] = cpu_baselines()
     if rank == 0 and line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:
