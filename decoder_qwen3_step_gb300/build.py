@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdec.so")
-SOURCES = ["api.cu", "attend.cu", "prefix.cu", "kernels_core.cu", "kernels_attn.cu", "kernels_attn_tc.cu", "kernels_tc.cu",
+SOURCES = ["api.cu", "attend.cu", "prefix.cu", "kernels_core.cu", "kernels_attn.cu", "kernels_attn_tc.cu", "kernels_attn_dec_tc.cu", "kernels_tc.cu",
            "kernels_tc_skinny.cu", "kernels_mega.cu", "kernels_int4.cu", "sampler.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -823,6 +823,18 @@ struct StepPlan {
   int32_t* argmax;
 };
 
+// The KV pool's tensor map (TMA boxes of 16 slots), made once per pool.
+static int ensure_kvmap(dec_model* m, const StepPlan& sp) {
+  const dec_config& c = m->cfg;
+  if (m->kvmap_slabs != sp.slabs || m->kvmap_blocks != sp.dm.n_blocks) {
+    const uint64_t rows = (uint64_t)c.n_layers * sp.dm.n_blocks * 2 * c.n_kv_heads * c.block_tokens;
+    if (!kv_map(&m->kvmap, sp.slabs, rows, c.head_dim)) return fail(DEC_ECUDA, "tensor map of the KV pool failed");
+    m->kvmap_slabs = sp.slabs;
+    m->kvmap_blocks = sp.dm.n_blocks;
+  }
+  return DEC_OK;
+}
+
 // Queue the kernels of one step on `st` (eager, or into a capture).
 static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   const dec_config& c = m->cfg;
@@ -857,6 +869,13 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     return launch_gemv(g, epi, bf, st);
   };
 
+  // serving-mode decode steps: attention on the tensor cores with the QK-norm,
+  // RoPE and cache append fused in
+  const bool dec_tc_attn = sp.decode && bf && !i4 && m->tc_on && m->tc_ready && attn_decode_tc_eligible(sp.dm);
+  if (dec_tc_attn) {
+    int rc = ensure_kvmap(m, sp);
+    if (rc) return rc;
+  }
   EmbedArgs ea{P + pl.embed, sp.meta.ids, N, d, c.vocab, R, (const float*)(layer(0) + pl.attn_norm), X, XN, SSQ, KEYS,
                ERR};
   DEC_LAUNCH(DEC_K_EMBED, launch_embed(ea, bf, st));
@@ -871,11 +890,15 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     // RMSNorm + [Wq;Wk;Wv]
     g.W = Lb + pl.wqkv; g.rows = qkv_rows(c); g.K = d; g.X = XN; g.x_row = nullptr; g.T = N; g.ssq = SSQ;
     g.out_f32 = RAW;
-    // the skinny product fuses QK-norm/RoPE/cache write up to 16 token rows;
-    // from 17 to 32 its raw output and k_qkv_post measure faster
-    const bool tc_qkv = bf && m->tc_on && m->tc_ready &&
+    // decode steps of the serving mode: raw q|k|v, then the tensor-core
+    // attention that also norms, rotates and appends (no launch in between);
+    // otherwise the skinny product fuses QK-norm/RoPE/cache write up to 16
+    // token rows, and from 17 to 32 its raw output and k_qkv_post measure faster
+    const bool tc_qkv = bf && m->tc_on && m->tc_ready && !dec_tc_attn &&
                         ((N > kGemvMaxTokens && tc_eligible(g)) || (N <= kQkvFuseMaxSkinny && tc_skinny_eligible(g)));
-    if (tc_qkv) {
+    if (dec_tc_attn) {
+      DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV_RAW, &m->tm_qkv[l], &m->tm_xn, &m->tm_xn32));
+    } else if (tc_qkv) {
       // tensor-core product with QK-norm, RoPE and the cache write in its epilogue
       g.qf = QkvFuse{(const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope), Q,
                      sp.slabs, l, sp.meta, c.n_heads, c.n_kv_heads, c.head_dim, dm.B, dm.n_blocks, dm.max_blocks};
@@ -889,7 +912,11 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     // attention
     AttnArgs aa{Q, sp.slabs, l, sp.meta, dm, ATT, PART, m->NCH, sp.S, 1.0f / std::sqrt((float)c.head_dim),
                 (int*)(ws + wl.ACNT), ERR};
-    if (sp.decode) {
+    if (dec_tc_attn) {
+      AttnDecTcArgs ta{aa, RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm),
+                       (const float*)(P + pl.rope)};
+      DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode_tc(ta, &m->kvmap, sp.slots, st));
+    } else if (sp.decode) {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, sp.slots, bf, st));
     } else if (bf && m->tc_on && attn_prefill_tc_eligible(aa)) {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_prefill_tc(aa, sp.n_work, st));
@@ -998,12 +1025,8 @@ static int enqueue_mega(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   a.o_small = ms.o_small;
   a.o_bars = ms.o_bars;
   a.trace = m->trace && m->trace_n >= (size_t)m->num_sms * kMegaTraceStride ? m->trace : nullptr;
-  if (m->kvmap_slabs != sp.slabs || m->kvmap_blocks != sp.dm.n_blocks) {
-    const uint64_t rows = (uint64_t)c.n_layers * sp.dm.n_blocks * 2 * c.n_kv_heads * c.block_tokens;
-    if (!kv_map(&m->kvmap, sp.slabs, rows, c.head_dim)) return fail(DEC_ECUDA, "tensor map of the KV pool failed");
-    m->kvmap_slabs = sp.slabs;
-    m->kvmap_blocks = sp.dm.n_blocks;
-  }
+  int rc = ensure_kvmap(m, sp);
+  if (rc) return rc;
   a.tm_kv = m->kvmap;
   a.wait_extra = m->wait_extra;
   a.wait_limit = m->wait_limit;

@@ -51,6 +51,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "attn_fold.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -109,11 +110,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
   const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(y));
   return lo | (hi << 16);
 }
-__device__ __forceinline__ uint32_t pack_half(float x, float y) {
-  const uint32_t lo = __half_as_ushort(__float2half_rn(x));
-  const uint32_t hi = __half_as_ushort(__float2half_rn(y));
-  return lo | (hi << 16);
-}
 __device__ __forceinline__ uint32_t ld_acquire(const unsigned int* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -153,24 +149,12 @@ __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
 __device__ __forceinline__ void ldsm2(uint32_t addr, uint32_t (&r)[2]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
 }
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -245,25 +229,6 @@ __host__ __device__ constexpr int scr_bytes() {
   const int merge = (kCT * 4 + 2 * D) * 4;            // per-thread states, merged values
   return attn > prod ? (attn > merge ? attn : merge) : (prod > merge ? prod : merge);
 }
-
-// Where the K (or V) rows of one 16-slot block of one KV head land in an
-// attention tile: TMA boxes of 16 rows x min(D, 64) f16; with D >= 64 each
-// box row is 128 bytes and its 16-byte chunks are XOR-swizzled by the row
-// (the 128-byte swizzle), so the 8 rows an ldmatrix reads at one column hit
-// 8 different bank groups.
-template <int D>
-struct KvSlab {
-  static constexpr int kBoxDims = D >= 64 ? 64 : D;
-  static constexpr int kBoxes = D / kBoxDims;
-  static constexpr int kRowBytes = kBoxDims * 2;
-  static constexpr int kBoxBytes = 16 * kRowBytes;
-  static constexpr bool kSwizzle = kBoxDims == 64;
-  // byte offset of (row r, the 8 dims from d, d a multiple of 8) in the slab
-  static __device__ __forceinline__ int chunk(int r, int d) {
-    const int bx = d / kBoxDims, c = (d % kBoxDims) >> 3;
-    return bx * kBoxBytes + r * kRowBytes + ((kSwizzle ? (c ^ (r & 7)) : c) << 4);
-  }
-};
 
 // Shared memory of one CTA.
 struct Smem {
@@ -728,94 +693,13 @@ struct Flow {
   }
 
   // Warp gw folds block gw (16 keys) of a tile for both query heads of its
-  // group: S = Q K^T (queries as MMA rows 0 and 1, rows 2..15 zero), the
-  // softmax of each head's row in fp32 (keys past the context masked),
-  // O = P V with P rounded to f16; (max, sum) and O per head to the scratch.
+  // group on the f16 tensor cores (fold16): (max, sum) and O per head to the
+  // group scratch.
   __device__ void fold(GroupScr<D>* gs, const __half* Ks, const __half* Vs, int keys_here) {
     const int gw = warp & 3;
-    const int nkeys = min(16, keys_here - gw * 16);
-    constexpr int kNT = D / 16;  // value n-tiles of 8 dims per half of the head
-    float mh = -INFINITY, lh = 0.f;
-    uint32_t P4[4] = {0u, 0u, 0u, 0u};
-    if (nkeys > 0) {
-      const __half* Kb = Ks + gw * 16 * D;
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const int qr = lane & 15;
-      const uint32_t qa = (qr < 2 ? smem_u32(&gs->q[qr][0]) : smem_u32(sm.zrow)) + (lane >> 4) * 16;
-      const int key = (lane & 7) + ((lane >> 4) << 3), doff = ((lane >> 3) & 1) * 8;
-      const uint32_t kb = smem_u32(Kb);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; kk += 2) {
-        uint32_t A[4], B[4], A2[4], B2[4];
-        ldsm4(qa + kk * 32, A);
-        ldsm4(kb + KvSlab<D>::chunk(key, kk * 16 + doff), B);
-        ldsm4(qa + kk * 32 + 32, A2);
-        ldsm4(kb + KvSlab<D>::chunk(key, kk * 16 + 16 + doff), B2);
-        mma_f16(s[0], A, B[0], B[1]);
-        mma_f16(s[1], A, B[2], B[3]);
-        mma_f16(s2[0], A2, B2[0], B2[1]);
-        mma_f16(s2[1], A2, B2[2], B2[3]);
-      }
-      // row lane>>2 (a query head for lanes 0..7): keys nt*8 + 2*(lane&3) + e
-      float sc[2][2];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int kx = nt * 8 + 2 * (lane & 3) + e;
-          sc[nt][e] = kx < nkeys ? (s[nt][e] + s2[nt][e]) * a.scale : -INFINITY;
-          mx = fmaxf(mx, sc[nt][e]);
-        }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      float p[2][2], ps = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          p[nt][e] = sc[nt][e] == -INFINITY ? 0.f : expf(sc[nt][e] - mx);
-          ps += p[nt][e];
-        }
-      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-      mh = mx;
-      lh = ps;
-      // P as the A operand: rows 8..15 are not query heads and stay zero
-      P4[0] = pack_half(p[0][0], p[0][1]);
-      P4[2] = pack_half(p[1][0], p[1][1]);
-    }
-    // O = P V in two halves of the head dimension (fewer live accumulators)
-    const __half* Vb = Vs + gw * 16 * D;
-    const int vkey = (lane & 7) + ((lane >> 3) & 1) * 8, vd = (lane >> 4) * 8;
-    const uint32_t vb = smem_u32(Vb);
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      float oacc[kNT][4];
-#pragma unroll
-      for (int j = 0; j < kNT; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
-      if (nkeys > 0) {
-#pragma unroll
-        for (int j = 0; j < kNT / 2; ++j) {
-          uint32_t B[4];
-          ldsm4t(vb + KvSlab<D>::chunk(vkey, (hf * kNT / 2 + j) * 16 + vd), B);
-          mma_f16(oacc[2 * j], P4, B[0], B[1]);
-          mma_f16(oacc[2 * j + 1], P4, B[2], B[3]);
-        }
-      }
-      if (lane < 8) {
-        const int h = lane >> 2;
-#pragma unroll
-        for (int j = 0; j < kNT; ++j)
-          *reinterpret_cast<float2*>(&gs->o[gw][h][hf * (D / 2) + 8 * j + 2 * (lane & 3)]) =
-              make_float2(oacc[j][0], oacc[j][1]);
-      }
-    }
-    if (lane < 8 && (lane & 3) == 0) {
-      gs->m[gw][lane >> 2] = mh;
-      gs->l[gw][lane >> 2] = lh;
-    }
+    fold16<D>(gs->q[0], gs->q[1], sm.zrow, reinterpret_cast<const uint8_t*>(Ks + gw * 16 * D),
+              reinterpret_cast<const uint8_t*>(Vs + gw * 16 * D), min(16, keys_here - gw * 16), a.scale,
+              &gs->o[gw][0][0], gs->m[gw], gs->l[gw]);
   }
 
   // The chunk's record: the four warps' states merged in warp order, per
@@ -959,23 +843,16 @@ struct Flow {
         head_row(s, (is_v ? a.H + a.Hkv + g : a.H + g) * D, is_v ? nullptr : k_norm, pos, v);
         const int blk = __ldg(a.tables + (size_t)s * a.max_blocks + pos / 16);
         __half* dst = a.kv + kv_offset(l, blk, is_v, g, pos % 16, a.n_blocks, a.Hkv, 16, D);
-        const int kk = pos - c * kKeys, r = kk % 16;
-        uint8_t* slab_s = reinterpret_cast<uint8_t*>((is_v ? Vs : Ks) + (kk / 16) * kSlabElems);
-        // this lane's kDim dims sit inside one 16-byte chunk of the slab row
-        __half* stl = reinterpret_cast<__half*>(slab_s + KvSlab<D>::chunk(r, (lane * kDim) & ~7)) + ((lane * kDim) & 7);
+        const int kk = pos - c * kKeys;
+        __half hv[kDim];
 #pragma unroll
         for (int e = 0; e < kDim; ++e) {
-          const __half hv = __float2half_rn(v[e]);
-          dst[lane * kDim + e] = hv;
-          stl[e] = hv;
+          hv[e] = __float2half_rn(v[e]);
+          dst[lane * kDim + e] = hv[e];
         }
-        if (is_v) {  // value rows past the context (the block's tail) become zeros: P V must not meet NaN bits
-          constexpr int kRB = KvSlab<D>::kRowBytes / 4;  // 32-bit words of a box row
-          for (int i = lane; i < (15 - r) * KvSlab<D>::kBoxes * kRB; i += 32) {
-            const int rr = r + 1 + i / (KvSlab<D>::kBoxes * kRB), rem = i % (KvSlab<D>::kBoxes * kRB);
-            reinterpret_cast<uint32_t*>(slab_s + (rem / kRB) * KvSlab<D>::kBoxBytes + rr * KvSlab<D>::kRowBytes)[rem % kRB] = 0u;
-          }
-        }
+        // patch the tile; value rows past the context (the block's tail)
+        // become zeros: P V must not meet NaN bits
+        patch_row<D>(reinterpret_cast<uint8_t*>((is_v ? Vs : Ks) + (kk / 16) * kSlabElems), kk % 16, hv, is_v);
         // the slot is refilled by bulk copies later: order these stores before them
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }

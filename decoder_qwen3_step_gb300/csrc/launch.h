@@ -127,6 +127,21 @@ int skinny_splits(int rows, int K);
 cudaError_t launch_gemm_tc_skinny(const GemvArgs& a, int epi, const void* tmW, const void* tmX, uint32_t* err,
                                   bool pdl, cudaStream_t s);
 
+// Serving-mode decode attention (f16 KV cache, two query heads per KV head)
+// on the warp-level tensor cores, with QK-norm, RoPE and the cache append of
+// the step's token fused in: it reads the QKV product's raw rows instead of
+// Q.  tm_kv points at a host copy of the pool's CUtensorMap ([rows, D] f16,
+// box 16 x min(D, 64), 128-byte swizzle when D >= 64).
+struct AttnDecTcArgs {
+  AttnArgs at;            // Q is not read
+  const float* raw;       // [T, (H+2Hkv)*D] q|k|v before QK-norm and RoPE
+  const float* q_norm;    // [D] QK-norm gains of the layer
+  const float* k_norm;
+  const float* rope;      // [max_positions, D/2, 2] (cos, sin)
+};
+bool attn_decode_tc_eligible(const Dims& dm);
+cudaError_t launch_attn_decode_tc(const AttnDecTcArgs& a, const void* tm_kv, int nchunk, cudaStream_t s);
+
 // Query rows of one prefill attention tile (query-head rows / group size).
 int prefill_tile_queries(int G);
 
