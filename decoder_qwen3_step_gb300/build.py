@@ -18,6 +18,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdec.so")
+# DEC_DEBUG build: device bounds checks that set an error bit (never trap)
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libdec_debug.so")
 SOURCES = ["api.cu", "attend.cu", "prefix.cu", "kernels_core.cu", "kernels_attn.cu", "kernels_attn_tc.cu", "kernels_attn_dec_tc.cu", "kernels_tc.cu",
            "kernels_tc_skinny.cu", "kernels_mega.cu", "kernels_int4.cu", "sampler.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,8 +37,8 @@ def cuda_home() -> str:
     return os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
 
 
-def _flags():
-    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3", "--expt-relaxed-constexpr",
+def _flags(debug: bool = False):
+    return ARCH + (["-DDEC_DEBUG"] if debug else []) + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3", "--expt-relaxed-constexpr",
                    "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 
 
@@ -46,17 +49,20 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    """Compile every translation unit (those older than their sources) and
+    link; debug=True builds libdec_debug.so with DEC_DEBUG defined."""
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "dec.h"))
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            jobs.append([nvcc(), *_flags(), "-c", s, "-o", o])
+            jobs.append([nvcc(), *_flags(debug), "-c", s, "-o", o])
 
     def run(cmd):
         if verbose:
@@ -69,12 +75,12 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
+    if force or jobs or _stale(lib, objs):
         libdir = os.path.join(cuda_home(), "lib64")
-        run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", LIB, *objs,
+        run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", lib, *objs,
              "-Xlinker", f"-rpath,{libdir}", "-L", libdir])
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

@@ -200,6 +200,7 @@ struct GraphEntry {
   const void* logits;
   const void* argmax;
   const void* slabs;
+  int n_blocks;        // the pool's size (its tensor map is a kernel argument in the graph)
   uint32_t prof_mask;  // kernel classes profiled when the step was captured
   cudaGraph_t graph;   // kept while it has profiling nodes: their handles address the executable graph's nodes
   cudaGraphExec_t exec;
@@ -245,6 +246,7 @@ struct dec_model {
   bool mega_shape;  // the shape and device allow it
   uint32_t wait_extra;         // test hook of the one-kernel step's hand-off waits
   uint64_t wait_limit;
+  int32_t poison[3];           // debug builds: (sequence, column, value) for the next step's device table; seq -1: none
   const void* kvmap_slabs;  // the pool the one-kernel step's KV tensor map was made for
   int kvmap_blocks;
   CUtensorMap kvmap;
@@ -536,6 +538,7 @@ int dec_create(const dec_config* cfg, const dec_weights* w, void* packed_buf, si
   m->kvmap_slabs = nullptr;
   m->wait_extra = 0;
   m->wait_limit = 1000000000ull;
+  m->poison[0] = -1;
   m->kvmap_blocks = 0;
   m->trace = nullptr;
   m->trace_n = 0;
@@ -666,6 +669,30 @@ int dec_debug_wait_timeout(dec_model* m, uint32_t extra, uint64_t limit_ns) {
   m->wait_extra = extra;
   m->wait_limit = extra ? limit_ns : 1000000000ull;
   return DEC_OK;
+}
+
+uint32_t dec_build_flags(void) {
+#ifdef DEC_DEBUG
+  return DEC_BUILD_DEBUG;
+#else
+  return 0;
+#endif
+}
+
+int dec_debug_poison_table(dec_model* m, int32_t seq, int32_t col, int32_t value) {
+  if (!m) return fail(DEC_EINVAL, "NULL model");
+#ifdef DEC_DEBUG
+  if (seq < 0 || col < 0) return fail(DEC_EINVAL, "sequence and column must be >= 0");
+  m->poison[0] = seq;
+  m->poison[1] = col;
+  m->poison[2] = value;
+  return DEC_OK;
+#else
+  (void)seq;
+  (void)col;
+  (void)value;
+  return fail(DEC_EINVAL, "dec_debug_poison_table needs a DEC_DEBUG build");
+#endif
 }
 
 int dec_megakernel_available(const dec_model* m, int32_t* available) {
@@ -823,6 +850,14 @@ struct StepPlan {
   int32_t* argmax;
 };
 
+// Serving-mode decode steps run attention on the tensor cores with the
+// QK-norm, RoPE and cache append fused in (a persistent kernel whose launch
+// does not depend on the contexts).
+static bool decode_tc_attn(const dec_model* m, const StepPlan& sp) {
+  return sp.decode && serving(m->cfg) && !int4_proj(m->cfg) && m->tc_on && m->tc_ready &&
+         attn_decode_tc_eligible(sp.dm);
+}
+
 // The KV pool's tensor map (TMA boxes of 16 slots), made once per pool.
 static int ensure_kvmap(dec_model* m, const StepPlan& sp) {
   const dec_config& c = m->cfg;
@@ -871,7 +906,7 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
 
   // serving-mode decode steps: attention on the tensor cores with the QK-norm,
   // RoPE and cache append fused in
-  const bool dec_tc_attn = sp.decode && bf && !i4 && m->tc_on && m->tc_ready && attn_decode_tc_eligible(sp.dm);
+  const bool dec_tc_attn = decode_tc_attn(m, sp);
   if (dec_tc_attn) {
     int rc = ensure_kvmap(m, sp);
     if (rc) return rc;
@@ -901,12 +936,12 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     } else if (tc_qkv) {
       // tensor-core product with QK-norm, RoPE and the cache write in its epilogue
       g.qf = QkvFuse{(const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm), (const float*)(P + pl.rope), Q,
-                     sp.slabs, l, sp.meta, c.n_heads, c.n_kv_heads, c.head_dim, dm.B, dm.n_blocks, dm.max_blocks};
+                     sp.slabs, l, sp.meta, c.n_heads, c.n_kv_heads, c.head_dim, dm.B, dm.n_blocks, dm.max_blocks, ERR};
       DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV, &m->tm_qkv[l], &m->tm_xn, &m->tm_xn32));
     } else {
       DEC_LAUNCH(DEC_K_QKV, product(g, EPI_QKV_RAW, bf ? &m->tm_qkv[l] : nullptr, &m->tm_xn, &m->tm_xn32));
       QkvPostArgs qa{RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm),
-                     (const float*)(P + pl.rope), Q, sp.slabs, l, sp.meta, dm};
+                     (const float*)(P + pl.rope), Q, sp.slabs, l, sp.meta, dm, ERR};
       DEC_LAUNCH(DEC_K_QKV_POST, launch_qkv_post(qa, N, bf, st));
     }
     // attention
@@ -915,7 +950,7 @@ static int enqueue_step(dec_model* m, const StepPlan& sp, cudaStream_t st) {
     if (dec_tc_attn) {
       AttnDecTcArgs ta{aa, RAW, (const float*)(Lb + pl.q_norm), (const float*)(Lb + pl.k_norm),
                        (const float*)(P + pl.rope)};
-      DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode_tc(ta, &m->kvmap, sp.slots, st));
+      DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode_ring(ta, &m->kvmap, sp.meta.work, m->num_sms, st));
     } else if (sp.decode) {
       DEC_LAUNCH(DEC_K_ATTN, launch_attn_decode(aa, sp.slots, bf, st));
     } else if (bf && m->tc_on && attn_prefill_tc_eligible(aa)) {
@@ -1101,14 +1136,14 @@ static void drop_graph(GraphEntry& g) {
 
 // Decode steps of one shape replay a captured CUDA graph: the per-step
 // metadata lives at fixed device addresses (one host->device copy before the
-// replay), so (S, attention grid, logits, argmax, pool, profiled classes) key
-// a graph.  A key's first step runs eagerly; its second captures.
+// replay), so (S, attention grid, logits, argmax, pool and its size, profiled
+// classes) key a graph.  A key's first step runs eagerly; its second captures.
 static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st) {
   const uint32_t mask = prof_mask(m);
   GraphEntry* hit = nullptr;
   for (auto& e : m->graphs)
     if (e.S == sp.S && e.slots == sp.slots && e.logits == sp.logits && e.argmax == sp.argmax &&
-        e.slabs == sp.slabs && e.prof_mask == mask)
+        e.slabs == sp.slabs && e.n_blocks == sp.dm.n_blocks && e.prof_mask == mask)
       hit = &e;
   ++m->graph_clock;
   if (hit && hit->exec) {
@@ -1129,6 +1164,7 @@ static int launch_decode_graph(dec_model* m, const StepPlan& sp, cudaStream_t st
     e.logits = sp.logits;
     e.argmax = sp.argmax;
     e.slabs = sp.slabs;
+    e.n_blocks = sp.dm.n_blocks;
     e.prof_mask = mask;
     e.last_use = m->graph_clock;
     m->graphs.push_back(e);
@@ -1271,6 +1307,12 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
     for (int i = 0; i < MB; ++i) H[o_tab + (size_t)s * MB + i] = i < nb ? b->block_table[(size_t)s * b->max_blocks + i] : 0;
   }
   H[o_start + S] = N;
+#ifdef DEC_DEBUG
+  if (m->poison[0] >= 0) {  // test hook: a bad entry in the device copy only (the host used the real table)
+    if (m->poison[0] < S && m->poison[1] < MB) H[o_tab + (size_t)m->poison[0] * MB + m->poison[1]] = m->poison[2];
+    m->poison[0] = -1;
+  }
+#endif
   if (rows_mode == DEC_ROWS_ALL)
     for (int t = 0; t < N; ++t) H[o_row + t] = t;
   else
@@ -1289,27 +1331,16 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
     for (int k = 0; k < 3; ++k) H[o_work + 3 * i + k] = work[i][k];
   o += 3 * work.size();
   const bool mega = decode && m->mega_on && m->mega_shape && N <= kMegaAutoTokens && !m->dump;
-  if (mega) {
-    // one-kernel step: the first attention item of every sequence (KV heads x 64-key chunks each)
+  static_assert(kMegaKeys == kDecodeChunk, "one attention item layout for both decode paths");
+  if (decode) {
+    // decode attention items, sequence-major: the first of every sequence (KV heads x 64-key chunks each)
     int first = 0;
     for (int s = 0; s < S; ++s) {
       H[o_work + s] = first;
-      first += c.n_kv_heads * ((b->positions[b->seq_start[s + 1] - 1] + kMegaKeys) / kMegaKeys);
+      first += c.n_kv_heads * ((b->positions[b->seq_start[s + 1] - 1] + kDecodeChunk) / kDecodeChunk);
     }
     H[o_work + S] = first;
     o += S + 1;
-  } else if (decode) {
-    // decode attention work list: n, then (sequence, 64-key chunk) pairs, chunk-major
-    int n = 0, cmax = (max_ctx + kDecodeChunk - 1) / kDecodeChunk;
-    for (int cc = 0; cc < cmax; ++cc)
-      for (int s = 0; s < S; ++s)
-        if (cc * kDecodeChunk < b->positions[b->seq_start[s + 1] - 1] + 1) {
-          H[o_work + 1 + 2 * n] = s;
-          H[o_work + 2 + 2 * n] = cc;
-          ++n;
-        }
-    H[o_work] = n;
-    o += 1 + 2 * (size_t)n;
   }
   if (o > m->wl.meta_ints) return fail(DEC_ERANGE, "step metadata exceeds the workspace");
 
@@ -1343,6 +1374,7 @@ static int run_step(dec_model* m, dec_pool* pool, const dec_batch* b, int rows_m
   // decode attention grid: one CTA per 64-key chunk of the longest sequence, rounded
   // up to a multiple of 4 chunks so a captured graph serves 256 positions of growth
   sp.slots = std::min(m->NCH, ((max_ctx + kDecodeChunk - 1) / kDecodeChunk + 3) / 4 * 4);
+  if (decode_tc_attn(m, sp)) sp.slots = 0;  // unused there: one captured graph serves every context
   sp.slabs = pool->slabs;
   sp.logits = logits;
   sp.argmax = argmax;

@@ -27,6 +27,7 @@ constexpr int kDecodeChunk = 64;  // keys per split-K work item of decode attent
 constexpr uint32_t kErrBadId = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 constexpr uint32_t kErrCapacity = 4u;  // a kernel's fixed-size list overflowed (the host sizes grids to avoid it)
+constexpr uint32_t kErrBounds = 8u;    // DEC_DEBUG builds: a block-table column or pool block id out of range
 constexpr int kMaxPositions = 40960;    // the longest context a model may be built for (Qwen3's limit)
 
 using bf16 = __nv_bfloat16;
@@ -172,6 +173,31 @@ __host__ __device__ __forceinline__ int64_t kv_offset(int layer, int block, int 
                                                       int n_blocks, int Hkv, int B, int D) {
   int64_t slab = ((int64_t)layer * n_blocks + block) * 2 + is_v;
   return slab * (int64_t)Hkv * B * D + ((int64_t)kv_head * B + slot) * D;
+}
+
+// Pool block id in column `col` of sequence s's block-table row (row stride
+// max_blocks).  The host validates every table before a step; a DEC_DEBUG
+// build checks again on the device: a column or id out of range sets
+// kErrBounds in *err and yields block 0, so the access stays inside the pool
+// (the step's results are then invalid, and the error word says so).
+__device__ __forceinline__ int table_block(const int32_t* tables, int s, int col, int max_blocks, int n_blocks,
+                                           uint32_t* err) {
+#ifdef DEC_DEBUG
+  if ((unsigned)col >= (unsigned)max_blocks) {
+    atomicOr(err, kErrBounds);
+    return 0;
+  }
+  const int blk = __ldg(tables + (size_t)s * max_blocks + col);
+  if ((unsigned)blk >= (unsigned)n_blocks) {
+    atomicOr(err, kErrBounds);
+    return 0;
+  }
+  return blk;
+#else
+  (void)n_blocks;
+  (void)err;
+  return __ldg(tables + (size_t)s * max_blocks + col);
+#endif
 }
 
 }  // namespace dec

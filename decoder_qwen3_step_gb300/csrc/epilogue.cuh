@@ -159,7 +159,7 @@ __device__ __forceinline__ float qk_rope(const QkvFuse& f, int gh, int j, float 
 
 // Cache block holding position `pos` of the sequence of token row tt.
 __device__ __forceinline__ int qkv_block(const QkvFuse& f, int tt, int pos) {
-  return f.meta.tables[(size_t)f.meta.tok_seq[tt] * f.max_blocks + pos / f.B];
+  return table_block(f.meta.tables, f.meta.tok_seq[tt], pos / f.B, f.max_blocks, f.n_blocks, f.err);
 }
 
 // Write output row j of head gh for absolute token row tt at position pos

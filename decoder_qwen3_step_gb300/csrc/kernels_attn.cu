@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) k_attn_decode(AttnArgs a) {
     __syncwarp();
     if (lane < nblk) {
       const KT* kv = reinterpret_cast<const KT*>(a.kv);
-      const int blk = a.meta.tables[(size_t)s * dm.max_blocks + c * kDecBlocks + lane];
+      const int blk = table_block(a.meta.tables, s, c * kDecBlocks + lane, dm.max_blocks, dm.n_blocks, a.err);
       bulk_g2s(Ks + lane * 16 * D, kv + kv_offset(a.layer, blk, 0, g, 0, dm.n_blocks, dm.Hkv, 16, D), kSlab, &bar);
       bulk_g2s(Vs + lane * 16 * D, kv + kv_offset(a.layer, blk, 1, g, 0, dm.n_blocks, dm.Hkv, 16, D), kSlab, &bar);
     }
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(128) k_attn_prefill(AttnArgs a) {
       const int j = j0 + kk;
       float kvv[8], vvv[8];
       if (j <= p_last) {
-        const int blk = a.meta.tables[(size_t)s * dm.max_blocks + j / dm.B];
+        const int blk = table_block(a.meta.tables, s, j / dm.B, dm.max_blocks, dm.n_blocks, a.err);
         const int slot = j % dm.B;
         load8(kv + kv_offset(a.layer, blk, 0, g, slot, dm.n_blocks, dm.Hkv, dm.B, D) + c8, kvv);
         load8(kv + kv_offset(a.layer, blk, 1, g, slot, dm.n_blocks, dm.Hkv, dm.B, D) + c8, vvv);

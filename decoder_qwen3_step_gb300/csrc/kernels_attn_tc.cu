@@ -81,7 +81,6 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) k_attn_prefill_tc(AttnArgs a
   const int p0 = a.meta.tok_pos[tok0];
   const int p_last = p0 + ntok - 1;
   const __half* kv = reinterpret_cast<const __half*>(a.kv);
-  const int* table = a.meta.tables + (size_t)s * dm.max_blocks;
 
   // key tile kt of K and V into stage st (16-byte pieces, rows past p_last zero)
   auto load_tile = [&](int kt, int st) {
@@ -92,7 +91,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2) k_attn_prefill_tc(AttnArgs a
       const int kk = i / kPieces, c8 = (i % kPieces) * 8;
       const int j = kt * kTcKeys + kk;
       const bool in = j <= p_last;
-      const int blk = in ? __ldg(table + j / dm.B) : 0;
+      const int blk = in ? table_block(a.meta.tables, s, j / dm.B, dm.max_blocks, dm.n_blocks, a.err) : 0;
       const int slot = in ? j % dm.B : 0;
       const __half* ksrc = kv + kv_offset(a.layer, blk, 0, g, slot, dm.n_blocks, dm.Hkv, dm.B, D) + c8;
       const __half* vsrc = kv + kv_offset(a.layer, blk, 1, g, slot, dm.n_blocks, dm.Hkv, dm.B, D) + c8;

@@ -237,7 +237,7 @@ __global__ void k_qkv_post(QkvPostArgs a) {
   const float* raw = a.raw + (size_t)t * width + (size_t)warp * D;
   const int pos = a.meta.tok_pos[t];
   const int seq = a.meta.tok_seq[t];
-  const int blk = a.meta.tables[(size_t)seq * dm.max_blocks + pos / dm.B];
+  const int blk = table_block(a.meta.tables, seq, pos / dm.B, dm.max_blocks, dm.n_blocks, a.err);
   const int slot = pos % dm.B;
   KT* kv = reinterpret_cast<KT*>(a.kv);
   float* mine = buf + warp * D;

@@ -238,7 +238,7 @@ struct Smem {
   float* rstd;                 // [8]
   unsigned long long* best;    // [8]
   float* sq;                   // [8][16]
-  int* flags;                  // [0] abort, [1] tiles issued
+  int* flags;                  // [0] abort, [1] tiles issued (at the loader's end), [2] tiles claimed
   __half* zrow;                // [D] zeros (MMA rows 2..15 of the queries)
   uint64_t* full;              // [kNB]
   uint64_t* empty;             // [kNB]
@@ -249,6 +249,28 @@ struct Smem {
 };
 constexpr int kSmallBytes = 32 + 64 + 512 + 64 + 256;  // rstd, best, sq, flags, zrow
 constexpr int kBarBytes = kNB * (8 + 8 + 4 + 4) + (kGroups + 1) * ((int)sizeof(Item) + 4);
+
+// A compute warp's wait for ring tile n.  A parity test only tells the
+// barrier's current phase from the one before: while tile n - kNB (the
+// previous use of the same barrier) is still landing, the test for tile n
+// passes on the phase before that.  So after the wait, the loader's claim
+// count must show tile n as claimed (its claim waited for the release of
+// tile n - kNB); if not, wait for the claim and then for the tile again.
+__device__ __forceinline__ bool tile_wait(const Smem& sm, uint32_t n, uint32_t* err) {
+  if (!mbar_wait(&sm.full[n % kNB], (n / kNB) & 1, sm.flags, err)) return false;
+  volatile int* claimed = sm.flags + 2;
+  if ((uint32_t)*claimed > n) return true;
+  const uint64_t t0 = global_ns();
+  while ((uint32_t)*claimed <= n) {
+    if (*(volatile int*)sm.flags) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *(volatile int*)sm.flags = 1;
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+  return mbar_wait(&sm.full[n % kNB], (n / kNB) & 1, sm.flags, err);
+}
 
 // ---------------------------------------------------------------------------
 // The loader warp: the CTA's tiles in the order the compute warps take them.
@@ -282,6 +304,7 @@ __device__ void loader(const MegaArgs& a, const Smem& sm, int b, int P) {
         off = (int)(v % R);
         sm.toff[n % kNB] = (uint32_t)off;
         mbar_expect_tx(&sm.full[n % kNB], tx);
+        *(volatile int*)(sm.flags + 2) = (int)(n + 1);  // tiles claimed (tile_wait)
       }
     }
     return __shfl_sync(0xffffffffu, off, 0);
@@ -348,7 +371,7 @@ __device__ void loader(const MegaArgs& a, const Smem& sm, int b, int P) {
         constexpr int kB = KvSlab<D>::kBoxes;
         if (lane < 2 * nb * kB) {
           const int bx = lane % kB, j = (lane / kB) % nb, is_v = lane / (kB * nb);
-          const int blk = __ldg(a.tables + (size_t)it.s * a.max_blocks + it.c * (kKeys / 16) + j);
+          const int blk = table_block(a.tables, it.s, it.c * (kKeys / 16) + j, a.max_blocks, a.n_blocks, a.err);
           const int row = (((l * a.n_blocks + blk) * 2 + is_v) * a.Hkv + it.g) * 16;
           tma_load_2d(sm.ring + off + (is_v * (kKeys / 16) + j) * slab + bx * KvSlab<D>::kBoxBytes, &a.tm_kv,
                       bx * KvSlab<D>::kBoxDims, row, &sm.full[n % kNB]);
@@ -533,7 +556,7 @@ struct Flow {
       for (int ks = 0; ks < nks; ++ks) {
         const int kslice = min(kKS, K - ks * kKS), rs = kslice * 2 + 16, nsteps = kslice / 16;
         const uint32_t n = tile + ks * mt + m + q;
-        if (!mbar_wait(&sm.full[n % kNB], (n / kNB) & 1, sm.flags, a.err)) {
+        if (!tile_wait(sm, n, a.err)) {
           got = false;
           break;
         }
@@ -830,7 +853,7 @@ struct Flow {
         for (int e = 0; e < kDim; ++e) gs->q[gw][lane * kDim + e] = __float2half_rn(v[e]);
       }
       if (k == 0) substamp(0);
-      bool wok = mbar_wait(&sm.full[n % kNB], (n / kNB) & 1, sm.flags, a.err);
+      bool wok = tile_wait(sm, n, a.err);
       if (k == 0) substamp(1);
       const int keys_here = min(kKeys, ctx - c * kKeys);
       __half* Ks = reinterpret_cast<__half*>(sm.ring + sm.toff[n % kNB]);
@@ -841,7 +864,7 @@ struct Flow {
         const int is_v = gw == 3;
         float v[kDim];
         head_row(s, (is_v ? a.H + a.Hkv + g : a.H + g) * D, is_v ? nullptr : k_norm, pos, v);
-        const int blk = __ldg(a.tables + (size_t)s * a.max_blocks + pos / 16);
+        const int blk = table_block(a.tables, s, pos / 16, a.max_blocks, a.n_blocks, a.err);
         __half* dst = a.kv + kv_offset(l, blk, is_v, g, pos % 16, a.n_blocks, a.Hkv, 16, D);
         const int kk = pos - c * kKeys;
         __half hv[kDim];

@@ -23,6 +23,7 @@ struct QkvFuse {
   int layer;
   StepMeta meta;
   int H, Hkv, D, B, n_blocks, max_blocks;
+  uint32_t* err;  // device error word
 };
 
 // Token rows up to which the weight-streaming kernel runs a product.
@@ -78,6 +79,7 @@ struct QkvPostArgs {
   int layer;
   StepMeta meta;
   Dims dims;
+  uint32_t* err;  // device error word
 };
 
 struct AttnArgs {
@@ -140,7 +142,11 @@ struct AttnDecTcArgs {
   const float* rope;      // [max_positions, D/2, 2] (cos, sin)
 };
 bool attn_decode_tc_eligible(const Dims& dm);
-cudaError_t launch_attn_decode_tc(const AttnDecTcArgs& a, const void* tm_kv, int nchunk, cudaStream_t s);
+// One persistent CTA per SM (grid CTAs) streaming its share of the
+// (sequence, KV head, 64-key chunk) items through a TMA ring; item_start
+// [S+1] (device) is the first item of every sequence (Hkv * chunks each).
+cudaError_t launch_attn_decode_ring(const AttnDecTcArgs& a, const void* tm_kv, const int32_t* item_start, int grid,
+                                    cudaStream_t s);
 
 // Query rows of one prefill attention tile (query-head rows / group size).
 int prefill_tile_queries(int G);

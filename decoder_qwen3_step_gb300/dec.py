@@ -10,12 +10,14 @@ import ctypes as C
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libdec.so")
+# DEC_DEBUG=1 in the environment loads the DEC_DEBUG build (device bounds checks) instead
+LIB_PATH = os.path.join(_HERE, "libdec_debug.so" if os.environ.get("DEC_DEBUG") == "1" else "libdec.so")
 
 DEC_OK, DEC_EINVAL, DEC_ECAPACITY, DEC_EBLOCK, DEC_ERANGE, DEC_EVOCAB, DEC_ECUDA, DEC_EDEVICE = range(8)
 DEC_FP32, DEC_BF16_F16KV, DEC_INT4_F16KV = 0, 1, 2
 DEC_ROWS_ALL, DEC_ROWS_LAST = 0, 1
-DEC_DEV_BAD_ID, DEC_DEV_TIMEOUT, DEC_DEV_CAPACITY = 1, 2, 4
+DEC_DEV_BAD_ID, DEC_DEV_TIMEOUT, DEC_DEV_CAPACITY, DEC_DEV_BOUNDS = 1, 2, 4, 8
+DEC_BUILD_DEBUG = 1
 DEC_PURPOSE_SAMPLE = 4
 DEC_SAMPLE_BAD_ID, DEC_SAMPLE_BAD_LOGIT, DEC_SAMPLE_NO_FINITE, DEC_SAMPLE_OVERFLOW = 1, 2, 4, 8
 
@@ -34,6 +36,7 @@ EXPORTS = (
     "dec_child_seed", "dec_rng_stream", "dec_rng_next_u32", "dec_rng_uniform", "dec_sampler_workspace_bytes",
     "dec_sampler_create", "dec_sampler_destroy", "dec_sampler_status", "dec_sample", "dec_debug_df_exp",
     "dec_quantize_int4", "dec_batch_check", "dec_attend_noalloc_status", "dec_debug_wait_timeout",
+    "dec_build_flags", "dec_debug_poison_table",
 )
 KERNEL_CLASSES = ("embed", "qkv", "qkv_post", "attn", "attn_merge", "oproj", "gateup", "down", "lmhead", "argmax",
                   "step")
@@ -81,7 +84,8 @@ def lib() -> C.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libdec.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run __graft_entry__.build()"
+                               " (the DEC_DEBUG build: python -m decoder_qwen3_step_gb300.build --debug)")
         L = C.CDLL(LIB_PATH)
         V, I, SZ, I64 = C.c_void_p, C.c_int, C.c_size_t, C.c_int64
         cfgp = C.POINTER(dec_config)
@@ -138,6 +142,8 @@ def lib() -> C.CDLL:
             "dec_batch_check": (I, [V, C.POINTER(dec_batch), C.c_int32]),
             "dec_attend_noalloc_status": (I, [V, C.POINTER(C.c_uint32)]),
             "dec_debug_wait_timeout": (I, [V, C.c_uint32, C.c_uint64]),
+            "dec_build_flags": (C.c_uint32, []),
+            "dec_debug_poison_table": (I, [V, C.c_int32, C.c_int32, C.c_int32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)

@@ -137,6 +137,8 @@ const char* dec_last_error(void);
 #define DEC_DEV_BAD_ID   1u /* a device-side token id was outside the vocabulary */
 #define DEC_DEV_TIMEOUT  2u /* a bounded wait in a kernel gave up */
 #define DEC_DEV_CAPACITY 4u /* a kernel's fixed-size work list overflowed */
+#define DEC_DEV_BOUNDS   8u /* DEC_DEBUG builds only: a kernel met a block-table column or pool
+                               block id outside its range; it used block 0 instead */
 
 /* ---- model ---------------------------------------------------------------- */
 /* Check a config; DEC_OK if the decoder can run it. */
@@ -486,6 +488,25 @@ int dec_debug_df_exp(const double* x, double* y, int64_t n, void* stream);
 
 /* Library version string. */
 const char* dec_version(void);
+
+/* ---- debug build ------------------------------------------------------------
+ * Building with DEC_DEBUG defined (python -m decoder_qwen3_step_gb300.build
+ * --debug writes libdec_debug.so beside libdec.so) adds device-side bounds
+ * checks to every kernel that reads a block table: a column past the row or a
+ * pool block id outside the pool sets DEC_DEV_BOUNDS in the model's device
+ * error word (dec_device_status) and the access goes to block 0 instead, so
+ * nothing outside the pool is read or written.  No check traps.  The release
+ * build compiles the checks out; the host validates every step's batch
+ * (dec_batch_check) in both builds. */
+#define DEC_BUILD_DEBUG 1u
+/* Bit mask of the build's options (DEC_BUILD_DEBUG). */
+uint32_t dec_build_flags(void);
+
+/* Debug builds only (DEC_EINVAL otherwise): the next step's device copy of
+ * the block table gets `value` in column `col` of sequence `seq`'s row, after
+ * the host has validated and used the real table; one step only.  Lets a test
+ * reach the device bounds checks with an id the host would refuse. */
+int dec_debug_poison_table(dec_model* m, int32_t seq, int32_t col, int32_t value);
 
 #ifdef __cplusplus
 }

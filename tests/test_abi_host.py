@@ -148,3 +148,16 @@ def test_kv_offset_follows_the_worked_block_address_example(L):
     bad = (C.c_int32 * 3)(7, 2, 12)
     assert L.dec_kv_offset(p, bad, 3, 37, 0, 0, 0, C.byref(off)) == dec.DEC_EBLOCK
     L.dec_pool_destroy(p)
+
+
+def test_release_build_has_no_debug_hooks(L):
+    """The release library reports no build options and refuses the debug
+    build's table-poisoning hook; the DEC_DEBUG build adds -DDEC_DEBUG to every
+    translation unit and links libdec_debug.so beside libdec.so."""
+    from decoder_qwen3_step_gb300 import build
+
+    if os.environ.get("DEC_DEBUG") != "1":
+        assert L.dec_build_flags() == 0
+    assert L.dec_debug_poison_table(None, 0, 0, 0) == dec.DEC_EINVAL
+    assert "-DDEC_DEBUG" in build._flags(debug=True) and "-DDEC_DEBUG" not in build._flags()
+    assert build.LIB_DEBUG != build.LIB and build.BUILD_DEBUG != build.BUILD
