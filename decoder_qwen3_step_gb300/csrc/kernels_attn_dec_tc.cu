@@ -356,10 +356,21 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn_decode_ring(const __gr
         const int per_head = nch * (D + 2);
         const bool staged = 2 * per_head + 2 * kChunkCap + 2 <= kPart / 4 && !*abort_flag;
         if (staged) {
-          for (int x = ltid; x < per_head; x += 128) {  // float2 pieces, per_head / 2 a head
-            const int h = x / (per_head / 2), r = x % (per_head / 2);
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(base + (size_t)h * a.at.nchunk_cap * (D + 2)) + r);
-            *reinterpret_cast<float2*>(stg + h * per_head + 2 * r) = v;
+          // float2 pieces (per_head / 2 a head), kU loads in flight per thread before their stores
+          constexpr int kU = 16;
+          for (int x0 = ltid; x0 < per_head; x0 += 128 * kU) {
+            float2 v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const int x = x0 + u * 128, h = x / (per_head / 2), r = x % (per_head / 2);
+              if (x < per_head)
+                v[u] = __ldcg(reinterpret_cast<const float2*>(base + (size_t)h * a.at.nchunk_cap * (D + 2)) + r);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const int x = x0 + u * 128, h = x / (per_head / 2), r = x % (per_head / 2);
+              if (x < per_head) *reinterpret_cast<float2*>(stg + h * per_head + 2 * r) = v[u];
+            }
           }
           asm volatile("bar.sync %0, 128;" ::"r"(1 + gq) : "memory");
         }

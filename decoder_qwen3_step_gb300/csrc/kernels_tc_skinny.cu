@@ -185,12 +185,29 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     if (has_rows && ks > 1) {
-      for (int i = et; i < rows_per * kSkN; i += 128) {
-        const int t = i / rows_per, rr = i - t * rows_per;
-        const float* p = tile + t * kSkLd + r_lo + rr;
-        float sum = 0.f;
-        for (int q = 0; q < ks; ++q) sum += dsmem_ld(dsmem_addr(p, (uint32_t)q));
-        red[t * kSkRedLd + rr] = sum;
+      // two outputs a pass: all their remote loads in flight together, then
+      // the sums in rank order
+      constexpr int kMaxKs = 16, kU = 2;
+      const int n = rows_per * kSkN;
+      for (int i0 = et; i0 < n; i0 += 128 * kU) {
+        float v[kU][kMaxKs];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + u * 128, t = i / rows_per, rr = i - t * rows_per;
+          const float* p = tile + t * kSkLd + r_lo + rr;
+#pragma unroll
+          for (int q = 0; q < kMaxKs; ++q)
+            if (q < ks) v[u][q] = i < n ? dsmem_ld(dsmem_addr(p, (uint32_t)q)) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + u * 128, t = i / rows_per, rr = i - t * rows_per;
+          float sum = 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxKs; ++q)
+            if (q < ks) sum += v[u][q];
+          if (i < n) red[t * kSkRedLd + rr] = sum;
+        }
       }
       src = red;
       src_ld = kSkRedLd;
@@ -235,8 +252,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       const int h_lo = r_lo / D, h_n = rows_per >= D ? rows_per / D : 1;
       for (int i = et; i < h_n * ntok; i += 128) {
         const int hl = h_lo + i / ntok, t = i % ntok;
+        float pv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (q < ks) pv[q] = ks > 1 ? dsmem_ld(dsmem_addr(&sh->psq[hl][t], (uint32_t)q)) : sh->psq[hl][t];
         float ss = 0.f;
-        for (int q = 0; q < ks; ++q) ss += ks > 1 ? dsmem_ld(dsmem_addr(&sh->psq[hl][t], (uint32_t)q)) : sh->psq[hl][t];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (q < ks) ss += pv[q];
         sh->rn[hl][t] = 1.0f / sqrtf(ss / (float)D + a.eps);
       }
       epi_bar();
