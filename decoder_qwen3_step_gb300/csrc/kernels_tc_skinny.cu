@@ -45,6 +45,53 @@ struct SkShared {
 constexpr size_t kSkSmemBytes = 1024 + (size_t)kSkStages * (kSkStageA + kSkStageB) + (size_t)kSkN * kSkLd * 4 +
                                 (size_t)kSkN * kSkRedLd * 4 + kSkN * 4 + sizeof(SkShared);
 
+__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Split-K reduction of this CTA's rows [r_lo, r_lo + rows_per) over the KS
+// partial tiles of the cluster (token-major, kSkLd apart) into red (kSkRedLd
+// apart): 4 consecutive rows of one token per 16-byte load, 16 / KS such
+// groups per thread and pass, every remote load of a pass issued before the
+// first sum; each sum runs over the ranks in order.
+template <int KS>
+__device__ __forceinline__ void sk_reduce(const float* tile, float* red, int r_lo, int rows_per, int et) {
+  constexpr int kG = 16 / KS;
+  const int g4 = rows_per / 4, n = g4 * kSkN;
+  for (int i0 = et; i0 < n; i0 += 128 * kG) {
+    float4 v[kG][KS];
+#pragma unroll
+    for (int u = 0; u < kG; ++u) {
+      const int i = i0 + u * 128, t = i / g4, rr = (i - t * g4) * 4;
+      const uint32_t loc = smem_u32(tile + t * kSkLd + r_lo + rr);
+#pragma unroll
+      for (int q = 0; q < KS; ++q) {
+        uint32_t ra;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(loc), "r"(q));
+        v[u][q] = i < n ? dsmem_ld4(ra) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kG; ++u) {
+      const int i = i0 + u * 128, t = i / g4, rr = (i - t * g4) * 4;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < KS; ++q) {
+        sum.x += v[u][q].x;
+        sum.y += v[u][q].y;
+        sum.z += v[u][q].z;
+        sum.w += v[u][q].w;
+      }
+      if (i < n) *reinterpret_cast<float4*>(red + t * kSkRedLd + rr) = sum;
+    }
+  }
+}
+
 template <typename AT, int EPI>
 __global__ void __launch_bounds__(kSkThreads, 1)
     k_gemm_tc_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, GemvArgs a,
@@ -185,29 +232,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   if (warp >= 2) {
     const int et = threadIdx.x - 64;
     if (has_rows && ks > 1) {
-      // two outputs a pass: all their remote loads in flight together, then
-      // the sums in rank order
-      constexpr int kMaxKs = 16, kU = 2;
-      const int n = rows_per * kSkN;
-      for (int i0 = et; i0 < n; i0 += 128 * kU) {
-        float v[kU][kMaxKs];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int i = i0 + u * 128, t = i / rows_per, rr = i - t * rows_per;
-          const float* p = tile + t * kSkLd + r_lo + rr;
-#pragma unroll
-          for (int q = 0; q < kMaxKs; ++q)
-            if (q < ks) v[u][q] = i < n ? dsmem_ld(dsmem_addr(p, (uint32_t)q)) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int i = i0 + u * 128, t = i / rows_per, rr = i - t * rows_per;
-          float sum = 0.f;
-#pragma unroll
-          for (int q = 0; q < kMaxKs; ++q)
-            if (q < ks) sum += v[u][q];
-          if (i < n) red[t * kSkRedLd + rr] = sum;
-        }
+      switch (ks) {  // every rank's partial of 4 rows in flight at once, summed in rank order
+        case 2: sk_reduce<2>(tile, red, r_lo, rows_per, et); break;
+        case 4: sk_reduce<4>(tile, red, r_lo, rows_per, et); break;
+        case 8: sk_reduce<8>(tile, red, r_lo, rows_per, et); break;
+        default: sk_reduce<16>(tile, red, r_lo, rows_per, et); break;
       }
       src = red;
       src_ld = kSkRedLd;
