@@ -303,7 +303,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn_decode_ring(const __gr
   // the completed pairs q, q + kRingGroups, ... in its own third of the idle
   // ring (records staged in one round trip, then the merge reads shared
   // memory; the arithmetic and its order are the same for every path).
-  __threadfence();  // the records, before the counts that publish them
+  // The records go before the counts that publish them: the CTA barrier
+  // orders every thread's records before the counting threads' atomics,
+  // which release (and acquire: the merging side reads other CTAs' records).
   __syncthreads();
   if (i0 >= i1) return;
   int* pl = flags + 2;  // [kRingPairs] (sequence, KV head, chunks here) packed, then [kRingPairs] completed
@@ -335,7 +337,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn_decode_ring(const __gr
     if ((int)threadIdx.x < np) {
       const int s = plist[3 * threadIdx.x], g = plist[3 * threadIdx.x + 1], here = plist[3 * threadIdx.x + 2];
       const int nch = (__ldg(seq_ctx + s) + kDecodeChunk - 1) / kDecodeChunk;
-      pdone[threadIdx.x] = atomicAdd(a.at.counters + s * dm.Hkv + g, here) + here == nch;
+      unsigned old;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                   : "=r"(old)
+                   : "l"(a.at.counters + s * dm.Hkv + g), "r"((unsigned)here)
+                   : "memory");
+      pdone[threadIdx.x] = (int)old + here == nch;
     }
     __syncthreads();
     i = pl[1];
@@ -350,14 +357,14 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn_decode_ring(const __gr
         if (!pdone[p]) continue;
         const int s = plist[3 * p], g = plist[3 * p + 1];
         const int nch = (__ldg(seq_ctx + s) + kDecodeChunk - 1) / kDecodeChunk;
-        __threadfence();
         const int t = __ldg(a.at.meta.seq_start + s);
         const float* base = a.at.part + ((size_t)s * dm.H + 2 * g) * a.at.nchunk_cap * (D + 2);
         const int per_head = nch * (D + 2);
         const bool staged = 2 * per_head + 2 * kChunkCap + 2 <= kPart / 4 && !*abort_flag;
         if (staged) {
           // float2 pieces (per_head / 2 a head), kU loads in flight per thread before their stores
-          constexpr int kU = 16;
+          // (one pass up to 23 chunks at D = 128, 31 below)
+          constexpr int kU = D == 128 ? 24 : 16;
           for (int x0 = ltid; x0 < per_head; x0 += 128 * kU) {
             float2 v[kU];
 #pragma unroll
