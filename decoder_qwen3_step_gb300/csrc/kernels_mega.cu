@@ -256,10 +256,8 @@ constexpr int kBarBytes = kNB * (8 + 8 + 4 + 4) + (kGroups + 1) * ((int)sizeof(I
 // passes on the phase before that.  So after the wait, the loader's claim
 // count must show tile n as claimed (its claim waited for the release of
 // tile n - kNB); if not, wait for the claim and then for the tile again.
-__device__ __forceinline__ bool tile_wait(const Smem& sm, uint32_t n, uint32_t* err) {
-  if (!mbar_wait(&sm.full[n % kNB], (n / kNB) & 1, sm.flags, err)) return false;
+__device__ __noinline__ bool tile_rewait(const Smem& sm, uint32_t n, uint32_t* err) {  // the rare path, kept out of line
   volatile int* claimed = sm.flags + 2;
-  if ((uint32_t)*claimed > n) return true;
   const uint64_t t0 = global_ns();
   while ((uint32_t)*claimed <= n) {
     if (*(volatile int*)sm.flags) return false;
@@ -270,6 +268,11 @@ __device__ __forceinline__ bool tile_wait(const Smem& sm, uint32_t n, uint32_t* 
     }
   }
   return mbar_wait(&sm.full[n % kNB], (n / kNB) & 1, sm.flags, err);
+}
+__device__ __forceinline__ bool tile_wait(const Smem& sm, uint32_t n, uint32_t* err) {
+  if (!mbar_wait(&sm.full[n % kNB], (n / kNB) & 1, sm.flags, err)) return false;
+  if ((uint32_t) * (volatile int*)(sm.flags + 2) > n) return true;
+  return tile_rewait(sm, n, err);
 }
 
 // ---------------------------------------------------------------------------
