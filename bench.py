@@ -181,6 +181,8 @@ def our_arm(args, rank, world):
     next_ids = torch.cat(first).to(torch.int32)
     torch.cuda.synchronize()
     pos = list(lens)
+    # the decode steps pass their block tables as int32 arrays (no per-step list conversion)
+    tables = [np.asarray(t, dtype=np.int32) for t in tables]
 
     V = shape["vocab"]
     logits = torch.empty((S, V), dtype=torch.float32, device=dev)
