@@ -94,6 +94,7 @@ struct RingSmem {
   static constexpr int kGroup = (kGM + 2 * 4 * 2 * 4 + 127) / 128 * 128;
   static constexpr int kGroups = kRingSlots * kSlot;
   static constexpr int kF = kGroups + kRingGroups * kGroup;   // the end-of-CTA pair list and completion flags
+                                                              // (4 x kRingPairs ints of the area used)
   static constexpr int kZ = (kF + (2 * kChunkCap + 2) * 4 + 127) / 128 * 128;  // f16 [D] zeros
   static constexpr int kBar = (kZ + D * 2 + 15) / 16 * 16;    // full[kRingSlots], empty[kRingSlots], flags
   static constexpr int kTotal = kBar + 2 * kRingSlots * 8 + 16 * 4;
