@@ -193,3 +193,24 @@ def test_one_kernel_step_wait_gives_up_and_the_gpu_stays_usable():
     check(np_(lg), np_(am), ref, "bf16", "decode after a timed-out step")
     assert m.device_status() == 0
     m.close()
+
+
+def test_long_context_decode_merges_records_without_staging():
+    """Contexts long enough that a (sequence, KV head)'s chunk records no longer
+    fit the decode attention kernel's shared-memory staging (more than 52
+    64-key chunks at head_dim 64): the merge then reads the records from
+    global memory.  Two sequences of about 3,500 tokens at the small shape,
+    decoded on the per-operation kernels (the one-kernel step off), against
+    the oracle."""
+    lens = [3400, 3530]
+    m, orc, w = make_pair("small", "bf16", max_positions=3600, max_tokens=10496, max_seqs=4,
+                          n_blocks=sum((n + 16) // 16 + 1 for n in lens) + 8)
+    m.set_megakernel(False)
+    V = inputs.SHAPES["small"]["vocab"]
+    prompts = [inputs.make_ids(V, n, seed=160 + s) for s, n in enumerate(lens)]
+    got, ids, want = decode_run(m, orc, prompts, steps=2)
+    for i in range(2):
+        check(got[i], ids[i], want[i], "bf16", f"long-context decode step {i}", case="long-context decode",
+              path=f"per-operation decode step {i}, contexts {[n + 1 + i for n in lens]}")
+    assert m.device_status() == 0
+    m.close()
