@@ -214,3 +214,20 @@ def test_long_context_decode_merges_records_without_staging():
               path=f"per-operation decode step {i}, contexts {[n + 1 + i for n in lens]}")
     assert m.device_status() == 0
     m.close()
+
+
+def test_decode_above_32_sequences_matches_the_oracle():
+    """A decode step of 40 sequences: more token rows than the skinny
+    products take, so the projections run on the many-token tcgen05 kernel,
+    and the decode attention's items span 40 x 4 (sequence, KV head) pairs of
+    different lengths (small shape, serving mode), against the oracle."""
+    S = 40
+    m, orc, w = make_pair("small", "bf16", max_positions=256, max_tokens=8192, max_seqs=S)
+    V = inputs.SHAPES["small"]["vocab"]
+    prompts = [inputs.make_ids(V, 20 + 5 * s, seed=200 + s) for s in range(S)]
+    got, ids, want = decode_run(m, orc, prompts, steps=2)
+    for i in range(2):
+        check(got[i], ids[i], want[i], "bf16", f"40-sequence decode step {i}", case="decode above 32 sequences",
+              path=f"per-operation decode step {i}, 40 sequences")
+    assert m.device_status() == 0
+    m.close()
