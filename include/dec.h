@@ -257,8 +257,10 @@ int dec_decode(dec_model* m, dec_pool* pool, const dec_batch* b, float* logits, 
  * Kernel classes of one step, in launch order. */
 #define DEC_K_EMBED       0 /* embedding gather */
 #define DEC_K_QKV         1 /* RMSNorm + [Wq;Wk;Wv] product */
-#define DEC_K_QKV_POST    2 /* QK-norm + RoPE + KV-cache write */
-#define DEC_K_ATTN        3 /* attention: split-K decode or tiled prefill */
+#define DEC_K_QKV_POST    2 /* QK-norm + RoPE + KV-cache write (parity mode; serving prefill steps of
+                               17-32 tokens; serving decode steps fuse it into DEC_K_ATTN) */
+#define DEC_K_ATTN        3 /* attention: split-K decode (serving: with QK-norm, RoPE and the
+                               cache append of the step's token fused in) or tiled prefill */
 #define DEC_K_ATTN_MERGE  4 /* reserved (the split-K merge is fused into DEC_K_ATTN) */
 #define DEC_K_OPROJ       5 /* O projection + residual */
 #define DEC_K_GATEUP      6 /* RMSNorm + gate/up + SiLU*mul */
@@ -277,7 +279,8 @@ int dec_profile_read(dec_model* m, int32_t kernel_class, double* total_ms, int64
  * default); off routes them to the CUDA-core kernels. */
 int dec_set_tensor_cores(dec_model* m, int32_t on);
 /* Decode steps replay CUDA graphs (on by default): the first step of a given
- * (batch size, logits, argmax, pool) runs eagerly, the second is captured on
+ * (batch size, logits, argmax, pool and its size; in the parity mode also the
+ * decode attention grid, which grows every 256 positions) runs eagerly, the second is captured on
  * a private stream, later ones replay it on the caller's stream.  Off: every
  * step launches its kernels one by one.  Graphs are bypassed while a dump is
  * active.  Profiled kernel classes (dec_profile_enable) stay timed inside
