@@ -161,3 +161,23 @@ def test_release_build_has_no_debug_hooks(L):
     assert L.dec_debug_poison_table(None, 0, 0, 0) == dec.DEC_EINVAL
     assert "-DDEC_DEBUG" in build._flags(debug=True) and "-DDEC_DEBUG" not in build._flags()
     assert build.LIB_DEBUG != build.LIB and build.BUILD_DEBUG != build.BUILD
+
+
+def test_debug_build_compiles_and_reports_its_flag():
+    """The DEC_DEBUG build (device bounds checks behind #ifdef) compiles for
+    sm_103a and exports the same symbols; loaded in a child process it reports
+    DEC_BUILD_DEBUG.  No device work runs."""
+    import subprocess
+    import sys
+
+    from decoder_qwen3_step_gb300 import build
+
+    lib = build.build(debug=True)
+    assert os.path.exists(lib) and lib.endswith("libdec_debug.so")
+    code = ("from decoder_qwen3_step_gb300 import dec; L = dec.lib(); "
+            "assert dec.LIB_PATH.endswith('libdec_debug.so'); "
+            "assert L.dec_build_flags() == dec.DEC_BUILD_DEBUG; "
+            "assert all(hasattr(L, n) for n in dec.EXPORTS); print('ok')")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env={**os.environ, "DEC_DEBUG": "1"},
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stderr[-2000:]
