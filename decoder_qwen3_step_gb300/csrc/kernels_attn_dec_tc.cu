@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn_decode_ring(const __gr
   extern __shared__ __align__(1024) uint8_t dsm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm + SM::kBar);
   uint64_t* empty = full + kRingSlots;
-  int* flags = reinterpret_cast<int*>(empty + kRingSlots);  // [0] abort, [1] merge this pair
+  int* flags = reinterpret_cast<int*>(empty + kRingSlots);  // [0] abort, [2..7] the end-of-CTA pair list header
   __half* zrow = reinterpret_cast<__half*>(dsm + SM::kZ);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.at.S, P = gridDim.x, b = blockIdx.x;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn_decode_ring(const __gr
     }
     if (!waited) pdl_wait_prev();
   } else {
-    // ---- consumers: group gq takes the CTA's items gq, gq + 2, ... ----
+    // ---- consumers: group gq takes the CTA's items gq, gq + kRingGroups, ... ----
     pdl_wait_prev();  // the raw q|k|v rows are the previous kernel's
     const int gq = warp >> 2, gw = warp & 3, ltid = threadIdx.x & 127;
     uint8_t* G = dsm + SM::kGroups + gq * SM::kGroup;
